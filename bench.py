@@ -1,0 +1,403 @@
+#!/usr/bin/env python3
+"""Benchmark of the truncated-Taylor fixed-state attention hot path on B300.
+
+One JSON line on rank 0. The headline `value` is prefill tokens/s on the
+8,192-token workload (B=1, H=8, N=8192, d_k=16, d_v=64, n=3, fp32): one step is
+one tsa_prefill call over that batch (feature map, chunk-state contraction,
+span scan, inter-chunk readout, intra-chunk attention, normalise and store).
+The same line carries the decode workload (B=64, H=16, d_k=16, d_v=64, n=3,
+bf16 inputs, fp32 states prefilled with 65,536 tokens): microseconds per
+decode step and state GB/s, and the state merge.
+
+Timing: CUDA events on the launching stream; between timed prefill steps the
+L2 is flushed by writing a buffer larger than L2 (outside the events). Decode
+steps rotate over 8 independent state sets (8 x 41.5 MB > L2), captured in a
+CUDA graph, so every step streams its state from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "prefill tokens/s at N=8192 (n=3); decode µs/token and state GB/s on 1 B300"
+PREFILL = dict(workload="prefill_B1_H8_N8192", B=1, H=8, N=8192, d_k=16, d_v=64, n_terms=3, dtype="f32", seed=2)
+DECODE = dict(workload="decode_B64_H16_N65536", B=64, H=16, N=65536, d_k=16, d_v=64, n_terms=3, dtype="bf16", seed=3)
+L2_FLUSH_BYTES = 256 << 20
+DECODE_ROTATE = 8
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _algorithmic_prefill_bytes(w) -> int:
+    """q, k, v read + out written (element size of the dtype) + final states
+    written (fp32, D*(d_v+1) per head)."""
+    es = 4 if w["dtype"] == "f32" else 2
+    heads = w["B"] * w["H"]
+    D = sum(__import__("math").comb(w["d_k"] + m - 1, m) for m in range(w["n_terms"]))
+    io = heads * w["N"] * (2 * w["d_k"] + 2 * w["d_v"]) * es
+    return io + heads * D * (w["d_v"] + 1) * 4
+
+
+def _algorithmic_decode_bytes(w) -> int:
+    """State read + written once per step (D*(d_v+1) fp32 per head; padding not
+    counted) plus the step's q, k, v in and out."""
+    es = 4 if w["dtype"] == "f32" else 2
+    heads = w["B"] * w["H"]
+    D = sum(__import__("math").comb(w["d_k"] + m - 1, m) for m in range(w["n_terms"]))
+    return heads * (2 * D * (w["d_v"] + 1) * 4 + (2 * w["d_k"] + 2 * w["d_v"]) * es)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed work runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "20"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        if self.p is not None:
+            time.sleep(0.1)
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except Exception:
+                self.p.kill()
+
+    def summary(self):
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1])); mx = max(mx, float(r[2]))
+                for nm, val in zip(names, r[5:9]):
+                    if "Active" in val and "Not" not in val:
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline_prefill(w, max_heads=None):
+    """The float64 oracle (recurrent form, as it stands) on host cores."""
+    from fixed_state_recurrence_phi_b300.inputs import np_qkv
+    from oracle import tsa_oracle as O
+    heads = w["B"] * w["H"] if max_heads is None else max_heads
+    t = 0.0
+    for h in range(heads):
+        q, k, v = np_qkv(w["N"], w["d_k"], w["d_v"], seed=[w["seed"], h])
+        t0 = time.perf_counter()
+        O.prefill_recurrent(q, k, v, w["n_terms"])
+        t += time.perf_counter() - t0
+    per_head = t / heads
+    all_heads = w["B"] * w["H"]
+    return {"value": w["B"] * w["N"] / (per_head * all_heads), "unit": "tokens/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"recurrent float64 prefill, {heads} of {all_heads} heads x {w['N']} tokens on 1 "
+                      f"core; tokens/s = B*N / (mean head time x {all_heads} heads)"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    w = PREFILL
+    times = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline_prefill(w, max_heads=1)
+        if i >= args.warmup:
+            times.append(w["B"] * w["N"] / r["value"])
+    t = statistics.mean(times)
+    value = w["B"] * w["N"] / t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w["workload"], "B": w["B"], "H": w["H"], "N": w["N"], "d_k": w["d_k"],
+                   "d_v": w["d_v"], "n_terms": w["n_terms"], "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "each step: recurrent float64 prefill of 1 of 8 heads x 8192 tokens "
+                                   "on 1 host core; tokens/s scaled by the 8 heads"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    from fixed_state_recurrence_phi_b300 import build as tsa_build
+    tsa_build.build()
+    from fixed_state_recurrence_phi_b300 import tsa as T
+    from fixed_state_recurrence_phi_b300.inputs import torch_qkv
+
+    hbm_peak, peak_src = _peaks()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if ws == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---------------- prefill workload (weak scaling: one batch per rank) ----
+    w = PREFILL
+    cfg = T.Config(w["B"], w["H"], w["d_k"], w["d_v"], w["n_terms"], w["dtype"])
+    q, k, v = torch_qkv(w["B"], w["H"], w["N"], w["d_k"], w["d_v"], w["dtype"], w["seed"] + 1000 * rank,
+                        0, dev)
+    out = torch.empty((w["B"], w["H"], w["N"], w["d_v"]), dtype=q.dtype, device=dev)
+    st = T.new_states(cfg, dev)
+    plan = T.prefill_plan(cfg, w["N"])
+
+    def prefill_step():
+        T.prefill(cfg, w["N"], q, k, v, out, st, stream=stream)
+
+    gpu = torch.cuda.current_device()
+    with ClockSampler(gpu) as clk:
+        for _ in range(max(3, args.warmup)):
+            flush.fill_(1.0)
+            prefill_step()
+        barrier()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            evs[i][0].record(stream)
+            prefill_step()
+            evs[i][1].record(stream)
+        barrier()
+        step_ms = [a.elapsed_time(b) for a, b in evs]
+        ms = max_over_ranks(statistics.mean(step_ms))
+
+        # -------- e2e: pinned host buffers in, host result out, through the ABI
+        qh = q.cpu().pin_memory(); kh = k.cpu().pin_memory(); vh = v.cpu().pin_memory()
+        oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        sh = torch.empty(st.shape, dtype=st.dtype).pin_memory()
+        qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            qd.copy_(qh, non_blocking=True); kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            T.prefill(cfg, w["N"], qd, kd, vd, out, st, stream=stream)
+            oh.copy_(out, non_blocking=True); sh.copy_(st, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        barrier()
+        e_ms = []
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream); e2e_step(); b.record(stream)
+            e_ms.append((a, b))
+        barrier()
+        e2e_ms = max_over_ranks(statistics.mean([a.elapsed_time(b) for a, b in e_ms]))
+        h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
+        d2h = oh.numel() * oh.element_size() + sh.numel() * sh.element_size()
+        del qh, kh, vh, oh, sh, qd, kd, vd
+
+        # ---------------- decode workload ----------------------------------
+        dw = DECODE
+        dcfg = T.Config(dw["B"], dw["H"], dw["d_k"], dw["d_v"], dw["n_terms"], dw["dtype"])
+        dstates = []
+        dq, dk, dv = torch_qkv(dw["B"], dw["H"], dw["N"], dw["d_k"], dw["d_v"], dw["dtype"],
+                               dw["seed"] + 1000 * rank, 0, dev)
+        dout = torch.empty((dw["B"], dw["H"], dw["N"], dw["d_v"]), dtype=dq.dtype, device=dev)
+        s0 = T.new_states(dcfg, dev)
+        pa, pb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        pa.record(stream)
+        T.prefill(dcfg, dw["N"], dq, dk, dv, dout, s0, stream=stream)
+        pb.record(stream)
+        torch.cuda.synchronize()
+        long_prefill_ms = pa.elapsed_time(pb)
+        del dq, dk, dv, dout
+        torch.cuda.empty_cache()
+        for _ in range(DECODE_ROTATE):
+            dstates.append(s0.clone())
+        steps = 1024
+        tq, tk, tv = torch_qkv(dw["B"], dw["H"], steps, dw["d_k"], dw["d_v"], dw["dtype"],
+                               dw["seed"] + 1000 * rank, 1, dev)
+        tq = tq.permute(2, 0, 1, 3).contiguous(); tk = tk.permute(2, 0, 1, 3).contiguous()
+        tv = tv.permute(2, 0, 1, 3).contiguous()
+        touts = torch.empty((steps, dw["B"], dw["H"], dw["d_v"]), dtype=tq.dtype, device=dev)
+
+        def decode_all(s):
+            for t in range(steps):
+                T.decode_step(dcfg, tq[t], tk[t], tv[t], touts[t], dstates[t % DECODE_ROTATE], stream=s)
+
+        # eager, per-step events (first 64 steps, L2 rotation as in the graph)
+        decode_all(stream)
+        barrier()
+        eager = []
+        for t in range(64):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            T.decode_step(dcfg, tq[t], tk[t], tv[t], touts[t], dstates[t % DECODE_ROTATE], stream=stream)
+            b.record(stream)
+            eager.append((a, b))
+        barrier()
+        eager_us = statistics.median([a.elapsed_time(b) * 1e3 for a, b in eager])
+        # graph of 1024 steps
+        gs = torch.cuda.Stream()
+        gs.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gs):
+            with torch.cuda.graph(g, stream=gs):
+                decode_all(gs)
+        stream.wait_stream(gs)
+        g.replay(); barrier()
+        reps = 3
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        barrier()
+        dec_us = max_over_ranks(a.elapsed_time(b) * 1e3 / (reps * steps))
+
+        # ---------------- merge -------------------------------------------
+        m_ms = []
+        for i in range(10):
+            flush.fill_(float(i))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream); T.state_merge(dcfg, dstates[0], dstates[1], stream=stream); b.record(stream)
+            m_ms.append((a, b))
+        barrier()
+        merge_ms = statistics.median([a.elapsed_time(b) for a, b in m_ms])
+    clocks = clk.summary()
+
+    # ---------------- report -------------------------------------------------
+    tokens = w["B"] * w["N"]
+    value = ws * tokens / (ms / 1e3)
+    pre_bytes = _algorithmic_prefill_bytes(w)
+    dec_bytes = _algorithmic_decode_bytes(dw)
+    state_bytes_step = dw["B"] * dw["H"] * T.state_elems(dcfg) * 4 * 2
+    ach = pre_bytes / (ms / 1e3) / 1e9
+    if rank != 0:
+        return
+    cpu = cpu_baseline_prefill(w) if (ws == 1 and not args.no_cpu_baseline) else None
+    traffic = _profile_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w["workload"], "B": w["B"], "H": w["H"], "N": w["N"], "d_k": w["d_k"],
+                   "d_v": w["d_v"], "n_terms": w["n_terms"], "chunk": plan["chunk"],
+                   "n_spans": plan["n_spans"], "l2": "flushed between timed steps (256 MB write)"},
+        "roofline": {"bound": "hbm", "kernel": "tsa_prefill (all launches of the call)",
+                     "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
+                     "peak_source": f"{peak_src} (copy bandwidth)",
+                     "algorithmic_bytes": pre_bytes,
+                     "traffic": traffic.get("prefill")},
+        "e2e": {"value": ws * tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * plan["launches"],
+        "decode": {"workload": dw["workload"], "us_per_step": dec_us, "us_per_step_eager": eager_us,
+                   "us_per_token_per_sequence": dec_us / dw["B"],
+                   "state_GBps": state_bytes_step / (dec_us / 1e6) / 1e9,
+                   "roofline": {"bound": "hbm", "kernel": "decode_kernel",
+                                "achieved": dec_bytes / (dec_us / 1e6) / 1e9, "peak": hbm_peak,
+                                "unit": "GB/s", "frac": dec_bytes / (dec_us / 1e6) / 1e9 / hbm_peak,
+                                "algorithmic_bytes": dec_bytes, "traffic": traffic.get("decode")},
+                   "timing": f"CUDA graph of {steps} steps x {reps}, states rotated over "
+                             f"{DECODE_ROTATE} sets (> L2)",
+                   "gpu_launches": reps * steps,
+                   "prefill_N65536_ms": long_prefill_ms},
+        "merge": {"workload": dw["workload"], "ms": merge_ms,
+                  "GBps": 3 * T.state_bytes(dcfg) / (merge_ms / 1e3) / 1e9},
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _profile_traffic():
+    """DRAM traffic per launch from the committed ncu summary, if present and
+    current (profiles/traffic.json, written from a capture of this build)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            return json.load(f)
+    except Exception:
+        return {}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,410 @@
+// tsa_abi.cu -- host side of libtsa.so: argument validation, planning, scratch
+// from a library-owned stream-ordered memory pool, and kernel dispatch.
+// The C declarations and their contracts are in include/tsa.h.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/tsa.h"
+#include "tsa_internal.h"
+#include "common.cuh"
+#include "prefill_simt.cuh"
+#include "decode.cuh"
+
+namespace tsa {
+
+static thread_local std::string g_last_error;
+
+tsa_status fail(tsa_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+tsa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(TSA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape check shared by every call. Returns TSA_OK or the error.
+tsa_status check_config(const tsa_config* c) {
+  if (!c) return fail(TSA_ERR_INVALID, "config is NULL");
+  if (c->B < 1 || c->H < 1) return fail(TSA_ERR_INVALID, "B and H must be >= 1 (got %d, %d)", c->B, c->H);
+  if ((long long)c->B * c->H > (1LL << 30)) return fail(TSA_ERR_INVALID, "B*H too large");
+  if (c->d_k < 1 || c->d_v < 1 || c->n_terms < 1)
+    return fail(TSA_ERR_INVALID, "d_k, d_v and n_terms must be >= 1");
+  if (c->dtype != TSA_F32 && c->dtype != TSA_BF16) return fail(TSA_ERR_INVALID, "unknown dtype %d", (int)c->dtype);
+  if (c->chunk < 0) return fail(TSA_ERR_INVALID, "chunk must be >= 0");
+  if (c->d_k != 16 && c->d_k != 32) return fail(TSA_ERR_UNSUPPORTED, "d_k=%d not built (16, 32)", c->d_k);
+  if (c->d_v != 32 && c->d_v != 64 && c->d_v != 128)
+    return fail(TSA_ERR_UNSUPPORTED, "d_v=%d not built (32, 64, 128)", c->d_v);
+  if (c->n_terms > 4) return fail(TSA_ERR_UNSUPPORTED, "n_terms=%d not built (1..4)", c->n_terms);
+  if (feat_dim(c->d_k, c->n_terms) > 1024)
+    return fail(TSA_ERR_UNSUPPORTED, "feature dim %d > 1024 (d_k=%d, n=%d)",
+                feat_dim(c->d_k, c->n_terms), c->d_k, c->n_terms);
+  return TSA_OK;
+}
+
+size_t state_floats_per_head(const tsa_config* c) {
+  return (size_t)round_up(feat_dim(c->d_k, c->n_terms), 4) * (size_t)(c->d_v + 1);
+}
+
+// ---------------------------------------------------------------------------
+// Scratch: one stream-ordered pool per device, kept warm (release threshold at
+// max) so steady-state calls do not reach the driver.
+// ---------------------------------------------------------------------------
+static std::mutex g_pool_mu;
+static cudaMemPool_t g_pools[64];
+static bool g_pool_ok[64];
+
+tsa_status scratch_alloc(void** p, size_t bytes, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(TSA_ERR_CUDA, "device index %d out of range", dev);
+  {
+    std::lock_guard<std::mutex> lk(g_pool_mu);
+    if (!g_pool_ok[dev]) {
+      cudaMemPoolProps props;
+      memset(&props, 0, sizeof(props));
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      e = cudaMemPoolCreate(&g_pools[dev], &props);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+      uint64_t thr = ~0ull;
+      e = cudaMemPoolSetAttribute(g_pools[dev], cudaMemPoolAttrReleaseThreshold, &thr);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolSetAttribute");
+      g_pool_ok[dev] = true;
+    }
+  }
+  e = cudaMallocFromPoolAsync(p, bytes, g_pools[dev], s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync");
+  return TSA_OK;
+}
+
+tsa_status scratch_free(void* p, cudaStream_t s) {
+  cudaError_t e = cudaFreeAsync(p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync");
+  return TSA_OK;
+}
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// ---------------------------------------------------------------------------
+// Planning (host only; exported through tsa_prefill_plan for inspection).
+// ---------------------------------------------------------------------------
+static size_t simt_smem_bytes(int dk, int nt, int W) {
+#define TSA_SMEM_CASE(DK, NT)                                              \
+  if (dk == DK && nt == NT)                                                \
+    return W == 64 ? SimtLayout<DK, NT, 64>::bytes : SimtLayout<DK, NT, 32>::bytes;
+  TSA_SMEM_CASE(16, 1) TSA_SMEM_CASE(16, 2) TSA_SMEM_CASE(16, 3) TSA_SMEM_CASE(16, 4)
+  TSA_SMEM_CASE(32, 1) TSA_SMEM_CASE(32, 2) TSA_SMEM_CASE(32, 3)
+#undef TSA_SMEM_CASE
+  return 0;
+}
+
+static constexpr size_t kSmemLimit = 227 * 1024;
+static constexpr size_t kSmemPerSm = 228 * 1024;
+
+tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl) {
+  memset(pl, 0, sizeof(*pl));
+  const int chunk = 64;
+  if (c->chunk != 0 && c->chunk != chunk)
+    return fail(TSA_ERR_UNSUPPORTED, "chunk=%d not built (0 or 64)", c->chunk);
+  int W = (c->d_v % 64 == 0 && simt_smem_bytes(c->d_k, c->n_terms, 64) <= kSmemLimit) ? 64 : 32;
+  const size_t smem = simt_smem_bytes(c->d_k, c->n_terms, W);
+  if (smem == 0 || smem > kSmemLimit) return fail(TSA_ERR_UNSUPPORTED, "no kernel fits shared memory");
+  const int occ = std::max(1, std::min(2, (int)(kSmemPerSm / (smem + 1024))));
+  const long long heads = (long long)c->B * c->H;
+  const int n_slices = c->d_v / W;
+  const long long n_chunks = (N + chunk - 1) / chunk;
+  const long long units = heads * n_slices;
+  const long long slots = (long long)std::max(1, num_sms) * occ;
+  int best_s = 1;
+  double best_cost = 1e300;
+  const long long s_max = std::min<long long>(n_chunks, 1024);
+  for (long long s = 1; s <= std::max<long long>(1, s_max); ++s) {
+    const long long cps = (n_chunks + s - 1) / s;
+    const long long s_eff = cps > 0 ? (n_chunks + cps - 1) / cps : 1;
+    if (s_eff != s) continue;
+    const long long waves = (units * s_eff + slots - 1) / slots;
+    // span_state costs about 0.45 of a span_output chunk; the scan and the
+    // two extra launches about one chunk.
+    const double cost = (double)waves * cps * (s_eff > 1 ? 1.45 : 1.0) + (s_eff > 1 ? 1.0 : 0.0);
+    if (cost < best_cost - 1e-9) { best_cost = cost; best_s = (int)s_eff; }
+  }
+  pl->chunk = chunk;
+  pl->slice_width = W;
+  pl->n_slices = n_slices;
+  pl->n_spans = best_s;
+  pl->chunks_per_span = n_chunks > 0 ? (int)((n_chunks + best_s - 1) / best_s) : 0;
+  pl->smem_bytes = smem;
+  pl->ctas_per_sm = occ;
+  pl->scratch_bytes = best_s > 1 ? (size_t)heads * best_s * state_floats_per_head(c) * 4 : 0;
+  pl->launches = best_s > 1 ? 3 : 1;
+  return TSA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Dispatch
+// ---------------------------------------------------------------------------
+template <typename T, int DK, int NT, int W>
+static tsa_status launch_prefill_simt(const tsa_plan& pl, PrefillParams p, cudaStream_t s) {
+  using L = SimtLayout<DK, NT, W>;
+  const unsigned grid = (unsigned)((long long)p.heads * pl.n_slices * pl.n_spans);
+  cudaError_t e;
+  if (pl.n_spans > 1) {
+    e = cudaFuncSetAttribute(span_state_kernel<T, DK, NT, W>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_state)");
+    span_state_kernel<T, DK, NT, W><<<grid, 256, L::bytes, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch span_state");
+    const int elems4 = (int)(L::DPAD * (p.dv + 1) / 4);
+    dim3 g2((elems4 + 255) / 256, p.heads);
+    span_scan_kernel<<<g2, 256, 0, s>>>(p.states, p.scratch, p.heads, pl.n_spans, elems4, p.accumulate);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch span_scan");
+  }
+  e = cudaFuncSetAttribute(span_output_kernel<T, DK, NT, W>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_output)");
+  span_output_kernel<T, DK, NT, W><<<grid, 256, L::bytes, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch span_output");
+  return TSA_OK;
+}
+
+template <typename T, int DK, int NT>
+static tsa_status dispatch_prefill_w(const tsa_plan& pl, PrefillParams p, cudaStream_t s) {
+  if (pl.slice_width == 64) return launch_prefill_simt<T, DK, NT, 64>(pl, p, s);
+  return launch_prefill_simt<T, DK, NT, 32>(pl, p, s);
+}
+
+template <typename T>
+static tsa_status dispatch_prefill(const tsa_config* c, const tsa_plan& pl, PrefillParams p,
+                                   cudaStream_t s) {
+#define TSA_PF_CASE(DK, NT) \
+  if (c->d_k == DK && c->n_terms == NT) return dispatch_prefill_w<T, DK, NT>(pl, p, s);
+  TSA_PF_CASE(16, 1) TSA_PF_CASE(16, 2) TSA_PF_CASE(16, 3) TSA_PF_CASE(16, 4)
+  TSA_PF_CASE(32, 1) TSA_PF_CASE(32, 2) TSA_PF_CASE(32, 3)
+#undef TSA_PF_CASE
+  return fail(TSA_ERR_UNSUPPORTED, "no prefill kernel for d_k=%d n=%d", c->d_k, c->n_terms);
+}
+
+template <typename T, int DK, int NT>
+static tsa_status dispatch_decode_dv(int dv, DecodeParams p, cudaStream_t s) {
+  const unsigned grid = (unsigned)p.heads;
+  switch (dv) {
+    case 32: decode_kernel<T, DK, NT, 32><<<grid, 256, 0, s>>>(p); break;
+    case 64: decode_kernel<T, DK, NT, 64><<<grid, 256, 0, s>>>(p); break;
+    case 128: decode_kernel<T, DK, NT, 128><<<grid, 256, 0, s>>>(p); break;
+    default: return fail(TSA_ERR_UNSUPPORTED, "d_v=%d", dv);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch decode");
+  return TSA_OK;
+}
+
+template <typename T>
+static tsa_status dispatch_decode(const tsa_config* c, DecodeParams p, cudaStream_t s) {
+#define TSA_DC_CASE(DK, NT) \
+  if (c->d_k == DK && c->n_terms == NT) return dispatch_decode_dv<T, DK, NT>(c->d_v, p, s);
+  TSA_DC_CASE(16, 1) TSA_DC_CASE(16, 2) TSA_DC_CASE(16, 3) TSA_DC_CASE(16, 4)
+  TSA_DC_CASE(32, 1) TSA_DC_CASE(32, 2) TSA_DC_CASE(32, 3)
+#undef TSA_DC_CASE
+  return fail(TSA_ERR_UNSUPPORTED, "no decode kernel for d_k=%d n=%d", c->d_k, c->n_terms);
+}
+
+static unsigned grid_for(size_t n, unsigned per_block = 256) {
+  const size_t b = (n + per_block - 1) / per_block;
+  return (unsigned)std::max<size_t>(1, std::min<size_t>(b, 148u * 16u));
+}
+
+}  // namespace tsa
+
+using namespace tsa;
+
+extern "C" {
+
+size_t tsa_feature_dim(int d_k, int n_terms) {
+  if (d_k < 1 || n_terms < 1 || d_k > 4096 || n_terms > 16) return 0;
+  return (size_t)feat_dim(d_k, n_terms);
+}
+
+size_t tsa_state_pad_dim(int d_k, int n_terms) {
+  const size_t D = tsa_feature_dim(d_k, n_terms);
+  return (D + 3) / 4 * 4;
+}
+
+size_t tsa_state_elems(const tsa_config* c) {
+  if (!c) return 0;
+  return tsa_feature_dim(c->d_k, c->n_terms) * (size_t)(c->d_v + 1);
+}
+
+size_t tsa_state_bytes(const tsa_config* c) {
+  if (!c || c->B < 1 || c->H < 1 || c->d_v < 1) return 0;
+  return (size_t)c->B * c->H * tsa_state_pad_dim(c->d_k, c->n_terms) * (size_t)(c->d_v + 1) * 4;
+}
+
+tsa_status tsa_feature_index(int d_k, int n_terms, int* idx, float* weight) {
+  if (!idx || !weight) return fail(TSA_ERR_INVALID, "NULL output");
+  if (d_k < 1 || n_terms < 1) return fail(TSA_ERR_INVALID, "d_k and n_terms must be >= 1");
+#define TSA_FI_CASE(DK, NT)                                                  \
+  if (d_k == DK && n_terms == NT) {                                          \
+    constexpr FeatTab<DK, NT> t = make_feat_tab<DK, NT>();                   \
+    for (int a = 0; a < FeatTab<DK, NT>::D; ++a) {                           \
+      for (int f = 0; f < 3; ++f) {                                          \
+        const int i = (int)((t.code[a] >> (8 * f)) & 255u);                  \
+        idx[3 * a + f] = (i == DK) ? -1 : i;                                 \
+      }                                                                      \
+      weight[a] = t.w[a];                                                    \
+    }                                                                        \
+    return TSA_OK;                                                           \
+  }
+  TSA_FI_CASE(16, 1) TSA_FI_CASE(16, 2) TSA_FI_CASE(16, 3) TSA_FI_CASE(16, 4)
+  TSA_FI_CASE(32, 1) TSA_FI_CASE(32, 2) TSA_FI_CASE(32, 3)
+#undef TSA_FI_CASE
+  return fail(TSA_ERR_UNSUPPORTED, "no feature table for d_k=%d n=%d", d_k, n_terms);
+}
+
+tsa_status tsa_prefill_plan(const tsa_config* c, int64_t N, int num_sms, tsa_plan* out) {
+  if (!out) return fail(TSA_ERR_INVALID, "plan output is NULL");
+  tsa_status st = check_config(c);
+  if (st != TSA_OK) return st;
+  if (N < 0) return fail(TSA_ERR_INVALID, "N must be >= 0");
+  if (num_sms <= 0) {
+    num_sms = device_sm_count();
+    if (num_sms <= 0) return fail(TSA_ERR_CUDA, "no CUDA device to size the plan");
+  }
+  return make_plan(c, (long long)N, num_sms, out);
+}
+
+tsa_status tsa_prefill(const tsa_config* c, int64_t N, const void* q, const void* k, const void* v,
+                       void* out, float* states, unsigned flags, void* stream) {
+  tsa_status st = check_config(c);
+  if (st != TSA_OK) return st;
+  if (N < 0) return fail(TSA_ERR_INVALID, "N must be >= 0 (got %lld)", (long long)N);
+  if (flags & ~TSA_PREFILL_ACCUMULATE) return fail(TSA_ERR_INVALID, "unknown flags 0x%x", flags);
+  if (!states) return fail(TSA_ERR_INVALID, "states is NULL");
+  if (!aligned16(states)) return fail(TSA_ERR_INVALID, "states not 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool acc = (flags & TSA_PREFILL_ACCUMULATE) != 0;
+  if (N == 0) {
+    if (!acc) {
+      cudaError_t e = cudaMemsetAsync(states, 0, tsa_state_bytes(c), s);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(states)");
+    }
+    return TSA_OK;
+  }
+  if (!q || !k || !v || !out) return fail(TSA_ERR_INVALID, "q, k, v and out must be non-NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(TSA_ERR_INVALID, "q, k, v and out must be 16-byte aligned");
+  tsa_plan pl;
+  const int sms = device_sm_count();
+  if (sms <= 0) return fail(TSA_ERR_CUDA, "no CUDA device");
+  st = make_plan(c, (long long)N, sms, &pl);
+  if (st != TSA_OK) return st;
+
+  PrefillParams p;
+  p.q = q; p.k = k; p.v = v; p.out = out; p.states = states; p.scratch = nullptr;
+  p.N = N; p.heads = c->B * c->H; p.dv = c->d_v; p.n_slices = pl.n_slices;
+  p.n_spans = pl.n_spans; p.chunks_per_span = pl.chunks_per_span; p.accumulate = acc ? 1 : 0;
+  void* scratch = nullptr;
+  if (pl.scratch_bytes) {
+    st = scratch_alloc(&scratch, pl.scratch_bytes, s);
+    if (st != TSA_OK) return st;
+    p.scratch = static_cast<float*>(scratch);
+  }
+  st = (c->dtype == TSA_F32) ? dispatch_prefill<float>(c, pl, p, s)
+                             : dispatch_prefill<__nv_bfloat16>(c, pl, p, s);
+  if (scratch) {
+    tsa_status st2 = scratch_free(scratch, s);
+    if (st == TSA_OK) st = st2;
+  }
+  return st;
+}
+
+tsa_status tsa_decode_step(const tsa_config* c, const void* q, const void* k, const void* v,
+                           void* out, float* states, void* stream) {
+  tsa_status st = check_config(c);
+  if (st != TSA_OK) return st;
+  if (!q || !k || !v || !out || !states) return fail(TSA_ERR_INVALID, "NULL pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(states))
+    return fail(TSA_ERR_INVALID, "pointers must be 16-byte aligned");
+  DecodeParams p;
+  p.q = q; p.k = k; p.v = v; p.out = out; p.states = states; p.heads = c->B * c->H;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return (c->dtype == TSA_F32) ? dispatch_decode<float>(c, p, s)
+                               : dispatch_decode<__nv_bfloat16>(c, p, s);
+}
+
+tsa_status tsa_state_merge(const tsa_config* c, float* a, const float* b, void* stream) {
+  tsa_status st = check_config(c);
+  if (st != TSA_OK) return st;
+  if (!a || !b) return fail(TSA_ERR_INVALID, "NULL state pointer");
+  if (!aligned16(a) || !aligned16(b)) return fail(TSA_ERR_INVALID, "states must be 16-byte aligned");
+  const size_t n4 = tsa_state_bytes(c) / 16;
+  const char* pa = reinterpret_cast<const char*>(a);
+  const char* pb = reinterpret_cast<const char*>(b);
+  const size_t nb = n4 * 16;
+  if (pa != pb && pa < pb + nb && pb < pa + nb)
+    return fail(TSA_ERR_INVALID, "a and b overlap partially");
+  state_merge_kernel<<<grid_for(n4), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<float4*>(a), reinterpret_cast<const float4*>(b), n4);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch state_merge");
+  return TSA_OK;
+}
+
+tsa_status tsa_state_to_canonical(const tsa_config* c, const float* states, float* dst, void* stream) {
+  tsa_status st = check_config(c);
+  if (st != TSA_OK) return st;
+  if (!states || !dst) return fail(TSA_ERR_INVALID, "NULL pointer");
+  const int D = feat_dim(c->d_k, c->n_terms);
+  const int heads = c->B * c->H;
+  const size_t total = (size_t)heads * D * (c->d_v + 1);
+  state_canonical_kernel<<<grid_for(total), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      states, dst, heads, D, round_up(D, 4), c->d_v);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch state_canonical");
+  return TSA_OK;
+}
+
+tsa_status tsa_sync_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  return TSA_OK;
+}
+
+const char* tsa_status_string(tsa_status s) {
+  switch (s) {
+    case TSA_OK: return "TSA_OK";
+    case TSA_ERR_INVALID: return "TSA_ERR_INVALID";
+    case TSA_ERR_UNSUPPORTED: return "TSA_ERR_UNSUPPORTED";
+    case TSA_ERR_CUDA: return "TSA_ERR_CUDA";
+    case TSA_ERR_TIMEOUT: return "TSA_ERR_TIMEOUT";
+  }
+  return "TSA_UNKNOWN_STATUS";
+}
+
+const char* tsa_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,12 @@
+// tsa_internal.h -- host helpers shared by the translation units of libtsa.so.
+#pragma once
+#include <cuda_runtime.h>
+#include "../../include/tsa.h"
+
+namespace tsa {
+tsa_status fail(tsa_status s, const char* fmt, ...);
+tsa_status cuda_fail(cudaError_t e, const char* what);
+tsa_status check_config(const tsa_config* c);
+size_t state_floats_per_head(const tsa_config* c);
+int device_sm_count();
+}  // namespace tsa

@@ -1,0 +1,160 @@
+/*
+ * tsa.h -- C ABI of libtsa.so: truncated-Taylor, fixed-state causal attention
+ * on one NVIDIA B300 (sm_103a).
+ *
+ * The method (source pages, cited by title and section):
+ *   "Expanding Attention: A Taylor-Series Route to Linear-Time Transformers
+ *    with a Fixed Number of Recurrent States" (wpnews.pro), arXiv 2610.20637v1
+ *   abstract; "arXiv Introduces New Linear-Time Transformer Method via Taylor
+ *   Series Expansion and Fixed-State Recurrence" (zicq.com), sections
+ *   "Technical Mechanism Analysis" and "Engineering Trade-offs and
+ *   Performance"; the Hacker News thread on the paper (item 46888355), the
+ *   comments on the "+1" normaliser column and on (Q'K)V = Q'(KV).
+ *
+ * Per head, with T_n(x) = sum_{m<n} x^m/m! (the first n Taylor terms of exp):
+ *     out_i = sum_{j<=i} T_n(q_i.k_j) v_j / sum_{j<=i} T_n(q_i.k_j)
+ * computed through the symmetric tensor-power features
+ *     phi(x) = [phi_0(x) | ... | phi_{n-1}(x)],  phi_m(x)_a = x^a / sqrt(a!)
+ * (multi-indices |a| = m in non-decreasing index order, width C(d+m-1, m),
+ * so <phi_m(q), phi_m(k)> = (q.k)^m / m!) and the fixed state
+ *     S = sum_j phi(k_j) [v_j; 1]^T        (D rows, d_v + 1 columns)
+ * whose last column z = sum_j phi(k_j) is the normaliser.
+ *
+ * Conventions for every call:
+ *  - All pointers are DEVICE pointers on the current CUDA device, owned by the
+ *    caller; the library never frees them. Calls are asynchronous on the given
+ *    stream (a cudaStream_t passed as void*; NULL = legacy default stream).
+ *  - A tsa_status reports argument validation and launch errors only; a fault
+ *    inside a kernel surfaces at the caller's next synchronisation (or
+ *    tsa_sync_status). Nothing is thrown across the ABI. tsa_last_error()
+ *    gives a message for the calling thread's last non-OK status.
+ *  - Preconditions the library does NOT enforce: q and k rows have unit L2 norm
+ *    (the pages make query/key normalisation a prerequisite: it keeps
+ *    |q.k| <= 1, where the truncated series is accurate and T_n > 0). A score
+ *    temperature is applied by the caller scaling q.
+ *  - Pointers must be 16-byte aligned.
+ */
+#ifndef TSA_H
+#define TSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TSA_OK = 0,
+  TSA_ERR_INVALID = 1,      /* bad pointer, size, alignment or flag          */
+  TSA_ERR_UNSUPPORTED = 2,  /* valid but not built: (d_k, d_v, n_terms, chunk) */
+  TSA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed           */
+  TSA_ERR_TIMEOUT = 4       /* a device-side bounded wait gave up             */
+} tsa_status;
+
+typedef enum { TSA_F32 = 0, TSA_BF16 = 1 } tsa_dtype;
+
+typedef struct {
+  int B;            /* batch                                                   */
+  int H;            /* heads; B*H independent (b,h) heads                     */
+  int d_k;          /* query/key width d: 16 or 32                            */
+  int d_v;          /* value width: 32, 64 or 128                             */
+  int n_terms;      /* n Taylor terms, orders 0..n-1: 1..4 (feature dim <= 1024) */
+  tsa_dtype dtype;  /* element type of q, k, v and out (states are always fp32) */
+  int chunk;        /* prefill chunk length; 0 = library's choice             */
+} tsa_config;
+
+/* tsa_prefill flag: continue from the states already in `states` instead of
+ * starting from zero. Additivity of the states across chunks (abstract; the
+ * "Technical Mechanism Analysis" item 2) makes this exact: prefill(A) then
+ * prefill(B, ACCUMULATE) gives the outputs and states of prefill(A||B). */
+#define TSA_PREFILL_ACCUMULATE 1u
+
+/* D = sum_{m<n} C(d_k+m-1, m), the feature width ("the m-th state is
+ * C(d+m-1, m) wide", abstract). Returns 0 for d_k < 1 or n_terms < 1. */
+size_t tsa_feature_dim(int d_k, int n_terms);
+
+/* D_pad = D rounded up to a multiple of 4: rows of the stored state. */
+size_t tsa_state_pad_dim(int d_k, int n_terms);
+
+/* Algorithmic state size per head, D * (d_v + 1) fp32 elements (9,945 for
+ * d_k=16, d_v=64, n=3: the abstract's figure). 0 if cfg is NULL. */
+size_t tsa_state_elems(const tsa_config* cfg);
+
+/* Bytes of the whole `states` buffer: B*H*D_pad*(d_v+1)*4.
+ * Layout, per head h = b*H + hh, a contiguous block of D_pad*(d_v+1) floats:
+ *   S[a][c] at  h*D_pad*(d_v+1) + a*d_v + c      (a < D_pad, c < d_v)
+ *   z[a]    at  h*D_pad*(d_v+1) + D_pad*d_v + a
+ * Rows a >= D are padding and stay exactly 0. */
+size_t tsa_state_bytes(const tsa_config* cfg);
+
+/* Feature ordering: for row a < D of the state, idx[3a..3a+2] are the input
+ * indices whose product forms the monomial (-1 = no factor; an order-m row has
+ * m indices >= 0, non-decreasing) and weight[a] = 1/sqrt(a!). Host only; idx
+ * holds 3*D ints, weight D floats. */
+tsa_status tsa_feature_index(int d_k, int n_terms, int* idx, float* weight);
+
+/* How tsa_prefill splits the work (host only; num_sms <= 0 asks the current
+ * device). The sequence of each head is cut into n_spans spans of
+ * chunks_per_span chunks of `chunk` tokens; d_v into n_slices slices of
+ * slice_width columns. With n_spans > 1 the call launches a span-state pass,
+ * an exclusive scan over spans and the output pass (`launches` = 3), and takes
+ * scratch_bytes of stream-ordered scratch from the library's pool. */
+typedef struct {
+  int chunk;
+  int slice_width;
+  int n_slices;
+  int n_spans;
+  int chunks_per_span;
+  int ctas_per_sm;
+  int launches;
+  size_t smem_bytes;
+  size_t scratch_bytes;
+} tsa_plan;
+
+tsa_status tsa_prefill_plan(const tsa_config* cfg, int64_t N, int num_sms, tsa_plan* out);
+
+/* Causal chunked prefill of N tokens for every head.
+ *  q, k : [B, H, N, d_k]  dtype, contiguous      (input)
+ *  v    : [B, H, N, d_v]  dtype, contiguous      (input)
+ *  out  : [B, H, N, d_v]  dtype, contiguous      (output, fully written)
+ *  states: tsa_state_bytes(cfg) bytes, fp32, layout above. Output: the state
+ *         after the N tokens. With TSA_PREFILL_ACCUMULATE it is also an input
+ *         (the state before them) and the outputs attend to it.
+ * The library may take stream-ordered scratch from its own memory pool.
+ * N = 0 is a no-op (TSA_OK; states untouched unless ACCUMULATE is clear, in
+ * which case they are zeroed). Errors: NULL pointers, N < 0, misalignment ->
+ * TSA_ERR_INVALID; unsupported shapes -> TSA_ERR_UNSUPPORTED. */
+tsa_status tsa_prefill(const tsa_config* cfg, int64_t N, const void* q, const void* k,
+                       const void* v, void* out, float* states, unsigned flags,
+                       void* cuda_stream);
+
+/* One decode token for every head, constant cost in the context length:
+ *   S <- S + phi(k)[v; 1]^T;  out = (phi(q)^T S)[:d_v] / (phi(q)^T S)[d_v]
+ *  q, k : [B, H, d_k] dtype;  v, out : [B, H, d_v] dtype;
+ *  states: as for tsa_prefill, read and updated in place. */
+tsa_status tsa_decode_step(const tsa_config* cfg, const void* q, const void* k,
+                           const void* v, void* out, float* states, void* cuda_stream);
+
+/* a <- a + b over whole state buffers (the states of consecutive segments add;
+ * abstract, "states are additive across chunks"). a and b may not overlap
+ * partially; a == b doubles the state. */
+tsa_status tsa_state_merge(const tsa_config* cfg, float* a, const float* b,
+                           void* cuda_stream);
+
+/* Copy states into the canonical layout [B, H, D, d_v + 1] fp32 row-major
+ * (column d_v = z), dropping the padding rows. dst: B*H*D*(d_v+1) floats. */
+tsa_status tsa_state_to_canonical(const tsa_config* cfg, const float* states, float* dst,
+                                  void* cuda_stream);
+
+/* Synchronise the stream, then report TSA_ERR_CUDA for a pending fault or
+ * TSA_ERR_TIMEOUT if a device-side wait gave up since the last check. */
+tsa_status tsa_sync_status(void* cuda_stream);
+
+const char* tsa_status_string(tsa_status s);
+const char* tsa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TSA_H */

@@ -1,0 +1,131 @@
+"""CPU checks of the C ABI: the library loads, exports every symbol the header
+declares, and its host-only logic (sizes, feature ordering, work planning,
+argument validation) is right. No kernel is launched here."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+from fixed_state_recurrence_phi_b300 import build as tsa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def T():
+    tsa_build.build()
+    from fixed_state_recurrence_phi_b300 import tsa
+    return tsa
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "tsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tsa_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_match_header(T):
+    declared = _header_functions()
+    assert declared == sorted(T.EXPORTS)
+    lib = ctypes.CDLL(T.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+    # the ELF dynamic symbol table agrees
+    out = os.popen(f"nm -D --defined-only {T.LIB_PATH}").read()
+    for name in declared:
+        assert re.search(rf"\bT {name}$", out, flags=re.M), name
+
+
+def test_sizes(T):
+    for d in (1, 2, 16, 32):
+        for n in range(1, 5):
+            assert T.feature_dim(d, n) == sum(math.comb(d + m - 1, m) for m in range(n))
+    assert T.feature_dim(0, 3) == 0 and T.feature_dim(16, 0) == 0
+    cfg = T.Config(1, 1, 16, 64, 3)
+    assert T.state_elems(cfg) == 9945 == (1 + 16 + 136) * 65
+    assert T.state_pad_dim(16, 3) == 156
+    assert T.state_bytes(T.Config(64, 16, 16, 64, 3)) == 64 * 16 * 156 * 65 * 4
+    assert T.feature_dim(16, 4) == 969 and T.feature_dim(32, 3) == 561
+
+
+@pytest.mark.parametrize("d,n", [(16, 1), (16, 2), (16, 3), (16, 4), (32, 3)])
+def test_feature_order_matches_oracle(T, d, n):
+    """The CUDA feature table (rows of the state) enumerates the same monomials
+    in the same order with the same 1/sqrt(a!) weights as the oracle."""
+    from oracle import tsa_oracle as O
+    idx, w = T.feature_index(d, n)
+    want = [t for m in range(n) for t in O.monomials(d, m)]
+    got = [tuple(int(i) for i in row if i >= 0) for row in idx]
+    assert got == want
+    ww = np.array([1.0 / math.sqrt(O._alpha_factorial(t)) for t in want], dtype=np.float32)
+    assert np.array_equal(w, ww)
+
+
+def test_plan_covers_all_chunks(T):
+    for (B, H, N, d, dv, n) in [(1, 8, 8192, 16, 64, 3), (1, 1, 256, 16, 64, 3),
+                                (64, 16, 65536, 16, 64, 3), (4, 16, 32768, 16, 64, 4),
+                                (2, 32, 65536, 32, 128, 3), (1, 1, 1, 16, 64, 3),
+                                (3, 5, 1000, 32, 32, 2)]:
+        p = T.prefill_plan(T.Config(B, H, d, dv, n), N, num_sms=148)
+        chunks = -(-N // p["chunk"])
+        assert p["n_spans"] >= 1 and p["chunks_per_span"] >= 1
+        assert p["n_spans"] * p["chunks_per_span"] >= chunks
+        assert (p["n_spans"] - 1) * p["chunks_per_span"] < chunks   # no empty span
+        assert p["n_slices"] * p["slice_width"] == dv
+        assert p["smem_bytes"] <= 227 * 1024
+        if p["n_spans"] > 1:
+            assert p["launches"] == 3
+            assert p["scratch_bytes"] == B * H * p["n_spans"] * T.state_pad_dim(d, n) * (dv + 1) * 4
+        else:
+            assert p["launches"] == 1 and p["scratch_bytes"] == 0
+    # the 8-head, 8192-token prefill spreads each head over many spans
+    assert T.prefill_plan(T.Config(1, 8, 16, 64, 3), 8192, num_sms=148)["n_spans"] >= 8
+
+
+def test_validation_codes(T):
+    """Invalid arguments are rejected on the host before any CUDA call."""
+    ok = T.Config(1, 1, 16, 64, 3)
+    fake = 1 << 40   # aligned, never dereferenced: validation fails first
+    cases = [
+        (T.Config(1, 1, 8, 64, 3), T.TSA_ERR_UNSUPPORTED),
+        (T.Config(1, 1, 16, 48, 3), T.TSA_ERR_UNSUPPORTED),
+        (T.Config(1, 1, 16, 64, 5), T.TSA_ERR_UNSUPPORTED),
+        (T.Config(1, 1, 32, 64, 4), T.TSA_ERR_UNSUPPORTED),   # D = 6545 > 1024
+        (T.Config(0, 1, 16, 64, 3), T.TSA_ERR_INVALID),
+        (T.Config(1, 1, 16, 64, 0), T.TSA_ERR_INVALID),
+    ]
+    for cfg, code in cases:
+        with pytest.raises(T.TsaError) as e:
+            T.prefill(cfg, 10, fake, fake, fake, fake, fake, stream=0)
+        assert e.value.status == code, cfg
+        with pytest.raises(T.TsaError) as e:
+            T.decode_step(cfg, fake, fake, fake, fake, fake, stream=0)
+        assert e.value.status == code
+    with pytest.raises(T.TsaError) as e:          # N < 0
+        T.prefill(ok, -1, fake, fake, fake, fake, fake, stream=0)
+    assert e.value.status == T.TSA_ERR_INVALID
+    with pytest.raises(T.TsaError) as e:          # NULL states
+        T.prefill(ok, 10, fake, fake, fake, fake, 0, stream=0)
+    assert e.value.status == T.TSA_ERR_INVALID
+    with pytest.raises(T.TsaError) as e:          # misaligned q
+        T.prefill(ok, 10, fake + 4, fake, fake, fake, fake, stream=0)
+    assert e.value.status == T.TSA_ERR_INVALID
+    with pytest.raises(T.TsaError) as e:          # unknown flag bits
+        T._check("tsa_prefill", T._lib.tsa_prefill(ctypes.byref(ok.c()), 10, fake, fake, fake, fake,
+                                                   fake, 2, 0))
+    assert e.value.status == T.TSA_ERR_INVALID
+    with pytest.raises(T.TsaError) as e:          # NULL decode input
+        T.decode_step(ok, 0, fake, fake, fake, fake, stream=0)
+    assert e.value.status == T.TSA_ERR_INVALID
+    nb = T.state_bytes(ok)
+    with pytest.raises(T.TsaError) as e:          # partially overlapping merge
+        T.state_merge(ok, fake, fake + 16 * (nb // 32), stream=0)
+    assert e.value.status == T.TSA_ERR_INVALID
+    assert "overlap" in T.last_error()
+    with pytest.raises(T.TsaError) as e:
+        T.prefill_plan(ok, -5, num_sms=148)
+    assert e.value.status == T.TSA_ERR_INVALID
+    assert T.status_string(T.TSA_ERR_TIMEOUT) == "TSA_ERR_TIMEOUT"

@@ -1,0 +1,263 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle, on the
+same seeded inputs: small cases element by element over every head, and the
+full-size workloads on sampled heads (heads are independent, so a sampled head
+is checked exactly as it would be alone)."""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def G():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from fixed_state_recurrence_phi_b300 import build
+    build.build()
+    import gpu_helpers
+    return gpu_helpers
+
+
+def _all_heads(G, cfg, N, seed, accumulate_from=None):
+    T, O = G.T, G.O
+    q, k, v = G.make_inputs(cfg, N, seed)
+    out, st = G.gpu_prefill(cfg, q, k, v)
+    torch.cuda.synchronize()
+    Sg = G.canonical(cfg, st)
+    og = G.host(out)
+    qh, kh, vh = G.host(q), G.host(k), G.host(v)
+    tol = G.TOL[cfg.dtype]
+    errs = []
+    for b in range(cfg.B):
+        for h in range(cfg.H):
+            o_r, S_r = O.prefill_recurrent(qh[b, h], kh[b, h], vh[b, h], cfg.n_terms)
+            errs.append(G.check_head(cfg, og[b, h], Sg[b, h], o_r, S_r, tol, f"N={N} b={b} h={h}"))
+    return errs
+
+
+def test_single_head_prefill_then_64_decode_steps(G):
+    """B=1 H=1 N=256 d16 dv64 n=3 fp32, seed 0; then 64 decode steps on fresh
+    seeded tokens, each compared with the oracle's decode step."""
+    T, O = G.T, G.O
+    cfg = T.Config(1, 1, 16, 64, 3, "f32")
+    q, k, v = G.make_inputs(cfg, 256, seed=0)
+    out, st = G.gpu_prefill(cfg, q, k, v)
+    o_r, S_r = O.prefill_recurrent(G.host(q)[0, 0], G.host(k)[0, 0], G.host(v)[0, 0], 3)
+    G.check_head(cfg, G.host(out)[0, 0], G.canonical(cfg, st)[0, 0], o_r, S_r, 1e-4, "prefill")
+    dq, dk, dv = G.make_inputs(cfg, 64, seed=0, phase=1)
+    dqh, dkh, dvh = G.host(dq)[0, 0], G.host(dk)[0, 0], G.host(dv)[0, 0]
+    o1 = torch.empty((1, 1, 64), dtype=torch.float32, device="cuda")
+    S = S_r
+    worst = 0.0
+    for t in range(64):
+        T.decode_step(cfg, dq[:, :, t].contiguous(), dk[:, :, t].contiguous(),
+                      dv[:, :, t].contiguous(), o1, st)
+        o_ref, S = O.decode_step(dqh[t], dkh[t], dvh[t], S, 3)
+        worst = max(worst, G.rel_err(G.host(o1)[0, 0], o_ref))
+    assert worst <= 1e-4, worst
+    Sg = G.canonical(cfg, st)[0, 0]
+    assert G.rel_err(Sg[:, :64], S[:, :64]) <= 1e-4
+    assert G.rel_err(Sg[:, 64], S[:, 64]) <= 1e-4
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 63, 64, 65, 127, 129, 300, 1000])
+def test_ragged_lengths(G, N):
+    cfg = G.T.Config(2, 3, 16, 64, 3, "f32")
+    _all_heads(G, cfg, N, seed=100 + N)
+
+
+@pytest.mark.parametrize("d,dv,n,dtype", [
+    (16, 64, 1, "f32"), (16, 64, 2, "f32"), (16, 64, 4, "f32"), (32, 128, 3, "f32"),
+    (32, 32, 3, "f32"), (16, 32, 4, "f32"), (16, 128, 3, "bf16"), (16, 64, 4, "bf16"),
+    (32, 128, 3, "bf16"), (32, 64, 2, "bf16"), (16, 64, 3, "bf16"),
+])
+def test_shapes(G, d, dv, n, dtype):
+    cfg = G.T.Config(1, 2, d, dv, n, dtype)
+    _all_heads(G, cfg, 333, seed=7 + d + dv + n)
+
+
+def test_n1_is_running_mean(G):
+    """With one Taylor term every weight is 1: out_i = mean(v_0..v_i)."""
+    cfg = G.T.Config(1, 2, 16, 64, 1, "f32")
+    q, k, v = G.make_inputs(cfg, 500, seed=3)
+    out, _ = G.gpu_prefill(cfg, q, k, v)
+    vh = G.host(v)
+    want = np.cumsum(vh, axis=2) / np.arange(1, 501)[None, None, :, None]
+    assert G.rel_err(G.host(out), want) <= 1e-5
+
+
+def test_multi_span_8192(G):
+    """B=1 H=8 N=8192 d16 dv64 n=3 fp32 (the prefill workload the benchmark
+    times, same launch configuration), every head, spans scanned."""
+    cfg = G.T.Config(1, 8, 16, 64, 3, "f32")
+    assert G.T.prefill_plan(cfg, 8192)["n_spans"] > 1
+    _all_heads(G, cfg, 8192, seed=2)
+
+
+def test_accumulate_continues_the_sequence(G):
+    T, O = G.T, G.O
+    cfg = T.Config(1, 2, 16, 64, 3, "f32")
+    q, k, v = G.make_inputs(cfg, 1200, seed=11)
+    _, st = G.gpu_prefill(cfg, q[:, :, :700].contiguous(), k[:, :, :700].contiguous(),
+                          v[:, :, :700].contiguous())
+    out2, st = G.gpu_prefill(cfg, q[:, :, 700:].contiguous(), k[:, :, 700:].contiguous(),
+                             v[:, :, 700:].contiguous(), states=st, accumulate=True)
+    Sg = G.canonical(cfg, st)
+    qh, kh, vh = G.host(q), G.host(k), G.host(v)
+    for h in range(2):
+        o_r, S_r = O.prefill_recurrent(qh[0, h], kh[0, h], vh[0, h], 3)
+        G.check_head(cfg, G.host(out2)[0, h], Sg[0, h], o_r[700:], S_r, 1e-4, "accumulate")
+
+
+def test_merge_of_segments_equals_whole(G):
+    T, O = G.T, G.O
+    cfg = T.Config(2, 2, 16, 64, 3, "f32")
+    q, k, v = G.make_inputs(cfg, 900, seed=12)
+    sl = lambda x, a, b: x[:, :, a:b].contiguous()
+    _, sa = G.gpu_prefill(cfg, sl(q, 0, 400), sl(k, 0, 400), sl(v, 0, 400))
+    _, sb = G.gpu_prefill(cfg, sl(q, 400, 900), sl(k, 400, 900), sl(v, 400, 900))
+    T.state_merge(cfg, sa, sb)
+    Sg = G.canonical(cfg, sa)
+    kh, vh = G.host(k), G.host(v)
+    for b in range(2):
+        for h in range(2):
+            S_r = sum(O.chunk_states(kh[b, h], vh[b, h], 3, 900))
+            assert G.rel_err(Sg[b, h][:, :64], S_r[:, :64]) <= 1e-4
+            assert G.rel_err(Sg[b, h][:, 64], S_r[:, 64]) <= 1e-4
+
+
+def test_decode_equals_next_prefill_row(G):
+    T, O = G.T, G.O
+    cfg = T.Config(1, 4, 16, 64, 3, "f32")
+    q, k, v = G.make_inputs(cfg, 513, seed=13)
+    _, st = G.gpu_prefill(cfg, q[:, :, :512].contiguous(), k[:, :, :512].contiguous(),
+                          v[:, :, :512].contiguous())
+    o1 = torch.empty((1, 4, 64), dtype=torch.float32, device="cuda")
+    T.decode_step(cfg, q[:, :, 512].contiguous(), k[:, :, 512].contiguous(),
+                  v[:, :, 512].contiguous(), o1, st)
+    full, st_full = G.gpu_prefill(cfg, q, k, v)
+    qh, kh, vh = G.host(q), G.host(k), G.host(v)
+    for h in range(4):
+        o_r, S_r = O.prefill_recurrent(qh[0, h], kh[0, h], vh[0, h], 3)
+        assert G.rel_err(G.host(o1)[0, h], o_r[512]) <= 1e-4
+        assert G.rel_err(G.host(full)[0, h, 512], o_r[512]) <= 1e-4
+    assert G.rel_err(G.canonical(cfg, st), G.canonical(cfg, st_full)) <= 1e-5
+
+
+def test_deterministic_and_padding_zero(G):
+    T = G.T
+    cfg = T.Config(1, 8, 16, 64, 3, "f32")
+    q, k, v = G.make_inputs(cfg, 3000, seed=14)
+    o1, s1 = G.gpu_prefill(cfg, q, k, v)
+    o2, s2 = G.gpu_prefill(cfg, q, k, v)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    D, Dp = T.feature_dim(16, 3), T.state_pad_dim(16, 3)
+    st = s1.view(8, Dp * 65)
+    S = st[:, :Dp * 64].view(8, Dp, 64)
+    z = st[:, Dp * 64:]
+    assert torch.count_nonzero(S[:, D:]) == 0 and torch.count_nonzero(z[:, D:]) == 0
+
+
+def test_empty_sequence(G):
+    T = G.T
+    cfg = T.Config(1, 2, 16, 64, 3, "f32")
+    st = torch.randn(T.state_bytes(cfg) // 4, device="cuda")
+    keep = st.clone()
+    e = torch.empty(0, device="cuda")
+    q = torch.empty((1, 2, 0, 16), device="cuda")
+    T.prefill(cfg, 0, q, q, q, q, st, accumulate=True)
+    assert torch.equal(st, keep)
+    T.prefill(cfg, 0, q, q, q, q, st, accumulate=False)
+    assert torch.count_nonzero(st) == 0
+    del e
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, sampled heads
+# ---------------------------------------------------------------------------
+
+def _sampled_prefill_check(G, cfg, q, k, v, out, st, heads, chunked=256):
+    O = G.O
+    tol = G.TOL[cfg.dtype]
+    Sg = T_canon = G.canonical(cfg, st)
+    S_refs = {}
+    for (b, h) in heads:
+        qh, kh, vh = G.host(q[b, h]), G.host(k[b, h]), G.host(v[b, h])
+        o_r, S_r = G.oracle_prefill(qh, kh, vh, cfg.n_terms, chunked=chunked)
+        G.check_head(cfg, G.host(out[b, h]), Sg[b, h], o_r, S_r, tol, f"head {(b, h)}")
+        S_refs[(b, h)] = S_r
+    del T_canon
+    return S_refs
+
+
+def _decode_steps_check(G, cfg, st, S_refs, steps, seed):
+    """Run `steps` decode steps for all heads on the GPU; compare the sampled
+    heads' outputs at every step with the oracle's decode from its own state."""
+    T, O = G.T, G.O
+    dq, dk, dv = G.make_inputs(cfg, steps, seed=seed, phase=1)
+    outs = torch.empty((steps, cfg.B, cfg.H, cfg.d_v), dtype=dq.dtype, device="cuda")
+    qs = dq.permute(2, 0, 1, 3).contiguous()
+    ks = dk.permute(2, 0, 1, 3).contiguous()
+    vs = dv.permute(2, 0, 1, 3).contiguous()
+    for t in range(steps):
+        T.decode_step(cfg, qs[t], ks[t], vs[t], outs[t], st)
+    torch.cuda.synchronize()
+    tol = G.TOL[cfg.dtype]
+    Sg = G.canonical(cfg, st)
+    for (b, h), S in S_refs.items():
+        qh, kh, vh = G.host(qs[:, b, h]), G.host(ks[:, b, h]), G.host(vs[:, b, h])
+        og = G.host(outs[:, b, h])
+        worst = 0.0
+        for t in range(steps):
+            o_ref, S = O.decode_step(qh[t], kh[t], vh[t], S, cfg.n_terms)
+            worst = max(worst, G.rel_err(og[t], o_ref))
+        assert worst <= tol, (b, h, worst)
+        assert G.rel_err(Sg[b, h][:, :cfg.d_v], S[:, :cfg.d_v]) <= tol
+        assert G.rel_err(Sg[b, h][:, cfg.d_v], S[:, cfg.d_v]) <= tol
+
+
+def test_full_decode_B64_H16_N65536(G):
+    """B=64 H=16 d16 dv64 n=3 bf16: prefill of 65,536 tokens, then 1024 decode
+    steps (the decode workload the benchmark times)."""
+    T = G.T
+    cfg = T.Config(64, 16, 16, 64, 3, "bf16")
+    q, k, v = G.make_inputs(cfg, 65536, seed=3)
+    out, st = G.gpu_prefill(cfg, q, k, v)
+    heads = G.sample_heads(64, 16, k=2, seed=3)
+    S_refs = _sampled_prefill_check(G, cfg, q, k, v, out, st, heads)
+    del q, k, v, out
+    torch.cuda.empty_cache()
+    _decode_steps_check(G, cfg, st, S_refs, 1024, seed=3)
+
+
+def test_full_order4_B4_H16_N32768(G):
+    T = G.T
+    cfg = T.Config(4, 16, 16, 64, 4, "bf16")
+    q, k, v = G.make_inputs(cfg, 32768, seed=4)
+    out, st = G.gpu_prefill(cfg, q, k, v)
+    heads = G.sample_heads(4, 16, k=2, seed=4)
+    S_refs = _sampled_prefill_check(G, cfg, q, k, v, out, st, heads)
+    del q, k, v, out
+    _decode_steps_check(G, cfg, st, S_refs, 256, seed=4)
+
+
+def test_full_wide_B2_H32_N65536_with_merge(G):
+    T, O = G.T, G.O
+    cfg = T.Config(2, 32, 32, 128, 3, "bf16")
+    q, k, v = G.make_inputs(cfg, 65536, seed=5)
+    out, st = G.gpu_prefill(cfg, q, k, v)
+    heads = G.sample_heads(2, 32, k=2, seed=5)
+    S_refs = _sampled_prefill_check(G, cfg, q, k, v, out, st, heads)
+    # merge check: prefill of the two halves, states summed, vs the whole
+    half = 32768
+    sl = lambda x, a, b: x[:, :, a:b].contiguous()
+    _, sa = G.gpu_prefill(cfg, sl(q, 0, half), sl(k, 0, half), sl(v, 0, half))
+    _, sb = G.gpu_prefill(cfg, sl(q, half, 65536), sl(k, half, 65536), sl(v, half, 65536))
+    T.state_merge(cfg, sa, sb)
+    Sm = G.canonical(cfg, sa)
+    for (b, h), S_r in S_refs.items():
+        assert G.rel_err(Sm[b, h][:, :128], S_r[:, :128]) <= G.TOL["bf16"]
+        assert G.rel_err(Sm[b, h][:, 128], S_r[:, 128]) <= G.TOL["bf16"]
+    # and the merged state agrees with the single-pass state on every head
+    assert G.rel_err(G.host(sa), G.host(st)) <= 1e-4
