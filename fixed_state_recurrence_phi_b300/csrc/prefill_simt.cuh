@@ -25,24 +25,9 @@
 // features are built DT at a time: phiQ^T[DT][C] and phiK[C][DT(+4)].
 #pragma once
 #include "common.cuh"
+#include "prefill_params.h"
 
 namespace tsa {
-
-struct PrefillParams {
-  const void* q;
-  const void* k;
-  const void* v;
-  void* out;
-  float* states;    // [heads][DPAD*(dv+1)]
-  float* scratch;   // [heads][n_spans][DPAD*(dv+1)], used when n_spans > 1
-  long long N;
-  int heads;
-  int dv;
-  int n_slices;
-  int n_spans;
-  int chunks_per_span;
-  int accumulate;
-};
 
 template <int DK, int NT, int W>
 struct SimtLayout {

@@ -209,6 +209,14 @@ static tsa_status dispatch_prefill(const tsa_config* c, const tsa_plan& pl, Pref
   return fail(TSA_ERR_UNSUPPORTED, "no prefill kernel for d_k=%d n=%d", c->d_k, c->n_terms);
 }
 
+// Launch the prefill kernels of `pl` for either dtype (shared with the other
+// translation units of the library).
+tsa_status launch_prefill(const tsa_config* c, const tsa_plan& pl, PrefillParams p,
+                          cudaStream_t s) {
+  return (c->dtype == TSA_F32) ? dispatch_prefill<float>(c, pl, p, s)
+                               : dispatch_prefill<__nv_bfloat16>(c, pl, p, s);
+}
+
 template <typename T, int DK, int NT>
 static tsa_status dispatch_decode_dv(int dv, DecodeParams p, cudaStream_t s) {
   const unsigned grid = (unsigned)p.heads;

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda_runtime.h>
 #include "../../include/tsa.h"
+#include "prefill_params.h"
 
 namespace tsa {
 tsa_status fail(tsa_status s, const char* fmt, ...);
@@ -9,4 +10,6 @@ tsa_status cuda_fail(cudaError_t e, const char* what);
 tsa_status check_config(const tsa_config* c);
 size_t state_floats_per_head(const tsa_config* c);
 int device_sm_count();
+tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl);
+tsa_status launch_prefill(const tsa_config* c, const tsa_plan& pl, PrefillParams p, cudaStream_t s);
 }  // namespace tsa

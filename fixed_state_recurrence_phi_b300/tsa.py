@@ -23,7 +23,8 @@ TSA_PREFILL_ACCUMULATE = 1
 # Every symbol include/tsa.h declares (checked by the CPU test suite).
 EXPORTS = (
     "tsa_feature_dim", "tsa_state_pad_dim", "tsa_state_elems", "tsa_state_bytes",
-    "tsa_feature_index", "tsa_prefill_plan", "tsa_prefill", "tsa_decode_step",
+    "tsa_feature_index", "tsa_prefill_plan", "tsa_prefill", "tsa_prefill_noalloc",
+    "tsa_decode_step",
     "tsa_state_merge", "tsa_state_to_canonical", "tsa_sync_status",
     "tsa_status_string", "tsa_last_error",
 )
@@ -62,6 +63,7 @@ def _load():
         "tsa_feature_index": (I, [I, I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_float)]),
         "tsa_prefill_plan": (I, [C, I64, I, ctypes.POINTER(TsaPlan)]),
         "tsa_prefill": (I, [C, I64, P, P, P, P, P, U, P]),
+        "tsa_prefill_noalloc": (I, [C, I64, P, P, P, P, P, U, P]),
         "tsa_decode_step": (I, [C, P, P, P, P, P, P]),
         "tsa_state_merge": (I, [C, P, P, P]),
         "tsa_state_to_canonical": (I, [C, P, P, P]),
@@ -162,6 +164,15 @@ def prefill(cfg, N: int, q, k, v, out, states, accumulate: bool = False, stream=
     flags = TSA_PREFILL_ACCUMULATE if accumulate else 0
     _check("tsa_prefill", _lib.tsa_prefill(_cfg(cfg), int(N), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
                                            _ptr(states), flags, _stream(stream)))
+
+
+def prefill_noalloc(cfg, N: int, q, k, v, out, states, accumulate: bool = False, stream=None):
+    """tsa_prefill without any device allocation (fixed 16 MiB scratch array;
+    see include/tsa.h for the limits)."""
+    flags = TSA_PREFILL_ACCUMULATE if accumulate else 0
+    _check("tsa_prefill_noalloc",
+           _lib.tsa_prefill_noalloc(_cfg(cfg), int(N), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                    _ptr(states), flags, _stream(stream)))
 
 
 def decode_step(cfg, q, k, v, out, states, stream=None):

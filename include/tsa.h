@@ -129,6 +129,29 @@ tsa_status tsa_prefill(const tsa_config* cfg, int64_t N, const void* q, const vo
                        const void* v, void* out, float* states, unsigned flags,
                        void* cuda_stream);
 
+/* tsa_prefill_noalloc -- tsa_prefill for callers that cannot allocate.
+ * (A deployment variant: the pages have no counterpart to this call.)
+ * Same arguments, layouts, results and errors as tsa_prefill, but the call
+ * allocates nothing: no cudaMalloc, cudaMallocAsync, cudaFree or pool. It is
+ * for callers that cannot let a library allocate device memory -- a process
+ * whose memory budget belongs to its own allocator, a serving loop that must
+ * not allocate after start-up, or a GPU without the stream-ordered allocator.
+ * Its scratch is one fixed 16 MiB array in device memory that every GPU
+ * loading libtsa.so holds until the process exits. Shapes whose plan needs
+ * more scratch than that (tsa_prefill_plan's scratch_bytes > 16 MiB) are
+ * rejected with TSA_ERR_UNSUPPORTED before any work is queued; shapes with a
+ * single span per head need none.
+ *  - The first call on each device looks up the array's device address (once,
+ *    with that device current); make that first call before any stream
+ *    capture.
+ *  - All calls on a device share the one array, and a call leaves its own
+ *    contents there. Calls that can overlap on the GPU (different streams with
+ *    no ordering between them) race on it: order them on one stream, or use
+ *    tsa_prefill. Nothing in the array needs clearing between calls. */
+tsa_status tsa_prefill_noalloc(const tsa_config* cfg, int64_t N, const void* q, const void* k,
+                               const void* v, void* out, float* states, unsigned flags,
+                               void* cuda_stream);
+
 /* One decode token for every head, constant cost in the context length:
  *   S <- S + phi(k)[v; 1]^T;  out = (phi(q)^T S)[:d_v] / (phi(q)^T S)[d_v]
  *  q, k : [B, H, d_k] dtype;  v, out : [B, H, d_v] dtype;
