@@ -214,129 +214,134 @@ def run_ours(args):
         T.prefill(cfg, w["N"], q, k, v, out, st, stream=stream)
 
     gpu = torch.cuda.current_device()
+    do_pre = args.only in ("all", "prefill")
+    do_dec = args.only in ("all", "decode")
+    ms = e2e_ms = float("nan"); h2d = d2h = 0
+    dec_us = eager_us = long_prefill_ms = merge_ms = float("nan")
+    steps, reps = 1024, 3
+    dw = DECODE
+    dcfg = T.Config(dw["B"], dw["H"], dw["d_k"], dw["d_v"], dw["n_terms"], dw["dtype"])
     with ClockSampler(gpu) as clk:
-        for _ in range(max(3, args.warmup)):
-            flush.fill_(1.0)
-            prefill_step()
-        barrier()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for i in range(args.steps):
-            flush.fill_(float(i))
-            evs[i][0].record(stream)
-            prefill_step()
-            evs[i][1].record(stream)
-        barrier()
-        step_ms = [a.elapsed_time(b) for a, b in evs]
-        ms = max_over_ranks(statistics.mean(step_ms))
+      if do_pre:
+          for _ in range(max(3, args.warmup)):
+              flush.fill_(1.0)
+              prefill_step()
+          barrier()
+          evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)]
+          for i in range(args.steps):
+              flush.fill_(float(i))
+              evs[i][0].record(stream)
+              prefill_step()
+              evs[i][1].record(stream)
+          barrier()
+          step_ms = [a.elapsed_time(b) for a, b in evs]
+          ms = max_over_ranks(statistics.mean(step_ms))
 
-        # -------- e2e: pinned host buffers in, host result out, through the ABI
-        qh = q.cpu().pin_memory(); kh = k.cpu().pin_memory(); vh = v.cpu().pin_memory()
-        oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        sh = torch.empty(st.shape, dtype=st.dtype).pin_memory()
-        qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+          # -------- e2e: pinned host buffers in, host result out, through the ABI
+          qh = q.cpu().pin_memory(); kh = k.cpu().pin_memory(); vh = v.cpu().pin_memory()
+          oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+          sh = torch.empty(st.shape, dtype=st.dtype).pin_memory()
+          qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
 
-        def e2e_step():
-            qd.copy_(qh, non_blocking=True); kd.copy_(kh, non_blocking=True)
-            vd.copy_(vh, non_blocking=True)
-            T.prefill(cfg, w["N"], qd, kd, vd, out, st, stream=stream)
-            oh.copy_(out, non_blocking=True); sh.copy_(st, non_blocking=True)
+          def e2e_step():
+              qd.copy_(qh, non_blocking=True); kd.copy_(kh, non_blocking=True)
+              vd.copy_(vh, non_blocking=True)
+              T.prefill(cfg, w["N"], qd, kd, vd, out, st, stream=stream)
+              oh.copy_(out, non_blocking=True); sh.copy_(st, non_blocking=True)
 
-        for _ in range(3):
-            e2e_step()
-        barrier()
-        e_ms = []
-        for i in range(args.steps):
-            flush.fill_(float(i))
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream); e2e_step(); b.record(stream)
-            e_ms.append((a, b))
-        barrier()
-        e2e_ms = max_over_ranks(statistics.mean([a.elapsed_time(b) for a, b in e_ms]))
-        h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
-        d2h = oh.numel() * oh.element_size() + sh.numel() * sh.element_size()
-        del qh, kh, vh, oh, sh, qd, kd, vd
+          for _ in range(3):
+              e2e_step()
+          barrier()
+          e_ms = []
+          for i in range(args.steps):
+              flush.fill_(float(i))
+              a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+              a.record(stream); e2e_step(); b.record(stream)
+              e_ms.append((a, b))
+          barrier()
+          e2e_ms = max_over_ranks(statistics.mean([a.elapsed_time(b) for a, b in e_ms]))
+          h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
+          d2h = oh.numel() * oh.element_size() + sh.numel() * sh.element_size()
+          del qh, kh, vh, oh, sh, qd, kd, vd
 
-        # ---------------- decode workload ----------------------------------
-        dw = DECODE
-        dcfg = T.Config(dw["B"], dw["H"], dw["d_k"], dw["d_v"], dw["n_terms"], dw["dtype"])
-        dstates = []
-        dq, dk, dv = torch_qkv(dw["B"], dw["H"], dw["N"], dw["d_k"], dw["d_v"], dw["dtype"],
-                               dw["seed"] + 1000 * rank, 0, dev)
-        dout = torch.empty((dw["B"], dw["H"], dw["N"], dw["d_v"]), dtype=dq.dtype, device=dev)
-        s0 = T.new_states(dcfg, dev)
-        pa, pb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        pa.record(stream)
-        T.prefill(dcfg, dw["N"], dq, dk, dv, dout, s0, stream=stream)
-        pb.record(stream)
-        torch.cuda.synchronize()
-        long_prefill_ms = pa.elapsed_time(pb)
-        del dq, dk, dv, dout
-        torch.cuda.empty_cache()
-        for _ in range(DECODE_ROTATE):
-            dstates.append(s0.clone())
-        steps = 1024
-        tq, tk, tv = torch_qkv(dw["B"], dw["H"], steps, dw["d_k"], dw["d_v"], dw["dtype"],
-                               dw["seed"] + 1000 * rank, 1, dev)
-        tq = tq.permute(2, 0, 1, 3).contiguous(); tk = tk.permute(2, 0, 1, 3).contiguous()
-        tv = tv.permute(2, 0, 1, 3).contiguous()
-        touts = torch.empty((steps, dw["B"], dw["H"], dw["d_v"]), dtype=tq.dtype, device=dev)
+      if do_dec:
+          # ---------------- decode workload ----------------------------------
+          dstates = []
+          dq, dk, dv = torch_qkv(dw["B"], dw["H"], args.decode_prefill_n, dw["d_k"], dw["d_v"], dw["dtype"],
+                                 dw["seed"] + 1000 * rank, 0, dev)
+          dout = torch.empty((dw["B"], dw["H"], args.decode_prefill_n, dw["d_v"]), dtype=dq.dtype, device=dev)
+          s0 = T.new_states(dcfg, dev)
+          pa, pb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+          pa.record(stream)
+          T.prefill(dcfg, args.decode_prefill_n, dq, dk, dv, dout, s0, stream=stream)
+          pb.record(stream)
+          torch.cuda.synchronize()
+          long_prefill_ms = pa.elapsed_time(pb)
+          del dq, dk, dv, dout
+          torch.cuda.empty_cache()
+          for _ in range(DECODE_ROTATE):
+              dstates.append(s0.clone())
+          tq, tk, tv = torch_qkv(dw["B"], dw["H"], steps, dw["d_k"], dw["d_v"], dw["dtype"],
+                                 dw["seed"] + 1000 * rank, 1, dev)
+          tq = tq.permute(2, 0, 1, 3).contiguous(); tk = tk.permute(2, 0, 1, 3).contiguous()
+          tv = tv.permute(2, 0, 1, 3).contiguous()
+          touts = torch.empty((steps, dw["B"], dw["H"], dw["d_v"]), dtype=tq.dtype, device=dev)
 
-        def decode_all(s):
-            for t in range(steps):
-                T.decode_step(dcfg, tq[t], tk[t], tv[t], touts[t], dstates[t % DECODE_ROTATE], stream=s)
+          def decode_all(s):
+              for t in range(steps):
+                  T.decode_step(dcfg, tq[t], tk[t], tv[t], touts[t], dstates[t % DECODE_ROTATE], stream=s)
 
-        # eager, per-step events (first 64 steps, L2 rotation as in the graph)
-        decode_all(stream)
-        barrier()
-        eager = []
-        for t in range(64):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            T.decode_step(dcfg, tq[t], tk[t], tv[t], touts[t], dstates[t % DECODE_ROTATE], stream=stream)
-            b.record(stream)
-            eager.append((a, b))
-        barrier()
-        eager_us = statistics.median([a.elapsed_time(b) * 1e3 for a, b in eager])
-        # graph of 1024 steps
-        gs = torch.cuda.Stream()
-        gs.wait_stream(stream)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(gs):
-            with torch.cuda.graph(g, stream=gs):
-                decode_all(gs)
-        stream.wait_stream(gs)
-        g.replay(); barrier()
-        reps = 3
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(reps):
-            g.replay()
-        b.record(stream)
-        barrier()
-        dec_us = max_over_ranks(a.elapsed_time(b) * 1e3 / (reps * steps))
+          # eager, per-step events (first 64 steps, L2 rotation as in the graph)
+          decode_all(stream)
+          barrier()
+          eager = []
+          for t in range(64):
+              a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+              a.record(stream)
+              T.decode_step(dcfg, tq[t], tk[t], tv[t], touts[t], dstates[t % DECODE_ROTATE], stream=stream)
+              b.record(stream)
+              eager.append((a, b))
+          barrier()
+          eager_us = statistics.median([a.elapsed_time(b) * 1e3 for a, b in eager])
+          # graph of 1024 steps
+          gs = torch.cuda.Stream()
+          gs.wait_stream(stream)
+          g = torch.cuda.CUDAGraph()
+          with torch.cuda.stream(gs):
+              with torch.cuda.graph(g, stream=gs):
+                  decode_all(gs)
+          stream.wait_stream(gs)
+          g.replay(); barrier()
+          a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+          a.record(stream)
+          for _ in range(reps):
+              g.replay()
+          b.record(stream)
+          barrier()
+          dec_us = max_over_ranks(a.elapsed_time(b) * 1e3 / (reps * steps))
 
-        # ---------------- merge -------------------------------------------
-        m_ms = []
-        for i in range(10):
-            flush.fill_(float(i))
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream); T.state_merge(dcfg, dstates[0], dstates[1], stream=stream); b.record(stream)
-            m_ms.append((a, b))
-        barrier()
-        merge_ms = statistics.median([a.elapsed_time(b) for a, b in m_ms])
+          # ---------------- merge -------------------------------------------
+          m_ms = []
+          for i in range(10):
+              flush.fill_(float(i))
+              a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+              a.record(stream); T.state_merge(dcfg, dstates[0], dstates[1], stream=stream); b.record(stream)
+              m_ms.append((a, b))
+          barrier()
+          merge_ms = statistics.median([a.elapsed_time(b) for a, b in m_ms])
     clocks = clk.summary()
 
     # ---------------- report -------------------------------------------------
     tokens = w["B"] * w["N"]
-    value = ws * tokens / (ms / 1e3)
+    value = ws * tokens / (ms / 1e3) if do_pre else None
     pre_bytes = _algorithmic_prefill_bytes(w)
     dec_bytes = _algorithmic_decode_bytes(dw)
     state_bytes_step = dw["B"] * dw["H"] * T.state_elems(dcfg) * 4 * 2
-    ach = pre_bytes / (ms / 1e3) / 1e9
+    ach = pre_bytes / (ms / 1e3) / 1e9 if do_pre else float("nan")
     if rank != 0:
         return
-    cpu = cpu_baseline_prefill(w) if (ws == 1 and not args.no_cpu_baseline) else None
+    cpu = cpu_baseline_prefill(w) if (ws == 1 and do_pre and not args.no_cpu_baseline) else None
     traffic = _profile_traffic()
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
@@ -350,9 +355,9 @@ def run_ours(args):
                      "peak_source": f"{peak_src} (copy bandwidth)",
                      "algorithmic_bytes": pre_bytes,
                      "traffic": traffic.get("prefill")},
-        "e2e": {"value": ws * tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": ws * tokens / (e2e_ms / 1e3) if do_pre else None, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps * plan["launches"],
+        "gpu_launches": args.steps * plan["launches"] if do_pre else 0,
         "decode": {"workload": dw["workload"], "us_per_step": dec_us, "us_per_step_eager": eager_us,
                    "us_per_token_per_sequence": dec_us / dw["B"],
                    "state_GBps": state_bytes_step / (dec_us / 1e6) / 1e9,
@@ -363,7 +368,8 @@ def run_ours(args):
                    "timing": f"CUDA graph of {steps} steps x {reps}, states rotated over "
                              f"{DECODE_ROTATE} sets (> L2)",
                    "gpu_launches": reps * steps,
-                   "prefill_N65536_ms": long_prefill_ms},
+                   "states_prefilled_with_N": args.decode_prefill_n,
+                   "prefill_ms": long_prefill_ms},
         "merge": {"workload": dw["workload"], "ms": merge_ms,
                   "GBps": 3 * T.state_bytes(dcfg) / (merge_ms / 1e3) / 1e9},
         "clocks": clocks,
@@ -390,6 +396,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+                    help="run one part (profiling captures on small cases)")
+    ap.add_argument("--decode-prefill-n", type=int, default=DECODE["N"],
+                    help="tokens prefilled before the decode steps (default 65536)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -252,10 +252,20 @@ span_scan_kernel(float* __restrict__ states, float* __restrict__ scratch, int he
   float4* st = reinterpret_cast<float4*>(states) + (size_t)head * elems4;
   float4* sc = reinterpret_cast<float4*>(scratch) + (size_t)head * n_spans * elems4;
   float4 run = accumulate ? st[e] : make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < n_spans; ++s) {
-    const float4 x = sc[(size_t)s * elems4 + e];
-    sc[(size_t)s * elems4 + e] = run;
-    run.x += x.x; run.y += x.y; run.z += x.z; run.w += x.w;
+  // spans in groups of 8: all loads of a group are issued before its stores,
+  // so the memory latency is paid once per group rather than once per span
+  constexpr int G = 8;
+  for (int s0 = 0; s0 < n_spans; s0 += G) {
+    float4 x[G];
+#pragma unroll
+    for (int u = 0; u < G; ++u)
+      if (s0 + u < n_spans) x[u] = sc[(size_t)(s0 + u) * elems4 + e];
+#pragma unroll
+    for (int u = 0; u < G; ++u)
+      if (s0 + u < n_spans) {
+        sc[(size_t)(s0 + u) * elems4 + e] = run;
+        run.x += x[u].x; run.y += x[u].y; run.z += x[u].z; run.w += x[u].w;
+      }
   }
   st[e] = run;
 }
