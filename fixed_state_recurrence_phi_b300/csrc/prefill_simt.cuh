@@ -243,7 +243,7 @@ span_state_kernel(PrefillParams p) {
 // span_scan: exclusive prefix of span states, per head and element; the
 // running total after the last span is the final state.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256)
+static __global__ void __launch_bounds__(256)
 span_scan_kernel(float* __restrict__ states, float* __restrict__ scratch, int heads, int n_spans,
                  int elems4, int accumulate) {
   const int head = blockIdx.y;

@@ -1,0 +1,191 @@
+// prefill_tc.cu -- host side of the tensor-core prefill: value-column slicing
+// under the TMEM budget, TMA tensor maps, launches, and the device error word
+// that bounded waits set on time-out.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "tsa_internal.h"
+#include "prefill_tc.cuh"
+#include "prefill_simt.cuh"
+
+namespace tsa {
+namespace {
+
+// Set by a kernel whose bounded wait gave up; read and cleared by
+// tsa_sync_status.
+__device__ int g_tsa_err;
+
+std::mutex g_mu;
+int* g_err_addr[64];
+bool g_err_ready[64];
+
+constexpr size_t kSmemLimit = 227 * 1024;
+constexpr int kTmemCols = 512;
+
+}  // namespace
+
+tsa_status device_error_word(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(TSA_ERR_CUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ready[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_tsa_err);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    g_err_addr[dev] = static_cast<int*>(p);
+    g_err_ready[dev] = true;
+  }
+  *out = g_err_addr[dev];
+  return TSA_OK;
+}
+
+tsa_status take_device_error() {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_tsa_err, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  if (v != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_tsa_err, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+    return fail(TSA_ERR_TIMEOUT, "a device-side wait timed out (error word %d)", v);
+  }
+  return TSA_OK;
+}
+
+// Split d_v into slices whose TMEM footprint fits: each slice holds the state
+// (NB blocks of 128 rows x (W + 16) fp32 columns, the 16 being the normaliser
+// group) plus the A/O accumulator (max(128, W + 16) columns). Widths are
+// multiples of 16 and as equal as possible.
+bool tc_slicing(int dk, int nt, int dv, TcSlicing* ts) {
+  memset(ts, 0, sizeof(*ts));
+  if (dv % 16 != 0) return false;
+  const int D = feat_dim(dk, nt);
+  const int nb = (D + 127) / 128;
+  int nmax = std::min(dv + 16, (384 / nb) / 16 * 16);
+  if (nmax < 32) return false;
+  const int wmax = nmax - 16;
+  const int units = dv / 16;
+  const int s = (dv + wmax - 1) / wmax;
+  if (s > TC_MAX_SLICES) return false;
+  int c0 = 0, wbig = 0;
+  for (int k = 0; k < s; ++k) {
+    const int u = units / s + (k < units % s ? 1 : 0);
+    ts->w[k] = 16 * u;
+    ts->c0[k] = c0;
+    c0 += ts->w[k];
+    wbig = std::max(wbig, ts->w[k]);
+    const int nm = ts->w[k] + 16;
+    if (nb * nm + std::max(128, nm) > kTmemCols) return false;
+  }
+  ts->nb = nb;
+  ts->n_slices = s;
+  ts->nmax = wbig + 16;
+  ts->smem = TcSmem(dk, ts->nmax, nb).total;
+  return ts->smem <= kSmemLimit;
+}
+
+bool tc_supported(int dk, int nt) {
+  return (dk == 16 && nt >= 1 && nt <= 4) || (dk == 32 && nt >= 1 && nt <= 3);
+}
+
+namespace {
+
+// cuTensorMapEncodeTiled, looked up through the runtime so that the library
+// carries no link-time dependency on the driver library.
+tsa_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* out) {
+  static std::mutex mu;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !p)
+      return fail(TSA_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  *out = fn;
+  return TSA_OK;
+}
+
+// [heads][N][inner] bf16 viewed as 4-D (8, N, inner/8, heads) so that a box
+// (8, 128, groups, 1) lands in shared memory as [group][token][8] -- the
+// core-matrix layout of the MMA operands.
+tsa_status make_tmap(CUtensorMap* m, const void* base, int inner, long long N, int heads, int groups) {
+  cuuint64_t dims[4] = {8, (cuuint64_t)N, (cuuint64_t)(inner / 8), (cuuint64_t)heads};
+  cuuint64_t strides[3] = {(cuuint64_t)inner * 2, 16, (cuuint64_t)N * inner * 2};
+  cuuint32_t box[4] = {8, (cuuint32_t)TC_C, (cuuint32_t)groups, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  tsa_status st = encode_fn(&enc);
+  if (st != TSA_OK) return st;
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(TSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return TSA_OK;
+}
+
+template <int DK, int NT>
+tsa_status launch_tc(const tsa_plan& pl, const TcSlicing& ts, const PrefillParams& pp, cudaStream_t s) {
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  p.out = pp.out; p.states = pp.states; p.scratch = pp.scratch;
+  p.N = pp.N; p.heads = pp.heads; p.dv = pp.dv; p.n_spans = pl.n_spans;
+  p.chunks_per_span = pl.chunks_per_span; p.accumulate = pp.accumulate;
+  p.n_slices = ts.n_slices; p.nmax = ts.nmax;
+  for (int k = 0; k < ts.n_slices; ++k) { p.slice_c0[k] = ts.c0[k]; p.slice_w[k] = ts.w[k]; }
+  tsa_status st = device_error_word(&p.err);
+  if (st != TSA_OK) return st;
+  CUtensorMap mq, mk, mv;
+  if ((st = make_tmap(&mq, pp.q, DK, pp.N, pp.heads, DK / 8)) != TSA_OK) return st;
+  if ((st = make_tmap(&mk, pp.k, DK, pp.N, pp.heads, DK / 8)) != TSA_OK) return st;
+  if ((st = make_tmap(&mv, pp.v, pp.dv, pp.N, pp.heads, 2)) != TSA_OK) return st;
+  const unsigned grid = (unsigned)((long long)pp.heads * ts.n_slices * pl.n_spans);
+  const int smem = (int)ts.smem;
+  cudaError_t e;
+  if (pl.n_spans > 1) {
+    e = cudaFuncSetAttribute(span_state_tc_kernel<DK, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_state_tc)");
+    span_state_tc_kernel<DK, NT><<<grid, TC_THREADS, smem, s>>>(p, mk, mv);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch span_state_tc");
+    const int elems4 = (int)(round_up(feat_dim(DK, NT), 4) * (pp.dv + 1) / 4);
+    dim3 g2((elems4 + 255) / 256, pp.heads);
+    span_scan_kernel<<<g2, 256, 0, s>>>(pp.states, pp.scratch, pp.heads, pl.n_spans, elems4, pp.accumulate);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch span_scan");
+  }
+  e = cudaFuncSetAttribute(span_output_tc_kernel<__nv_bfloat16, DK, NT>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_output_tc)");
+  span_output_tc_kernel<__nv_bfloat16, DK, NT><<<grid, TC_THREADS, smem, s>>>(p, mq, mk, mv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch span_output_tc");
+  return TSA_OK;
+}
+
+}  // namespace
+
+tsa_status launch_prefill_tc(const tsa_config* c, const tsa_plan& pl, const PrefillParams& p, cudaStream_t s) {
+  TcSlicing ts;
+  if (!tc_slicing(c->d_k, c->n_terms, c->d_v, &ts))
+    return fail(TSA_ERR_UNSUPPORTED, "no tensor-core slicing for d_k=%d d_v=%d n=%d", c->d_k, c->d_v, c->n_terms);
+#define TSA_TC_CASE(DK, NT) \
+  if (c->d_k == DK && c->n_terms == NT) return launch_tc<DK, NT>(pl, ts, p, s);
+  TSA_TC_CASE(16, 1) TSA_TC_CASE(16, 2) TSA_TC_CASE(16, 3) TSA_TC_CASE(16, 4)
+  TSA_TC_CASE(32, 1) TSA_TC_CASE(32, 2) TSA_TC_CASE(32, 3)
+#undef TSA_TC_CASE
+  return fail(TSA_ERR_UNSUPPORTED, "no tensor-core prefill for d_k=%d n=%d", c->d_k, c->n_terms);
+}
+
+}  // namespace tsa

@@ -123,8 +123,52 @@ static size_t simt_smem_bytes(int dk, int nt, int W) {
 static constexpr size_t kSmemLimit = 227 * 1024;
 static constexpr size_t kSmemPerSm = 228 * 1024;
 
+// Tensor-core plan (bf16 inputs): chunks of 128 tokens, d_v sliced under the
+// TMEM budget, one CTA per SM. A span-state chunk costs about half an output
+// chunk (phi(K) and the update only).
+static tsa_status make_plan_tc(const tsa_config* c, long long N, int num_sms, const TcSlicing& ts,
+                               tsa_plan* pl) {
+  const int chunk = 128;
+  const long long heads = (long long)c->B * c->H;
+  const long long n_chunks = (N + chunk - 1) / chunk;
+  const long long units = heads * ts.n_slices;
+  const long long slots = std::max(1, num_sms);
+  int best_s = 1;
+  double best_cost = 1e300;
+  const long long s_max = std::min<long long>(n_chunks, 1024);
+  for (long long s = 1; s <= std::max<long long>(1, s_max); ++s) {
+    const long long cps = (n_chunks + s - 1) / s;
+    const long long s_eff = cps > 0 ? (n_chunks + cps - 1) / cps : 1;
+    if (s_eff != s) continue;
+    const long long waves = (units * s_eff + slots - 1) / slots;
+    const double cost = (double)waves * cps * (s_eff > 1 ? 1.5 : 1.0) + (s_eff > 1 ? 1.0 : 0.0);
+    if (cost < best_cost - 1e-9) { best_cost = cost; best_s = (int)s_eff; }
+  }
+  int wmax = 0;
+  for (int k = 0; k < ts.n_slices; ++k) wmax = std::max(wmax, ts.w[k]);
+  pl->chunk = chunk;
+  pl->slice_width = wmax;
+  pl->n_slices = ts.n_slices;
+  pl->n_spans = best_s;
+  pl->chunks_per_span = n_chunks > 0 ? (int)((n_chunks + best_s - 1) / best_s) : 0;
+  pl->smem_bytes = ts.smem;
+  pl->ctas_per_sm = 1;
+  pl->scratch_bytes = best_s > 1 ? (size_t)heads * best_s * state_floats_per_head(c) * 4 : 0;
+  pl->launches = best_s > 1 ? 3 : 1;
+  pl->path = TSA_PATH_TC;
+  return TSA_OK;
+}
+
 tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl) {
   memset(pl, 0, sizeof(*pl));
+  if (c->dtype == TSA_BF16 && tc_supported(c->d_k, c->n_terms)) {
+    TcSlicing ts;
+    if (tc_slicing(c->d_k, c->n_terms, c->d_v, &ts)) {
+      if (c->chunk != 0 && c->chunk != 128)
+        return fail(TSA_ERR_UNSUPPORTED, "chunk=%d not built for bf16 (0 or 128)", c->chunk);
+      return make_plan_tc(c, N, num_sms, ts, pl);
+    }
+  }
   const int chunk = 64;
   if (c->chunk != 0 && c->chunk != chunk)
     return fail(TSA_ERR_UNSUPPORTED, "chunk=%d not built (0 or 64)", c->chunk);
@@ -159,6 +203,7 @@ tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl
   pl->ctas_per_sm = occ;
   pl->scratch_bytes = best_s > 1 ? (size_t)heads * best_s * state_floats_per_head(c) * 4 : 0;
   pl->launches = best_s > 1 ? 3 : 1;
+  pl->path = TSA_PATH_SIMT;
   return TSA_OK;
 }
 
@@ -213,6 +258,7 @@ static tsa_status dispatch_prefill(const tsa_config* c, const tsa_plan& pl, Pref
 // translation units of the library).
 tsa_status launch_prefill(const tsa_config* c, const tsa_plan& pl, PrefillParams p,
                           cudaStream_t s) {
+  if (pl.path == TSA_PATH_TC) return launch_prefill_tc(c, pl, p, s);
   return (c->dtype == TSA_F32) ? dispatch_prefill<float>(c, pl, p, s)
                                : dispatch_prefill<__nv_bfloat16>(c, pl, p, s);
 }
@@ -341,8 +387,7 @@ tsa_status tsa_prefill(const tsa_config* c, int64_t N, const void* q, const void
     if (st != TSA_OK) return st;
     p.scratch = static_cast<float*>(scratch);
   }
-  st = (c->dtype == TSA_F32) ? dispatch_prefill<float>(c, pl, p, s)
-                             : dispatch_prefill<__nv_bfloat16>(c, pl, p, s);
+  st = launch_prefill(c, pl, p, s);
   if (scratch) {
     tsa_status st2 = scratch_free(scratch, s);
     if (st == TSA_OK) st = st2;
@@ -399,7 +444,7 @@ tsa_status tsa_state_to_canonical(const tsa_config* c, const float* states, floa
 tsa_status tsa_sync_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  return TSA_OK;
+  return take_device_error();
 }
 
 const char* tsa_status_string(tsa_status s) {

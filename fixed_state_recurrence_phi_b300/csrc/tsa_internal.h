@@ -12,4 +12,16 @@ size_t state_floats_per_head(const tsa_config* c);
 int device_sm_count();
 tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl);
 tsa_status launch_prefill(const tsa_config* c, const tsa_plan& pl, PrefillParams p, cudaStream_t s);
+
+// Tensor-core prefill (prefill_tc.cu).
+struct TcSlicing {
+  int nb, nmax, n_slices;
+  int c0[4], w[4];
+  size_t smem;
+};
+bool tc_supported(int dk, int nt);
+bool tc_slicing(int dk, int nt, int dv, TcSlicing* ts);
+tsa_status launch_prefill_tc(const tsa_config* c, const tsa_plan& pl, const PrefillParams& p, cudaStream_t s);
+tsa_status device_error_word(int** out);
+tsa_status take_device_error();
 }  // namespace tsa

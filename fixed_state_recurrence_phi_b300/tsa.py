@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libtsa.so")
 TSA_OK, TSA_ERR_INVALID, TSA_ERR_UNSUPPORTED, TSA_ERR_CUDA, TSA_ERR_TIMEOUT = range(5)
 TSA_F32, TSA_BF16 = 0, 1
 TSA_PREFILL_ACCUMULATE = 1
+TSA_PATH_SIMT, TSA_PATH_TC = 0, 1
 
 # Every symbol include/tsa.h declares (checked by the CPU test suite).
 EXPORTS = (
@@ -40,7 +41,8 @@ class TsaPlan(ctypes.Structure):
     _fields_ = [("chunk", ctypes.c_int), ("slice_width", ctypes.c_int), ("n_slices", ctypes.c_int),
                 ("n_spans", ctypes.c_int), ("chunks_per_span", ctypes.c_int),
                 ("ctas_per_sm", ctypes.c_int), ("launches", ctypes.c_int),
-                ("smem_bytes", ctypes.c_size_t), ("scratch_bytes", ctypes.c_size_t)]
+                ("smem_bytes", ctypes.c_size_t), ("scratch_bytes", ctypes.c_size_t),
+                ("path", ctypes.c_int)]
 
 
 class TsaError(RuntimeError):

@@ -96,10 +96,14 @@ tsa_status tsa_feature_index(int d_k, int n_terms, int* idx, float* weight);
 
 /* How tsa_prefill splits the work (host only; num_sms <= 0 asks the current
  * device). The sequence of each head is cut into n_spans spans of
- * chunks_per_span chunks of `chunk` tokens; d_v into n_slices slices of
+ * chunks_per_span chunks of `chunk` tokens; d_v into n_slices slices of at most
  * slice_width columns. With n_spans > 1 the call launches a span-state pass,
  * an exclusive scan over spans and the output pass (`launches` = 3), and takes
- * scratch_bytes of stream-ordered scratch from the library's pool. */
+ * scratch_bytes of stream-ordered scratch from the library's pool.
+ * path: TSA_PATH_SIMT (fp32 FFMA on the CUDA cores) or TSA_PATH_TC (bf16
+ * tcgen05 tensor cores with fp32 TMEM accumulators; bf16 inputs). */
+#define TSA_PATH_SIMT 0
+#define TSA_PATH_TC 1
 typedef struct {
   int chunk;
   int slice_width;
@@ -110,6 +114,7 @@ typedef struct {
   int launches;
   size_t smem_bytes;
   size_t scratch_bytes;
+  int path;
 } tsa_plan;
 
 tsa_status tsa_prefill_plan(const tsa_config* cfg, int64_t N, int num_sms, tsa_plan* out);
@@ -171,7 +176,11 @@ tsa_status tsa_state_to_canonical(const tsa_config* cfg, const float* states, fl
                                   void* cuda_stream);
 
 /* Synchronise the stream, then report TSA_ERR_CUDA for a pending fault or
- * TSA_ERR_TIMEOUT if a device-side wait gave up since the last check. */
+ * TSA_ERR_TIMEOUT if a device-side wait gave up since the last check (the
+ * tensor-core kernels bound every wait on their mbarriers at 1 s; a CTA whose
+ * wait runs out records it here, stops, releases its tensor memory and exits,
+ * leaving its outputs incomplete). The flag is per device and is cleared by
+ * this call. */
 tsa_status tsa_sync_status(void* cuda_stream);
 
 const char* tsa_status_string(tsa_status s);

@@ -1,0 +1,110 @@
+"""Parity of the tensor-core prefill path (bf16 q, k, v; tcgen05 MMAs with fp32
+TMEM accumulators) with the float64 oracle on the same seeded inputs: ragged
+tails around the 128-token chunk, several spans per head (span-state pass and
+scan), several value-column slices, continuation with ACCUMULATE, and
+determinism. Tolerance: normwise relative error per head <= 2e-2 (bf16 inputs,
+fp32 accumulation and states)."""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def G():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from fixed_state_recurrence_phi_b300 import build
+    build.build()
+    import gpu_helpers
+    return gpu_helpers
+
+
+def _check_all_heads(G, cfg, N, seed, chunked=None):
+    O = G.O
+    q, k, v = G.make_inputs(cfg, N, seed)
+    out, st = G.gpu_prefill(cfg, q, k, v)
+    G.T.sync_status()
+    Sg = G.canonical(cfg, st)
+    og = G.host(out)
+    qh, kh, vh = G.host(q), G.host(k), G.host(v)
+    worst = 0.0
+    for b in range(cfg.B):
+        for h in range(cfg.H):
+            o_r, S_r = G.oracle_prefill(qh[b, h], kh[b, h], vh[b, h], cfg.n_terms, chunked=chunked)
+            e = G.check_head(cfg, og[b, h], Sg[b, h], o_r, S_r, G.TOL["bf16"], f"N={N} b={b} h={h}")
+            worst = max(worst, max(e))
+    return worst
+
+
+def test_bf16_uses_tensor_core_path(G):
+    T = G.T
+    for d, dv, n in [(16, 64, 3), (16, 64, 4), (32, 128, 3), (16, 128, 3), (32, 64, 2), (16, 32, 1)]:
+        p = T.prefill_plan(T.Config(2, 4, d, dv, n, "bf16"), 4096)
+        assert p["path"] == T.TSA_PATH_TC and p["chunk"] == 128, (d, dv, n, p)
+    assert T.prefill_plan(T.Config(1, 8, 16, 64, 3, "f32"), 8192)["path"] == T.TSA_PATH_SIMT
+
+
+@pytest.mark.parametrize("N", [1, 2, 127, 128, 129, 255, 256, 257, 1000])
+def test_tc_ragged_lengths(G, N):
+    cfg = G.T.Config(2, 3, 16, 64, 3, "bf16")
+    _check_all_heads(G, cfg, N, seed=200 + N)
+
+
+@pytest.mark.parametrize("d,dv,n,N", [
+    (16, 64, 4, 700),     # 8 feature blocks, two value slices of 32
+    (32, 128, 3, 600),    # 5 feature blocks, three value slices
+    (16, 128, 3, 500),    # one slice of 128 (+ the normaliser group: N = 144)
+    (32, 32, 2, 400),     # one feature block
+    (16, 32, 1, 300),     # n = 1: a running mean
+])
+def test_tc_slicing_shapes(G, d, dv, n, N):
+    cfg = G.T.Config(1, 2, d, dv, n, "bf16")
+    _check_all_heads(G, cfg, N, seed=300 + d + dv + n)
+
+
+def test_tc_multi_span(G):
+    """Few heads and a long sequence: the plan cuts each head into spans, so
+    the span-state pass, the scan and the prefix-state readout all run."""
+    cfg = G.T.Config(1, 2, 16, 64, 3, "bf16")
+    plan = G.T.prefill_plan(cfg, 8192)
+    assert plan["n_spans"] > 1 and plan["launches"] == 3
+    _check_all_heads(G, cfg, 8192, seed=31, chunked=256)
+
+
+def test_tc_multi_span_multi_slice_order4(G):
+    cfg = G.T.Config(1, 1, 16, 64, 4, "bf16")
+    plan = G.T.prefill_plan(cfg, 5000)
+    assert plan["n_spans"] > 1 and plan["n_slices"] == 2
+    _check_all_heads(G, cfg, 5000, seed=32, chunked=256)
+
+
+def test_tc_accumulate_continues_the_sequence(G):
+    T, O = G.T, G.O
+    cfg = T.Config(1, 2, 16, 64, 3, "bf16")
+    q, k, v = G.make_inputs(cfg, 1500, seed=33)
+    sl = lambda x, a, b: x[:, :, a:b].contiguous()
+    _, st = G.gpu_prefill(cfg, sl(q, 0, 650), sl(k, 0, 650), sl(v, 0, 650))
+    out2, st = G.gpu_prefill(cfg, sl(q, 650, 1500), sl(k, 650, 1500), sl(v, 650, 1500), states=st,
+                             accumulate=True)
+    Sg = G.canonical(cfg, st)
+    qh, kh, vh = G.host(q), G.host(k), G.host(v)
+    for h in range(2):
+        o_r, S_r = O.prefill_recurrent(qh[0, h], kh[0, h], vh[0, h], 3)
+        G.check_head(cfg, G.host(out2)[0, h], Sg[0, h], o_r[650:], S_r, G.TOL["bf16"], "accumulate")
+
+
+def test_tc_deterministic_and_padding_zero(G):
+    T = G.T
+    cfg = T.Config(1, 4, 16, 64, 4, "bf16")
+    q, k, v = G.make_inputs(cfg, 3000, seed=34)
+    o1, s1 = G.gpu_prefill(cfg, q, k, v)
+    o2, s2 = G.gpu_prefill(cfg, q, k, v)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    D, Dp = T.feature_dim(16, 4), T.state_pad_dim(16, 4)
+    st = s1.view(4, Dp * 65)
+    S = st[:, :Dp * 64].view(4, Dp, 64)
+    z = st[:, Dp * 64:]
+    assert torch.count_nonzero(S[:, D:]) == 0 and torch.count_nonzero(z[:, D:]) == 0
+    T.sync_status()
