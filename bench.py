@@ -35,6 +35,8 @@ import numpy as np  # noqa: E402
 METRIC = "prefill tokens/s at N=8192 (n=3); decode µs/token and state GB/s on 1 B300"
 PREFILL = dict(workload="prefill_B1_H8_N8192", B=1, H=8, N=8192, d_k=16, d_v=64, n_terms=3, dtype="f32", seed=2)
 DECODE = dict(workload="decode_B64_H16_N65536", B=64, H=16, N=65536, d_k=16, d_v=64, n_terms=3, dtype="bf16", seed=3)
+ORDER4 = dict(workload="order4_B4_H16_N32768", B=4, H=16, N=32768, d_k=16, d_v=64, n_terms=4, dtype="bf16", seed=4)
+WIDE = dict(workload="wide_B2_H32_N65536", B=2, H=32, N=65536, d_k=32, d_v=128, n_terms=3, dtype="bf16", seed=5)
 L2_FLUSH_BYTES = 256 << 20
 DECODE_ROTATE = 8
 
@@ -63,6 +65,25 @@ def _algorithmic_prefill_bytes(w) -> int:
     D = sum(__import__("math").comb(w["d_k"] + m - 1, m) for m in range(w["n_terms"]))
     io = heads * w["N"] * (2 * w["d_k"] + 2 * w["d_v"]) * es
     return io + heads * D * (w["d_v"] + 1) * 4
+
+
+def _algorithmic_prefill_flops(w) -> float:
+    """Per token-head: state update 2*D*(d_v+1), readout 2*D*(d_v+1), intra-chunk
+    2*C*(d_k+d_v+1) at the reference chunk C = 64 (dense; padding and the
+    implementation's own chunk length are not counted)."""
+    import math
+    D = sum(math.comb(w["d_k"] + m - 1, m) for m in range(w["n_terms"]))
+    per = 4 * D * (w["d_v"] + 1) + 2 * 64 * (w["d_k"] + w["d_v"] + 1)
+    return float(per) * w["B"] * w["H"] * w["N"]
+
+
+def _bf16_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["bf16_tflops"], p["bf16_tflops_sustained"], "measured"
+    except Exception:
+        return 1800.0, 1400.0, "fallback"
 
 
 def _algorithmic_decode_bytes(w) -> int:
@@ -265,6 +286,50 @@ def run_ours(args):
           d2h = oh.numel() * oh.element_size() + sh.numel() * sh.element_size()
           del qh, kh, vh, oh, sh, qd, kd, vd
 
+      tc_lines = []
+      for tw in (ORDER4, WIDE):
+          if args.only not in ("all", tw["workload"].split("_")[0]):
+              continue
+          tw = dict(tw)
+          if args.tc_n:
+              tw["N"] = args.tc_n
+          tcfg = T.Config(tw["B"], tw["H"], tw["d_k"], tw["d_v"], tw["n_terms"], tw["dtype"])
+          tq, tk, tv = torch_qkv(tw["B"], tw["H"], tw["N"], tw["d_k"], tw["d_v"], tw["dtype"],
+                                 tw["seed"] + 1000 * rank, 0, dev)
+          tout = torch.empty((tw["B"], tw["H"], tw["N"], tw["d_v"]), dtype=tq.dtype, device=dev)
+          tst = T.new_states(tcfg, dev)
+          tplan = T.prefill_plan(tcfg, tw["N"])
+          for _ in range(3):
+              flush.fill_(1.0)
+              T.prefill(tcfg, tw["N"], tq, tk, tv, tout, tst, stream=stream)
+          barrier()
+          tev = []
+          for i in range(max(3, args.steps // 2)):
+              flush.fill_(float(i))
+              a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+              a.record(stream)
+              T.prefill(tcfg, tw["N"], tq, tk, tv, tout, tst, stream=stream)
+              b.record(stream)
+              tev.append((a, b))
+          barrier()
+          tms = max_over_ranks(statistics.mean([a.elapsed_time(b) for a, b in tev]))
+          T.sync_status(stream)
+          fl = _algorithmic_prefill_flops(tw)
+          pk_burst, pk_sust, pk_src = _bf16_peaks()
+          ach = fl / (tms / 1e3) / 1e12
+          tc_lines.append({
+              "workload": tw["workload"], "N": tw["N"], "ms": tms,
+              "tokens_per_s": ws * tw["B"] * tw["N"] / (tms / 1e3),
+              "path": "tensor cores (tcgen05, bf16 in, fp32 TMEM accumulators)" if tplan["path"] == 1 else "simt",
+              "plan": {k2: tplan[k2] for k2 in ("chunk", "n_slices", "slice_width", "n_spans", "launches")},
+              "roofline": {"bound": "tensor", "achieved": ach, "peak": pk_burst, "unit": "TFLOP/s",
+                           "frac": ach / pk_burst, "frac_of_sustained": ach / pk_sust,
+                           "peak_source": f"{pk_src} cuBLAS bf16 (burst; sustained {pk_sust})",
+                           "algorithmic_flops": fl},
+          })
+          del tq, tk, tv, tout, tst
+          torch.cuda.empty_cache()
+
       if do_dec:
           # ---------------- decode workload ----------------------------------
           dstates = []
@@ -370,6 +435,7 @@ def run_ours(args):
                    "gpu_launches": reps * steps,
                    "states_prefilled_with_N": args.decode_prefill_n,
                    "prefill_ms": long_prefill_ms},
+        "prefill_tensor_core": tc_lines,
         "merge": {"workload": dw["workload"], "ms": merge_ms,
                   "GBps": 3 * T.state_bytes(dcfg) / (merge_ms / 1e3) / 1e9},
         "clocks": clocks,
@@ -396,8 +462,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "order4", "wide"], default="all",
                     help="run one part (profiling captures on small cases)")
+    ap.add_argument("--tc-n", type=int, default=0,
+                    help="sequence length of the order4/wide workloads (default: theirs)")
     ap.add_argument("--decode-prefill-n", type=int, default=DECODE["N"],
                     help="tokens prefilled before the decode steps (default 65536)")
     args = ap.parse_args()

@@ -61,37 +61,71 @@ __device__ __forceinline__ uint4 feat8(const float (&x)[DK + 1]) {
 }
 
 // Write the G groups of 8 features starting at A0 (a multiple of 8) for one
-// token. `pq` / `pk` point at the token's row inside a feature tile whose
-// 8-feature groups are 128 bytes apart.
-template <int DK, int NT, bool WITH_Q, int A0, int G>
+// token into the feature tile of every CTA of the cluster: `local` points at
+// the token's row in this CTA's tile (8-feature groups 128 bytes apart), and
+// `remote[r]` is the shared::cluster address of the same row in CTA r (used for
+// r != R, this CTA's rank).
+template <int DK, int NT, int NS, int R, int A0, int G>
 struct PhiGroups {
-  static __device__ __forceinline__ void run(const float (&xq)[DK + 1], const float (&xk)[DK + 1],
-                                             uint8_t* pq, uint8_t* pk) {
-    PhiGroups<DK, NT, WITH_Q, A0, G - 1>::run(xq, xk, pq, pk);
+  static __device__ __forceinline__ void run(const float (&x)[DK + 1], uint8_t* local, const uint32_t* remote) {
+    PhiGroups<DK, NT, NS, R, A0, G - 1>::run(x, local, remote);
     constexpr int a = A0 + 8 * (G - 1);
     constexpr int grp = (a % 128) / 8;
-    if constexpr (WITH_Q) *reinterpret_cast<uint4*>(pq + grp * 128) = feat8<DK, NT, a>(xq);
-    *reinterpret_cast<uint4*>(pk + grp * 128) = feat8<DK, NT, a>(xk);
+    const uint4 v = feat8<DK, NT, a>(x);
+    *reinterpret_cast<uint4*>(local + grp * 128) = v;
+#pragma unroll
+    for (int r = 0; r < NS; ++r)
+      if (r != R) tc::st_cluster_v4(remote[r] + grp * 128, v);
   }
 };
-template <int DK, int NT, bool WITH_Q, int A0>
-struct PhiGroups<DK, NT, WITH_Q, A0, 0> {
-  static __device__ __forceinline__ void run(const float (&)[DK + 1], const float (&)[DK + 1], uint8_t*,
-                                             uint8_t*) {}
+template <int DK, int NT, int NS, int R, int A0>
+struct PhiGroups<DK, NT, NS, R, A0, 0> {
+  static __device__ __forceinline__ void run(const float (&)[DK + 1], uint8_t*, const uint32_t*) {}
 };
 
-// Features [128 f + 64 half, +64) of block f for one token (runtime f and half
-// select one of the compile-time instantiations).
-template <int DK, int NT, bool WITH_Q, int F = 0>
-__device__ __forceinline__ void build_phi_half(int f, int half, const float (&xq)[DK + 1],
-                                               const float (&xk)[DK + 1], uint8_t* pq, uint8_t* pk) {
+// Groups of 8 (of the 16 in a 128-wide tile) that CTA r of a cluster of NS
+// builds: [tc_group0(NS, r), tc_group0(NS, r + 1)); each half of the CTA's
+// workers takes one part of that range.
+__host__ __device__ constexpr int tc_group0(int ns, int r) { return (16 * r + ns - 1) / ns; }
+__host__ __device__ constexpr int tc_group_mid(int ns, int r) {
+  return tc_group0(ns, r) + (tc_group0(ns, r + 1) - tc_group0(ns, r) + 1) / 2;
+}
+
+// This CTA's share of feature block f for one token (runtime f and half pick a
+// compile-time instantiation).
+template <int DK, int NT, int NS, int R, int F = 0>
+__device__ __forceinline__ void build_phi_part(int f, int half, const float (&x)[DK + 1], uint8_t* local,
+                                               const uint32_t* remote) {
   if constexpr (F < FeatConst<DK, NT>::NB) {
     if (f == F) {
-      if (half == 0) PhiGroups<DK, NT, WITH_Q, F * 128, 8>::run(xq, xk, pq, pk);
-      else PhiGroups<DK, NT, WITH_Q, F * 128 + 64, 8>::run(xq, xk, pq, pk);
+      constexpr int g0 = tc_group0(NS, R), gm = tc_group_mid(NS, R), g1 = tc_group0(NS, R + 1);
+      if (half == 0) PhiGroups<DK, NT, NS, R, F * 128 + 8 * g0, gm - g0>::run(x, local, remote);
+      else PhiGroups<DK, NT, NS, R, F * 128 + 8 * gm, g1 - gm>::run(x, local, remote);
       return;
     }
-    build_phi_half<DK, NT, WITH_Q, F + 1>(f, half, xq, xk, pq, pk);
+    build_phi_part<DK, NT, NS, R, F + 1>(f, half, x, local, remote);
+  }
+}
+
+// Runtime rank -> instantiation.
+template <int DK, int NT, int NS>
+__device__ __forceinline__ void build_phi_rank(int rank, int f, int half, const float (&x)[DK + 1],
+                                               uint8_t* local, const uint32_t* remote) {
+  if constexpr (NS == 1) {
+    build_phi_part<DK, NT, 1, 0>(f, half, x, local, remote);
+  } else if constexpr (NS == 2) {
+    if (rank == 0) build_phi_part<DK, NT, 2, 0>(f, half, x, local, remote);
+    else build_phi_part<DK, NT, 2, 1>(f, half, x, local, remote);
+  } else if constexpr (NS == 3) {
+    if (rank == 0) build_phi_part<DK, NT, 3, 0>(f, half, x, local, remote);
+    else if (rank == 1) build_phi_part<DK, NT, 3, 1>(f, half, x, local, remote);
+    else build_phi_part<DK, NT, 3, 2>(f, half, x, local, remote);
+  } else {
+    static_assert(NS >= 1 && NS <= 4, "cluster size");
+    if (rank == 0) build_phi_part<DK, NT, 4, 0>(f, half, x, local, remote);
+    else if (rank == 1) build_phi_part<DK, NT, 4, 1>(f, half, x, local, remote);
+    else if (rank == 2) build_phi_part<DK, NT, 4, 2>(f, half, x, local, remote);
+    else build_phi_part<DK, NT, 4, 3>(f, half, x, local, remote);
   }
 }
 

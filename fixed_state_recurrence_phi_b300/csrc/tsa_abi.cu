@@ -141,7 +141,12 @@ static tsa_status make_plan_tc(const tsa_config* c, long long N, int num_sms, co
     const long long s_eff = cps > 0 ? (n_chunks + cps - 1) / cps : 1;
     if (s_eff != s) continue;
     const long long waves = (units * s_eff + slots - 1) / slots;
-    const double cost = (double)waves * cps * (s_eff > 1 ? 1.5 : 1.0) + (s_eff > 1 ? 1.0 : 0.0);
+    // span states go to scratch and back four times (span pass, scan read and
+    // write, prefix read): charged at ~6 TB/s against ~4 us per chunk step
+    const double scratch_bytes = (double)heads * s_eff * state_floats_per_head(c) * 4.0;
+    const double scratch_cost = s_eff > 1 ? 2.0 + 4.0 * scratch_bytes / 6e12 / 4e-6 : 0.0;
+    if (s_eff > 1 && scratch_bytes > (double)(1ull << 30)) continue;
+    const double cost = (double)waves * cps * (s_eff > 1 ? 1.5 : 1.0) + scratch_cost;
     if (cost < best_cost - 1e-9) { best_cost = cost; best_s = (int)s_eff; }
   }
   int wmax = 0;
