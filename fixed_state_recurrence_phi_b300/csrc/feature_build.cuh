@@ -8,11 +8,13 @@
 // C(d+m-1, m) wide).
 //
 // One thread owns one token and holds its d inputs in registers; every feature
-// index, factor index and weight is a compile-time constant, so each feature
-// costs one multiply once the compiler has shared the run products x_i x_j (and
-// x_i x_j w) between the features of a run. Features are written as bf16, 8 at
-// a time (16 bytes), into the core-matrix tiles read by tcgen05.mma.
+// index, factor index and weight is a compile-time constant. A feature is
+// m * y with y its last input factor and m the run product x_i x_j w shared by
+// the features of a run; two features come from one bf16x2 multiply, whose
+// packed operands the compiler shares along the run. Features are written as
+// bf16, 8 at a time (16 bytes), into the core-matrix tiles read by tcgen05.mma.
 #pragma once
+#include <cuda_bf16.h>
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -50,13 +52,45 @@ __device__ __forceinline__ float feat_value(const float (&x)[DK + 1]) {
   }
 }
 
+// Feature A as a product m * y of two factors: y is the last input factor of
+// the monomial (exact in bf16, the inputs being bf16), m the rest including
+// the weight.
+template <int DK, int NT, int A>
+__device__ __forceinline__ void feat_factors(const float (&x)[DK + 1], float& m, float& y) {
+  using FC = FeatConst<DK, NT>;
+  if constexpr (A >= FC::D) {
+    m = 0.0f; y = 0.0f;
+  } else {
+    constexpr uint32_t cd = FC::tab.code[A];
+    constexpr int i = cd & 255, j = (cd >> 8) & 255, l = (cd >> 16) & 255;
+    constexpr float w = FC::tab.w[A];
+    if constexpr (i == DK) { m = x[DK]; y = 1.0f; }
+    else if constexpr (j == DK) { m = 1.0f; y = x[i]; }
+    else if constexpr (l == DK) { m = (w == 1.0f) ? x[i] : x[i] * w; y = x[j]; }
+    else { m = (w == 1.0f) ? x[i] * x[j] : (x[i] * x[j]) * w; y = x[l]; }
+  }
+}
+
+// Two features in one bf16x2 multiply: (m_a, m_b) * (y_a, y_b). The packed
+// factor pairs repeat along a run of monomials and are shared by the compiler.
+template <int DK, int NT, int A>
+__device__ __forceinline__ uint32_t feat2(const float (&x)[DK + 1]) {
+  float ma, ya, mb, yb;
+  feat_factors<DK, NT, A>(x, ma, ya);
+  feat_factors<DK, NT, A + 1>(x, mb, yb);
+  const uint32_t m = tc::pack_bf16x2(ma, mb), y = tc::pack_bf16x2(ya, yb);
+  const __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&m),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&y));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
 template <int DK, int NT, int A>
 __device__ __forceinline__ uint4 feat8(const float (&x)[DK + 1]) {
   uint4 r;
-  r.x = tc::pack_bf16x2(feat_value<DK, NT, A + 0>(x), feat_value<DK, NT, A + 1>(x));
-  r.y = tc::pack_bf16x2(feat_value<DK, NT, A + 2>(x), feat_value<DK, NT, A + 3>(x));
-  r.z = tc::pack_bf16x2(feat_value<DK, NT, A + 4>(x), feat_value<DK, NT, A + 5>(x));
-  r.w = tc::pack_bf16x2(feat_value<DK, NT, A + 6>(x), feat_value<DK, NT, A + 7>(x));
+  r.x = feat2<DK, NT, A + 0>(x);
+  r.y = feat2<DK, NT, A + 2>(x);
+  r.z = feat2<DK, NT, A + 4>(x);
+  r.w = feat2<DK, NT, A + 6>(x);
   return r;
 }
 

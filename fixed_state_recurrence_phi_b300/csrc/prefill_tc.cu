@@ -88,7 +88,13 @@ bool tc_slicing(int dk, int nt, int dv, TcSlicing* ts) {
   ts->nb = nb;
   ts->n_slices = s;
   ts->nmax = wbig + 16;
-  ts->smem = TcSmem(dk, ts->nmax, nb).total;
+  // three ring slots hide the issuer <-> worker round trip; two if they do not fit
+  ts->ring = TC_MAX_RING;
+  ts->smem = TcSmem(dk, ts->nmax, nb, ts->ring).total;
+  if (ts->smem > kSmemLimit) {
+    ts->ring = 2;
+    ts->smem = TcSmem(dk, ts->nmax, nb, ts->ring).total;
+  }
   return ts->smem <= kSmemLimit;
 }
 
@@ -135,38 +141,19 @@ tsa_status make_tmap(CUtensorMap* m, const void* base, int inner, long long N, i
   return TSA_OK;
 }
 
-// Launch `kernel` over `grid` CTAs in clusters of NS (the value slices of one
-// head and span share their feature tiles through distributed shared memory).
-template <int NS, typename Kern, typename... Args>
-cudaError_t launch_clustered(Kern kernel, unsigned grid, int smem, cudaStream_t s, Args... args) {
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg;
-  memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(TC_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = NS;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kernel, args...);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+template <typename Kern>
+cudaError_t set_smem(Kern kernel, int smem) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
-template <int DK, int NT, int NS>
+template <int DK, int NT>
 tsa_status launch_tc(const tsa_plan& pl, const TcSlicing& ts, const PrefillParams& pp, cudaStream_t s) {
   TcParams p;
   memset(&p, 0, sizeof(p));
   p.out = pp.out; p.states = pp.states; p.scratch = pp.scratch;
   p.N = pp.N; p.heads = pp.heads; p.dv = pp.dv; p.n_spans = pl.n_spans;
   p.chunks_per_span = pl.chunks_per_span; p.accumulate = pp.accumulate;
-  p.n_slices = ts.n_slices; p.nmax = ts.nmax;
+  p.n_slices = ts.n_slices; p.nmax = ts.nmax; p.ring = ts.ring;
   for (int k = 0; k < ts.n_slices; ++k) { p.slice_c0[k] = ts.c0[k]; p.slice_w[k] = ts.w[k]; }
   tsa_status st = device_error_word(&p.err);
   if (st != TSA_OK) return st;
@@ -178,7 +165,10 @@ tsa_status launch_tc(const tsa_plan& pl, const TcSlicing& ts, const PrefillParam
   const int smem = (int)ts.smem;
   cudaError_t e;
   if (pl.n_spans > 1) {
-    e = launch_clustered<NS>(span_state_tc_kernel<DK, NT, NS>, grid, smem, s, p, mk, mv);
+    e = set_smem(span_state_tc_kernel<DK, NT>, smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_state_tc)");
+    span_state_tc_kernel<DK, NT><<<grid, TC_THREADS, smem, s>>>(p, mk, mv);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch span_state_tc");
     const int elems4 = (int)(round_up(feat_dim(DK, NT), 4) * (pp.dv + 1) / 4);
     dim3 g2((elems4 + 255) / 256, pp.heads);
@@ -186,19 +176,12 @@ tsa_status launch_tc(const tsa_plan& pl, const TcSlicing& ts, const PrefillParam
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch span_scan");
   }
-  e = launch_clustered<NS>(span_output_tc_kernel<__nv_bfloat16, DK, NT, NS>, grid, smem, s, p, mq, mk, mv);
+  e = set_smem(span_output_tc_kernel<__nv_bfloat16, DK, NT>, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_output_tc)");
+  span_output_tc_kernel<__nv_bfloat16, DK, NT><<<grid, TC_THREADS, smem, s>>>(p, mq, mk, mv);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch span_output_tc");
   return TSA_OK;
-}
-
-// The value slices of a head run as independent CTAs (each builds the whole
-// feature map). Sharing the feature tiles across a cluster of the slices
-// (NS > 1) is implemented, but its cluster-scope fence and release per tile
-// cost more than the feature work it saves (measured on B300: 2x slower at
-// d_k=16, n=4), so every launch uses NS = 1.
-template <int DK, int NT>
-tsa_status launch_tc_ns(const tsa_plan& pl, const TcSlicing& ts, const PrefillParams& pp, cudaStream_t s) {
-  return launch_tc<DK, NT, 1>(pl, ts, pp, s);
 }
 
 }  // namespace
@@ -208,7 +191,7 @@ tsa_status launch_prefill_tc(const tsa_config* c, const tsa_plan& pl, const Pref
   if (!tc_slicing(c->d_k, c->n_terms, c->d_v, &ts))
     return fail(TSA_ERR_UNSUPPORTED, "no tensor-core slicing for d_k=%d d_v=%d n=%d", c->d_k, c->d_v, c->n_terms);
 #define TSA_TC_CASE(DK, NT) \
-  if (c->d_k == DK && c->n_terms == NT) return launch_tc_ns<DK, NT>(pl, ts, p, s);
+  if (c->d_k == DK && c->n_terms == NT) return launch_tc<DK, NT>(pl, ts, p, s);
   TSA_TC_CASE(16, 1) TSA_TC_CASE(16, 2) TSA_TC_CASE(16, 3) TSA_TC_CASE(16, 4)
   TSA_TC_CASE(32, 1) TSA_TC_CASE(32, 2) TSA_TC_CASE(32, 3)
 #undef TSA_TC_CASE

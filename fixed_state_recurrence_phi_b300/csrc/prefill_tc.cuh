@@ -17,21 +17,30 @@
 //
 // On chip, per CTA (one head, one span of chunks, one slice of W value
 // columns): the fp32 state lives in TMEM as NB blocks of 128 feature rows x
-// (W + 16) columns; its bf16 copy (the B operand of the readout) in shared
-// memory. The accumulator of A and O shares a further max(128, W + 16)
-// columns. The feature tiles phi(Q_c), phi(K_c) are built 128 features at a
-// time by the CUDA cores; one tile layout serves phi(Q) as a K-major A operand
-// (readout, M = tokens) and phi(K) as an MN-major A operand (update,
+// (W + 16) columns, its bf16 copy (the B operand of the readout) in shared
+// memory. A and O share a further max(128, W + 16) TMEM columns. The feature
+// tiles phi(Q_c), phi(K_c) are built 128 features at a time by the CUDA cores
+// into a ring of 32 KB slots; one tile layout serves phi(Q) as a K-major A
+// operand (readout, M = tokens) and phi(K) as an MN-major A operand (update,
 // M = features).
+//
+// Warp roles: 8 worker warps (TMEM lane quarter = warp % 4, column half =
+// warp / 4) build P and the feature tiles, write the outputs and convert the
+// updated state to bf16; one issuer warp (one lane) issues the TMA loads and
+// the MMAs. They hand off through mbarriers only. Per chunk c the issuer runs
+//     P [V,1] -> readouts phi(Q_f) [S_f,z_f] -> (O complete) -> update 0 ->
+//     Q_{c+1} K_{c+1}^T (as soon as the workers have read O) -> updates 1..
+// so that A of the next chunk is ready when the workers finish the chunk.
 //
 // Shared-memory tiles (no swizzle; byte offsets of element (row, col)):
 //   sQ, sK : [e/8][t][8]              (TMA box; K-major, LBO 2048, SBO 128)
 //   sV     : [c/8][t][8]              (TMA box; MN-major B, LBO 128, SBO 2048)
-//   sP     : (i/8)*2048 + (j/8)*128 + (i%8)*16 + (j%8)*2   (K-major A)
-//   sPQ/sPK: (t/8)*2048 + (a/8)*128 + (t%8)*16 + (a%8)*2   (K-major A / MN-major A)
+//   P      : (i/8)*2048 + (j/8)*128 + (i%8)*16 + (j%8)*2   (K-major A)
+//   phi    : (t/8)*2048 + (a/8)*128 + (t%8)*16 + (a%8)*2   (K-major A / MN-major A)
 //   sS_f   : (c/8)*2048 + a*16 + (c%8)*2                   (MN-major B)
 // Every wait on an mbarrier is bounded; on time-out the CTA records an error
-// word, stops issuing work, and releases its TMEM.
+// word, stops issuing work, waits (bounded) for what it has in flight, and
+// releases its TMEM.
 #pragma once
 #include <cuda.h>
 #include "common.cuh"
@@ -44,6 +53,7 @@ constexpr int TC_C = 128;
 constexpr int TC_THREADS = 288;   // 8 worker warps + 1 issuer warp
 constexpr int TC_WORKERS = 256;
 constexpr int TC_MAX_SLICES = 4;
+constexpr int TC_MAX_RING = 3;
 constexpr uint64_t TC_WAIT_NS = 1000000000ull;   // 1 s per wait
 
 struct TcParams {
@@ -52,31 +62,32 @@ struct TcParams {
   float* scratch;    // [heads][n_spans][DPAD*(dv+1)] (n_spans > 1)
   int* err;          // device error word (set on a timed-out wait)
   long long N;
-  int heads, dv, n_spans, chunks_per_span, accumulate, n_slices, nmax;
+  int heads, dv, n_spans, chunks_per_span, accumulate, n_slices, nmax, ring;
   int slice_c0[TC_MAX_SLICES];
   int slice_w[TC_MAX_SLICES];
 };
 
-// Byte offsets of the shared-memory tiles (identical on host and device).
-// q, k, v tiles are double-buffered (the next chunk's tiles land by TMA while
-// the current chunk runs); two 32 KB ring slots hold the feature tiles (and P).
+// Byte offsets of the shared-memory tiles (identical on host and device):
+// q and k tiles (single), v tiles (double-buffered: the next chunk's lands by
+// TMA while the current one is still read by the update MMAs), `ring` slots of
+// 32 KB, the bf16 state copy (NB blocks), then the barriers.
 struct TcSmem {
   size_t xt, vt, s, sblk, bar, total;
-  __host__ __device__ TcSmem(int dk, int nmax, int nb) {
+  int ring;
+  __host__ __device__ TcSmem(int dk, int nmax, int nb, int ring_slots) {
+    ring = ring_slots;
     xt = (size_t)128 * dk * 2;
     vt = (size_t)128 * nmax * 2;
-    s = 4 * xt + 2 * vt + 2 * 32768;
+    s = 2 * xt + 2 * vt + (size_t)ring * 32768;
     sblk = vt;
     bar = s + (size_t)nb * sblk;
-    total = bar + 128;
+    total = bar + 256;
   }
-  __host__ __device__ size_t q(int b) const { return b * xt; }
-  __host__ __device__ size_t k(int b) const { return (2 + b) * xt; }
-  __host__ __device__ size_t v(int b) const { return 4 * xt + b * vt; }
-  __host__ __device__ size_t ring(int r) const { return 4 * xt + 2 * vt + r * 32768; }
+  __host__ __device__ size_t q() const { return 0; }
+  __host__ __device__ size_t k() const { return xt; }
+  __host__ __device__ size_t v(int b) const { return 2 * xt + b * vt; }
+  __host__ __device__ size_t slot(int r) const { return 2 * xt + 2 * vt + (size_t)r * 32768; }
 };
-
-__device__ __forceinline__ bool tc_any_fail(bool ok) { return __syncthreads_or(ok ? 0 : 1) != 0; }
 
 // The d inputs of token t from a [e/8][t][8] bf16 tile, as fp32.
 template <int DK>
@@ -158,134 +169,137 @@ __device__ __forceinline__ TcUnit tc_unit(const TcParams& p) {
 }
 
 // mbarriers of a CTA (shared memory, in this order) and their arrival counts:
-//   tfull[2]  TMA tiles of buffer b landed      (1 + tx bytes, issuer)
-//   tempty[2] workers are done reading buffer b  (8, one per worker warp)
-//   sfull[2]  workers wrote ring slot s          (8 per CTA of the cluster)
-//   sempty[2] the MMAs reading ring slot s done  (1 per CTA, multicast commit)
-//   qk        A = Q K^T is in TMEM               (1, commit)
-//   odone     O of the chunk is complete         (1, commit)
-//   ofree     workers have read O                (8)
-//   conv      workers converted the state blocks (8)
-//   chunk     every MMA of the chunk is done     (1, commit)
-//   drain     every MMA issued is done           (1, commit)
+//   qkfull     q, k tiles of the chunk landed          (1 + tx bytes)
+//   qkempty    workers have read q, k into registers   (8, one per worker warp)
+//   vfull[2]   v tile of buffer b landed               (1 + tx bytes)
+//   sfull[3]   workers wrote ring slot s               (8)
+//   sempty[3]  the MMAs reading ring slot s are done   (1, tcgen05.commit)
+//   qk         A = Q K^T is in TMEM                    (1, commit)
+//   odone      O of the chunk is complete              (1, commit)
+//   ofree      workers have read O                     (8)
+//   conv       workers converted the state blocks      (8)
+//   chunk      every MMA of the chunk is done          (1, commit)
+//   drain      every MMA issued is done                (1, commit)
 struct TcBars {
   uint64_t* b;
-  __device__ uint64_t* tfull(int i) const { return b + i; }
-  __device__ uint64_t* tempty(int i) const { return b + 2 + i; }
+  __device__ uint64_t* qkfull() const { return b + 0; }
+  __device__ uint64_t* qkempty() const { return b + 1; }
+  __device__ uint64_t* vfull(int i) const { return b + 2 + i; }
   __device__ uint64_t* sfull(int i) const { return b + 4 + i; }
-  __device__ uint64_t* sempty(int i) const { return b + 6 + i; }
-  __device__ uint64_t* qk() const { return b + 8; }
-  __device__ uint64_t* odone() const { return b + 9; }
-  __device__ uint64_t* ofree() const { return b + 10; }
-  __device__ uint64_t* conv() const { return b + 11; }
-  __device__ uint64_t* chunk() const { return b + 12; }
-  __device__ uint64_t* drain() const { return b + 13; }
-  __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(b + 14); }
-  __device__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(b + 14) + 1; }
-  // sfull collects one arrival per worker warp of every CTA of the cluster,
-  // sempty one (multicast) commit per CTA.
-  __device__ void init(int ns) const {
-    const uint32_t cnt[14] = {1, 1, 8, 8, 8u * ns, 8u * ns, (uint32_t)ns, (uint32_t)ns, 1, 1, 8, 8, 1, 1};
-    for (int k = 0; k < 14; ++k) tc::mbar_init(b + k, cnt[k]);
+  __device__ uint64_t* sempty(int i) const { return b + 7 + i; }
+  __device__ uint64_t* qk() const { return b + 10; }
+  __device__ uint64_t* odone() const { return b + 11; }
+  __device__ uint64_t* ofree() const { return b + 12; }
+  __device__ uint64_t* conv() const { return b + 13; }
+  __device__ uint64_t* chunk() const { return b + 14; }
+  __device__ uint64_t* drain() const { return b + 15; }
+  __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(b + 16); }
+  __device__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(b + 16) + 1; }
+  __device__ void init() const {
+    const uint32_t cnt[16] = {1, 8, 1, 1, 8, 8, 8, 1, 1, 1, 1, 1, 8, 8, 1, 1};
+    for (int k = 0; k < 16; ++k) tc::mbar_init(b + k, cnt[k]);
     *abort_flag() = 0;
     tc::mbar_fence_init();
   }
 };
 
-// Issue the TMA loads of one chunk (k and v; q too if `tq`) into buffer b.
-__device__ __forceinline__ void tc_issue_tiles(const TcSmem& L, uint8_t* smem, uint64_t* bar, int b,
-                                               const CUtensorMap* tq, const CUtensorMap* tk,
-                                               const CUtensorMap* tv, long long t0, int head, int c0, int W,
-                                               int dk) {
-  const uint32_t bytes = (uint32_t)((tq ? 2 : 1) * 128 * dk * 2 + 128 * W * 2);
-  tc::mbar_arrive_expect_tx(bar, bytes);
-  if (tq) tc::tma_load_4d(smem + L.q(b), tq, bar, 0, (int)t0, 0, head);
-  tc::tma_load_4d(smem + L.k(b), tk, bar, 0, (int)t0, 0, head);
-  for (int u = 0; u < W / 16; ++u)
-    tc::tma_load_4d(smem + L.v(b) + u * 4096, tv, bar, 0, (int)t0, (c0 + 16 * u) / 8, head);
+__device__ __forceinline__ bool tc_wait(const TcBars& B, uint64_t* bar, uint32_t parity) {
+  return tc::mbar_wait_or_abort(bar, parity, TC_WAIT_NS, B.abort_flag());
 }
-
-// A worker warp's side of the two-slot ring. A slot exists in every CTA of
-// the cluster and each CTA's workers write their share of it into all of them:
-// before writing slot s the warp waits until the MMAs of every CTA that read
-// the slot's previous contents are done (sempty counts one multicast commit
-// per CTA); after writing it arrives on sfull[s] of every CTA.
-template <int NS>
-struct TcWorkerRing {
-  uint32_t eph = 0, pend = 0;
-  uint32_t sfull_c[2][NS];   // shared::cluster addresses of sfull[s] in each CTA
-  __device__ __forceinline__ void setup(const TcBars& B) {
-#pragma unroll
-    for (int s = 0; s < 2; ++s)
-#pragma unroll
-      for (int r = 0; r < NS; ++r) sfull_c[s][r] = tc::mapa(tc::smem_u32(B.sfull(s)), (uint32_t)r);
-  }
-  __device__ __forceinline__ bool acquire(const TcBars& B, int s) {
-    if (!((pend >> s) & 1u)) return true;
-    const bool ok = (NS == 1)
-        ? tc::mbar_wait_or_abort(B.sempty(s), (eph >> s) & 1u, TC_WAIT_NS, B.abort_flag())
-        : tc::mbar_wait_cluster_or_abort(B.sempty(s), (eph >> s) & 1u, TC_WAIT_NS, B.abort_flag());
-    eph ^= 1u << s;
-    pend &= ~(1u << s);
-    return __all_sync(0xffffffffu, ok);   // the whole warp gives up together
-  }
-  __device__ __forceinline__ void release(const TcBars& B, int s, int lane) {
-    if constexpr (NS == 1) tc::fence_proxy_async();
-    else tc::fence_proxy_async_cluster();
-    tc::fence_before_sync();
-    __syncwarp();
-    if (lane == 0) {
-      if constexpr (NS == 1) {
-        tc::mbar_arrive(B.sfull(s));
-      } else {
-#pragma unroll
-        for (int r = 0; r < NS; ++r) tc::mbar_arrive_cluster(s ? sfull_c[1][r] : sfull_c[0][r]);
-      }
-    }
-    pend |= 1u << s;
-  }
-};
-
+// A worker warp waits as one: if any lane gives up, the whole warp does.
+__device__ __forceinline__ bool tc_wait_warp(const TcBars& B, uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, tc_wait(B, bar, parity));
+}
 __device__ __forceinline__ void tc_warp_arrive(uint64_t* bar, int lane) {
   tc::fence_before_sync();
   __syncwarp();
   if (lane == 0) tc::mbar_arrive(bar);
 }
 
-// The issuer frees ring slot s in every CTA of the cluster once its MMAs are done.
-template <int NS>
-__device__ __forceinline__ void tc_commit_slot(const TcBars& B, int s) {
-  if constexpr (NS == 1) tc::mma_commit(B.sempty(s));
-  else tc::mma_commit_multicast(B.sempty(s), (uint16_t)((1u << NS) - 1u));
+// TMA loads of the q, k tiles of the chunk at t0 (q too if `tq`).
+__device__ __forceinline__ void tc_issue_qk(const TcSmem& L, uint8_t* smem, uint64_t* bar,
+                                            const CUtensorMap* tq, const CUtensorMap* tk, long long t0, int head,
+                                            int dk) {
+  if (!tc::elect_one()) return;
+  tc::mbar_arrive_expect_tx(bar, (uint32_t)((tq ? 2 : 1) * 128 * dk * 2));
+  if (tq) tc::tma_load_4d(smem + L.q(), tq, bar, 0, (int)t0, 0, head);
+  tc::tma_load_4d(smem + L.k(), tk, bar, 0, (int)t0, 0, head);
 }
+// TMA loads of the W value columns c0.. of the chunk at t0 into buffer b.
+__device__ __forceinline__ void tc_issue_v(const TcSmem& L, uint8_t* smem, uint64_t* bar, int b,
+                                           const CUtensorMap* tv, long long t0, int head, int c0, int W) {
+  if (!tc::elect_one()) return;
+  tc::mbar_arrive_expect_tx(bar, (uint32_t)(128 * W * 2));
+  for (int u = 0; u < W / 16; ++u)
+    tc::tma_load_4d(smem + L.v(b) + u * 4096, tv, bar, 0, (int)t0, (c0 + 16 * u) / 8, head);
+}
+
+// Ring position shared (in lock step) by the issuer and the workers: uses go
+// to slots 0, 1, .., R-1, 0, ..
+struct TcRingPos {
+  int s = 0, R = 2;
+  __device__ __forceinline__ void next() { s = (s + 1 == R) ? 0 : s + 1; }
+};
+
+// A worker warp's side of the ring: before writing slot s it waits for the
+// commit of the MMAs that read the slot's previous contents; after writing it
+// publishes the slot (one arrival per warp).
+struct TcWorkerRing {
+  uint32_t eph = 0, pend = 0;
+  __device__ __forceinline__ bool acquire(const TcBars& B, int s) {
+    if (!((pend >> s) & 1u)) return true;
+    const bool ok = tc_wait_warp(B, B.sempty(s), (eph >> s) & 1u);
+    eph ^= 1u << s;
+    pend &= ~(1u << s);
+    return ok;
+  }
+  __device__ __forceinline__ void release(const TcBars& B, int s, int lane) {
+    tc::fence_proxy_async();
+    tc_warp_arrive(B.sfull(s), lane);
+    pend |= 1u << s;
+  }
+};
+
+// The issuer's side: wait until every worker warp has written slot s.
+struct TcIssuerRing {
+  uint32_t fph = 0;
+  __device__ __forceinline__ bool take(const TcBars& B, int s) {
+    const bool ok = tc_wait_warp(B, B.sfull(s), (fph >> s) & 1u);
+    fph ^= 1u << s;
+    tc::fence_after_sync();
+    return ok;
+  }
+};
 
 // The issuer's last act: wait (bounded) until every MMA it issued and every
 // TMA load it requested has completed, so that the tensor memory can be freed.
-__device__ __forceinline__ void tc_issuer_drain(const TcBars& B, int filled, int consumed) {
-  tc::mma_commit(B.drain());
+__device__ __forceinline__ void tc_issuer_drain(const TcBars& B, int qk_req, int qk_got, int v_req, int v_got) {
+  tc::mma_commit_elect(B.drain());
   tc::mbar_wait(B.drain(), 0, TC_WAIT_NS);
-  for (; consumed < filled; ++consumed) tc::mbar_wait(B.tfull(consumed & 1), (consumed >> 1) & 1u, TC_WAIT_NS);
+  for (; qk_got < qk_req; ++qk_got) tc::mbar_wait(B.qkfull(), qk_got & 1u, TC_WAIT_NS);
+  for (; v_got < v_req; ++v_got) tc::mbar_wait(B.vfull(v_got & 1), (v_got >> 1) & 1u, TC_WAIT_NS);
 }
 
 // ---------------------------------------------------------------------------
 // span_state_tc: the state sum of one span (one slice) -> scratch.
-// Workers build phi(K) blocks into the ring; the issuer runs the update MMAs.
+// Workers build phi(K) blocks into the ring; the issuer runs the update MMAs
+// and keeps the k and v tiles one chunk ahead.
 // ---------------------------------------------------------------------------
-template <int DK, int NT, int NS>
+template <int DK, int NT>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 span_state_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v) {
   using FC = FeatConst<DK, NT>;
   constexpr int D = FC::D, NB = FC::NB, DPAD = round_up(D, 4);
   extern __shared__ __align__(1024) uint8_t smem[];
-  const TcSmem L(DK, p.nmax, NB);
+  const TcSmem L(DK, p.nmax, NB, p.ring);
   const TcBars B{reinterpret_cast<uint64_t*>(smem + L.bar)};
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wq = warp & 3, half = (warp >> 2) & 1;
   const TcUnit u = tc_unit(p);
   const int nm = u.nm;
 
   if (warp == 0) tc::tmem_alloc(B.tmem_slot(), 512);
-  if (tid == 0) B.init(NS);
+  if (tid == 0) B.init();
   if (tid < TC_WORKERS) {
     tc_write_ones(smem + L.v(0), u.W, tid);
     tc_write_ones(smem + L.v(1), u.W, tid);
@@ -293,85 +307,72 @@ span_state_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   tc::fence_proxy_async();
   tc::fence_before_sync();
   __syncthreads();
-  if constexpr (NS > 1) tc::cluster_sync();   // every peer's barriers exist before any remote arrival
   tc::fence_after_sync();
   const uint32_t tm = *B.tmem_slot();
   const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-  volatile int* abort_flag = B.abort_flag();
-  const int rank = (NS > 1) ? (int)tc::cluster_rank() : 0;
+  TcRingPos pos;
+  pos.R = p.ring;
 
   if (warp == 8) {
-    if (lane == 0) {
+    {   // the whole issuer warp runs the loop; one elected lane issues
       const uint32_t id_up = tc::idesc_bf16(128, nm, true, true);
-      const uint32_t aRing0 = tc::smem_u32(smem + L.ring(0));
-      uint32_t fph = 0;
-      int r = 0, filled = 0, consumed = 0;
+      TcIssuerRing ring;
+      int qk_req = 0, qk_got = 0, v_req = 0, v_got = 0;
       if (u.n_chunks > 0) {
-        tc_issue_tiles(L, smem, B.tfull(0), 0, nullptr, &tm_k, &tm_v, u.t_begin, u.head, u.c0, u.W, DK);
-        filled = 1;
+        tc_issue_qk(L, smem, B.qkfull(), nullptr, &tm_k, u.t_begin, u.head, DK);
+        tc_issue_v(L, smem, B.vfull(0), 0, &tm_v, u.t_begin, u.head, u.c0, u.W);
+        qk_req = v_req = 1;
       }
       for (int c = 0; c < u.n_chunks; ++c) {
         const int buf = c & 1;
-        if (!tc::mbar_wait_or_abort(B.tfull(buf), (c >> 1) & 1u, TC_WAIT_NS, abort_flag)) break;
-        ++consumed;
-        if (c > 0 && !tc::mbar_wait_or_abort(B.chunk(), (c - 1) & 1u, TC_WAIT_NS, abort_flag)) break;
+        const long long t0 = u.t_begin + (long long)c * TC_C;
+        if (!tc_wait_warp(B, B.qkfull(), c & 1u)) break;
+        ++qk_got;
         if (c + 1 < u.n_chunks) {
-          if (c + 1 >= 2 &&
-              !tc::mbar_wait_or_abort(B.tempty(buf ^ 1), ((c - 1) >> 1) & 1u, TC_WAIT_NS, abort_flag))
-            break;
-          tc_issue_tiles(L, smem, B.tfull(buf ^ 1), buf ^ 1, nullptr, &tm_k, &tm_v, u.t_begin + (c + 1) * TC_C,
-                         u.head, u.c0, u.W, DK);
-          ++filled;
+          if (!tc_wait_warp(B, B.qkempty(), c & 1u)) break;   // workers have the k inputs in registers
+          tc_issue_qk(L, smem, B.qkfull(), nullptr, &tm_k, t0 + TC_C, u.head, DK);
+          ++qk_req;
         }
-        const uint32_t aV = tc::smem_u32(smem + L.v(buf));
+        if (c > 0 && !tc_wait_warp(B, B.chunk(), (c - 1) & 1u)) break;   // v buffer buf^1 is free again
+        if (c + 1 < u.n_chunks) {
+          tc_issue_v(L, smem, B.vfull(buf ^ 1), buf ^ 1, &tm_v, t0 + TC_C, u.head, u.c0, u.W);
+          ++v_req;
+        }
+        if (!tc_wait_warp(B, B.vfull(buf), (c >> 1) & 1u)) break;
+        ++v_got;
+        const uint64_t dV = tc::sdesc(tc::smem_u32(smem + L.v(buf)), 128, 2048);
         bool ok = true;
-        for (int f = 0; f < NB; ++f, ++r) {
-          const int s = r & 1;
-          ok = (NS == 1) ? tc::mbar_wait_or_abort(B.sfull(s), (fph >> s) & 1u, TC_WAIT_NS, abort_flag)
-                         : tc::mbar_wait_cluster_or_abort(B.sfull(s), (fph >> s) & 1u, TC_WAIT_NS, abort_flag);
-          fph ^= 1u << s;
-          if (!ok) break;
-          tc::fence_after_sync();
-          const uint32_t aA = aRing0 + (uint32_t)s * 32768u;
+        for (int f = 0; f < NB; ++f, pos.next()) {
+          if (!(ok = ring.take(B, pos.s))) break;
+          const uint64_t dA = tc::sdesc(tc::smem_u32(smem + L.slot(pos.s)), 2048, 128);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            tc::mma_bf16(tm + f * nm, (tc::sdesc(aA, 2048, 128) + (uint64_t)(k * 256)), (tc::sdesc(aV, 128, 2048) + (uint64_t)(k * 16)),
-                         id_up, (k > 0 || c > 0) ? 1u : 0u);
-          tc_commit_slot<NS>(B, s);
+            tc::mma_bf16_elect(tm + f * nm, dA + (uint64_t)(k * 256), dV + (uint64_t)(k * 16), id_up,
+                         (k > 0 || c > 0) ? 1u : 0u);
+          tc::mma_commit_elect(B.sempty(pos.s));
         }
         if (!ok) break;
-        tc::mma_commit(B.chunk());
+        tc::mma_commit_elect(B.chunk());
       }
-      tc_issuer_drain(B, filled, consumed);
+      tc_issuer_drain(B, qk_req, qk_got, v_req, v_got);
     }
   } else {
     const int t = tid & 127;
     const int prow = (t / 8) * 2048 + (t % 8) * 16;
-    TcWorkerRing<NS> ring;
-    ring.setup(B);
-    uint32_t rc0[NS];   // ring slot 0 of every CTA, shared::cluster addresses
-#pragma unroll
-    for (int q = 0; q < NS; ++q) rc0[q] = tc::mapa(tc::smem_u32(smem + L.ring(0)), (uint32_t)q);
-    int r = 0;
+    TcWorkerRing ring;
     for (int c = 0; c < u.n_chunks; ++c) {
       const long long t0 = u.t_begin + (long long)c * TC_C;
-      const int buf = c & 1;
       const int valid = (int)min((long long)TC_C, u.t_end - t0);
-      if (!__all_sync(0xffffffffu, tc::mbar_wait_or_abort(B.tfull(buf), (c >> 1) & 1u, TC_WAIT_NS, abort_flag)))
-        break;
+      if (!tc_wait_warp(B, B.qkfull(), c & 1u)) break;
       float xk[DK + 1];
-      tc_load_x<DK>(smem + L.k(buf), t, xk);
+      tc_load_x<DK>(smem + L.k(), t, xk);
       xk[DK] = (t < valid) ? 1.0f : 0.0f;
-      tc_warp_arrive(B.tempty(buf), lane);
+      tc_warp_arrive(B.qkempty(), lane);
       bool ok = true;
-      for (int f = 0; f < NB; ++f, ++r) {
-        const int s = r & 1;
-        if (!(ok = ring.acquire(B, s))) break;
-        uint32_t rem[NS];
-#pragma unroll
-        for (int q = 0; q < NS; ++q) rem[q] = rc0[q] + (uint32_t)s * 32768u + (uint32_t)prow;
-        build_phi_rank<DK, NT, NS>(rank, f, half, xk, smem + L.ring(s) + prow, rem);
-        ring.release(B, s, lane);
+      for (int f = 0; f < NB; ++f, pos.next()) {
+        if (!(ok = ring.acquire(B, pos.s))) break;
+        build_phi_rank<DK, NT, 1>(0, f, half, xk, smem + L.slot(pos.s) + prow, nullptr);
+        ring.release(B, pos.s, lane);
       }
       if (!ok) break;
     }
@@ -379,7 +380,7 @@ span_state_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const bool aborted = *abort_flag != 0;
+  const bool aborted = *B.abort_flag() != 0;
   if (!aborted && tid < TC_WORKERS) {
     float* dst = p.scratch + ((size_t)u.head * p.n_spans + u.span) * (size_t)DPAD * (p.dv + 1);
     tc_store_state<D, DPAD, NB>(dst, tm, lane_off, nm, u.W, u.c0, p.dv, u.slice == 0, wq, lane, half);
@@ -387,7 +388,6 @@ span_state_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   if (aborted && tid == 0) atomicExch(p.err, 1);
   tc::fence_before_sync();
   __syncthreads();
-  if constexpr (NS > 1) tc::cluster_sync();   // no peer still writes into this CTA
   if (warp == 0) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tm, 512);
@@ -396,21 +396,15 @@ span_state_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
 
 // ---------------------------------------------------------------------------
 // span_output_tc: outputs of one span (one slice), state carried in TMEM.
-// Per chunk the issuer runs Q K^T, then P [V,1] (P from ring slot), the NB
-// readout MMAs phi(Q_f) [S_f, z_f] (O complete -> odone), and the NB update
-// MMAs phi(K_f)^T [V,1] into the TMEM state; the workers turn A into P, build
-// phi(Q_f) then phi(K_f) into the ring one block ahead of the MMAs, write the
-// output once O is complete, and convert each updated state block to its bf16
-// copy for the next chunk's readout. The next chunk's tiles land meanwhile.
 // ---------------------------------------------------------------------------
-template <typename T, int DK, int NT, int NS>
+template <typename T, int DK, int NT>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   using FC = FeatConst<DK, NT>;
   constexpr int D = FC::D, NB = FC::NB, DPAD = round_up(D, 4);
   extern __shared__ __align__(1024) uint8_t smem[];
-  const TcSmem L(DK, p.nmax, NB);
+  const TcSmem L(DK, p.nmax, NB, p.ring);
   const TcBars B{reinterpret_cast<uint64_t*>(smem + L.bar)};
   uint8_t* sS = smem + L.s;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wq = warp & 3, half = (warp >> 2) & 1;
@@ -420,7 +414,7 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
   const size_t st_elems = (size_t)DPAD * (p.dv + 1);
 
   if (warp == 0) tc::tmem_alloc(B.tmem_slot(), 512);
-  if (tid == 0) B.init(NS);
+  if (tid == 0) B.init();
   if (tid < TC_WORKERS) {
     tc_write_ones(smem + L.v(0), W, tid);
     tc_write_ones(smem + L.v(1), W, tid);
@@ -432,7 +426,6 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
   const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
   const uint32_t col_O = (uint32_t)(NB * nm);
   const int i = wq * 32 + lane;   // TMEM lane = query row / feature row of a block
-  volatile int* abort_flag = B.abort_flag();
 
   // initial state: span prefix (several spans), caller's state (ACCUMULATE) or 0
   if (tid < TC_WORKERS) {
@@ -467,102 +460,106 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
   tc::fence_proxy_async();
   tc::fence_before_sync();
   __syncthreads();
-  if constexpr (NS > 1) tc::cluster_sync();   // every peer's barriers exist before any remote arrival
   tc::fence_after_sync();
-  const int rank = (NS > 1) ? (int)tc::cluster_rank() : 0;
+  TcRingPos pos;
+  pos.R = p.ring;
 
   if (warp == 8) {
     // ------------------------------ issuer ---------------------------------
-    if (lane == 0) {
+    {   // the whole issuer warp runs the loop; one elected lane issues
       const uint32_t id_qk = tc::idesc_bf16(128, 128, false, false);
       const uint32_t id_pv = tc::idesc_bf16(128, nm, false, true);
       const uint32_t id_up = tc::idesc_bf16(128, nm, true, true);
-      const uint32_t aRing0 = tc::smem_u32(smem + L.ring(0));
+      const uint64_t dQ = tc::sdesc(tc::smem_u32(smem + L.q()), 2048, 128);
+      const uint64_t dK = tc::sdesc(tc::smem_u32(smem + L.k()), 2048, 128);
       const uint32_t aS = tc::smem_u32(sS);
-      uint32_t fph = 0;
-      int r = 0, filled = 0, consumed = 0;
-      auto wait = [&](uint64_t* bar, uint32_t par) {
-        return tc::mbar_wait_or_abort(bar, par, TC_WAIT_NS, abort_flag);
-      };
-      auto take_slot = [&](int s) {
-        const bool ok = (NS == 1)
-            ? tc::mbar_wait_or_abort(B.sfull(s), (fph >> s) & 1u, TC_WAIT_NS, abort_flag)
-            : tc::mbar_wait_cluster_or_abort(B.sfull(s), (fph >> s) & 1u, TC_WAIT_NS, abort_flag);
-        fph ^= 1u << s;
-        tc::fence_after_sync();
-        return ok;
-      };
-      if (u.n_chunks > 0) {
-        tc_issue_tiles(L, smem, B.tfull(0), 0, &tm_q, &tm_k, &tm_v, u.t_begin, u.head, u.c0, W, DK);
-        filled = 1;
-      }
-      for (int c = 0; c < u.n_chunks; ++c) {
-        const int buf = c & 1;
-        const bool need_update = single || (c + 1 < u.n_chunks);
-        if (!wait(B.tfull(buf), (c >> 1) & 1u)) break;
-        ++consumed;
-        if (c > 0 && !wait(B.ofree(), (c - 1) & 1u)) break;
-        tc::fence_after_sync();
-        const uint32_t aQ = tc::smem_u32(smem + L.q(buf)), aK = tc::smem_u32(smem + L.k(buf));
-        const uint32_t aV = tc::smem_u32(smem + L.v(buf));
+      TcIssuerRing ring;
+      int qk_req = 0, qk_got = 0, v_req = 0, v_got = 0;
+      auto issue_qk_mma = [&]() {
 #pragma unroll
         for (int k = 0; k < DK / 16; ++k)
-          tc::mma_bf16(tm + col_O, (tc::sdesc(aQ, 2048, 128) + (uint64_t)(k * 256)), (tc::sdesc(aK, 2048, 128) + (uint64_t)(k * 256)),
-                       id_qk, k > 0 ? 1u : 0u);
-        tc::mma_commit(B.qk());
-        // the previous chunk's MMAs (readers of buffer buf^1) must be done
-        if (c > 0 && !wait(B.chunk(), (c - 1) & 1u)) break;
-        if (c + 1 < u.n_chunks) {
-          if (c + 1 >= 2 && !wait(B.tempty(buf ^ 1), ((c - 1) >> 1) & 1u)) break;
-          tc_issue_tiles(L, smem, B.tfull(buf ^ 1), buf ^ 1, &tm_q, &tm_k, &tm_v, u.t_begin + (c + 1) * TC_C,
-                         u.head, u.c0, W, DK);
-          ++filled;
+          tc::mma_bf16_elect(tm + col_O, dQ + (uint64_t)(k * 256), dK + (uint64_t)(k * 256), id_qk, k > 0 ? 1u : 0u);
+        tc::mma_commit_elect(B.qk());
+      };
+      bool ok = true;
+      if (u.n_chunks > 0) {
+        tc_issue_qk(L, smem, B.qkfull(), &tm_q, &tm_k, u.t_begin, u.head, DK);
+        tc_issue_v(L, smem, B.vfull(0), 0, &tm_v, u.t_begin, u.head, u.c0, W);
+        qk_req = v_req = 1;
+        ok = tc_wait_warp(B, B.qkfull(), 0u);
+        if (ok) {
+          ++qk_got;
+          tc::fence_after_sync();
+          issue_qk_mma();   // A of chunk 0
         }
+      }
+      for (int c = 0; c < u.n_chunks && ok; ++c) {
+        const int buf = c & 1;
+        const long long t0 = u.t_begin + (long long)c * TC_C;
+        const bool need_update = single || (c + 1 < u.n_chunks);
+        const bool has_next = (c + 1 < u.n_chunks);
+        // q, k tiles of the next chunk: once the workers hold this chunk's in
+        // registers and Q K^T of this chunk (the other reader) has completed
+        if (has_next) {
+          if (!(ok = tc_wait_warp(B, B.qkempty(), c & 1u))) break;
+          if (!(ok = tc_wait_warp(B, B.qk(), c & 1u))) break;
+          tc_issue_qk(L, smem, B.qkfull(), &tm_q, &tm_k, t0 + TC_C, u.head, DK);
+          ++qk_req;
+        }
+        // v tile of the next chunk into the buffer the previous chunk used
+        if (c > 0 && !(ok = tc_wait_warp(B, B.chunk(), (c - 1) & 1u))) break;
+        if (has_next) {
+          tc_issue_v(L, smem, B.vfull(buf ^ 1), buf ^ 1, &tm_v, t0 + TC_C, u.head, u.c0, W);
+          ++v_req;
+        }
+        if (!(ok = tc_wait_warp(B, B.vfull(buf), (c >> 1) & 1u))) break;
+        ++v_got;
+        const uint64_t dV = tc::sdesc(tc::smem_u32(smem + L.v(buf)), 128, 2048);
         // O = P [V, 1]
+        if (!(ok = ring.take(B, pos.s))) break;
         {
-          const int s = r & 1;
-          if (!take_slot(s)) break;
-          const uint32_t aA = aRing0 + (uint32_t)s * 32768u;
+          const uint64_t dP = tc::sdesc(tc::smem_u32(smem + L.slot(pos.s)), 128, 2048);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            tc::mma_bf16(tm + col_O, (tc::sdesc(aA, 128, 2048) + (uint64_t)(k * 16)), (tc::sdesc(aV, 128, 2048) + (uint64_t)(k * 16)),
-                         id_pv, k > 0 ? 1u : 0u);
-          tc_commit_slot<NS>(B, s);
-          ++r;
+            tc::mma_bf16_elect(tm + col_O, dP + (uint64_t)(k * 16), dV + (uint64_t)(k * 16), id_pv, k > 0 ? 1u : 0u);
+          tc::mma_commit_elect(B.sempty(pos.s));
+          pos.next();
         }
-        if (c > 0 && !wait(B.conv(), (c - 1) & 1u)) break;
-        bool ok = true;
+        // the bf16 state copy must hold S_{<c} (converted by the workers)
+        if (c > 0 && !(ok = tc_wait_warp(B, B.conv(), (c - 1) & 1u))) break;
         // O += phi(Q_f) [S_f, z_f]
-        for (int f = 0; f < NB; ++f, ++r) {
-          const int s = r & 1;
-          if (!(ok = take_slot(s))) break;
-          const uint32_t aA = aRing0 + (uint32_t)s * 32768u;
-          const uint32_t aSf = aS + (uint32_t)(f * L.sblk);
+        for (int f = 0; f < NB; ++f, pos.next()) {
+          if (!(ok = ring.take(B, pos.s))) break;
+          const uint64_t dA = tc::sdesc(tc::smem_u32(smem + L.slot(pos.s)), 128, 2048);
+          const uint64_t dS = tc::sdesc(aS + (uint32_t)(f * L.sblk), 128, 2048);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            tc::mma_bf16(tm + col_O, (tc::sdesc(aA, 128, 2048) + (uint64_t)(k * 16)), (tc::sdesc(aSf, 128, 2048) + (uint64_t)(k * 16)),
-                         id_pv, 1u);
-          tc_commit_slot<NS>(B, s);
+            tc::mma_bf16_elect(tm + col_O, dA + (uint64_t)(k * 16), dS + (uint64_t)(k * 16), id_pv, 1u);
+          tc::mma_commit_elect(B.sempty(pos.s));
         }
         if (!ok) break;
-        tc::mma_commit(B.odone());
-        // S_f += phi(K_f)^T [V, 1]
-        if (need_update) {
-          for (int f = 0; f < NB; ++f, ++r) {
-            const int s = r & 1;
-            if (!(ok = take_slot(s))) break;
-            const uint32_t aA = aRing0 + (uint32_t)s * 32768u;
+        tc::mma_commit_elect(B.odone());
+        // S_f += phi(K_f)^T [V, 1]; after block 0, the next chunk's Q K^T as
+        // soon as the workers have read O (A and O share their TMEM columns)
+        for (int f = 0; f < (need_update ? NB : 0); ++f, pos.next()) {
+          if (!(ok = ring.take(B, pos.s))) break;
+          const uint64_t dA = tc::sdesc(tc::smem_u32(smem + L.slot(pos.s)), 2048, 128);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              tc::mma_bf16(tm + f * nm, (tc::sdesc(aA, 2048, 128) + (uint64_t)(k * 256)), (tc::sdesc(aV, 128, 2048) + (uint64_t)(k * 16)),
-                           id_up, 1u);
-            tc_commit_slot<NS>(B, s);
+          for (int k = 0; k < 8; ++k)
+            tc::mma_bf16_elect(tm + f * nm, dA + (uint64_t)(k * 256), dV + (uint64_t)(k * 16), id_up, 1u);
+          tc::mma_commit_elect(B.sempty(pos.s));
+          if (f == 0 && has_next) {
+            if (!(ok = tc_wait_warp(B, B.ofree(), c & 1u))) break;
+            if (!(ok = tc_wait_warp(B, B.qkfull(), (c + 1) & 1u))) break;
+            ++qk_got;
+            tc::fence_after_sync();
+            issue_qk_mma();
           }
-          if (!ok) break;
         }
-        tc::mma_commit(B.chunk());
+        if (!ok) break;
+        tc::mma_commit_elect(B.chunk());
       }
-      tc_issuer_drain(B, filled, consumed);
+      tc_issuer_drain(B, qk_req, qk_got, v_req, v_got);
     }
   } else {
     // ------------------------------ workers --------------------------------
@@ -570,18 +567,7 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
     const int prow = (t / 8) * 2048 + (t % 8) * 16;
     const int row_hi = wq * 32 + 31;
     T* og = static_cast<T*>(p.out) + (size_t)u.head * p.N * p.dv + u.c0;
-    TcWorkerRing<NS> ring;
-    ring.setup(B);
-    uint32_t rc0[NS];   // ring slot 0 of every CTA, shared::cluster addresses
-#pragma unroll
-    for (int q = 0; q < NS; ++q) rc0[q] = tc::mapa(tc::smem_u32(smem + L.ring(0)), (uint32_t)q);
-    // key groups of P that this CTA computes (and stores to every CTA)
-    const int pg0 = tc_group0(NS, rank), pgm = tc_group_mid(NS, rank), pg1 = tc_group0(NS, rank + 1);
-    const int pga = half ? pgm : pg0, pgb = half ? pg1 : pgm;
-    int r = 0;
-    auto wait = [&](uint64_t* bar, uint32_t par) {
-      return __all_sync(0xffffffffu, tc::mbar_wait_or_abort(bar, par, TC_WAIT_NS, abort_flag));
-    };
+    TcWorkerRing ring;
     // S block f (TMEM) -> its bf16 copy, the next chunk's readout operand
     auto convert_block = [&](int f) {
       uint8_t* d = sS + f * L.sblk + i * 16;
@@ -598,26 +584,24 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
     };
     for (int c = 0; c < u.n_chunks; ++c) {
       const long long t0 = u.t_begin + (long long)c * TC_C;
-      const int buf = c & 1;
       const int valid = (int)min((long long)TC_C, u.t_end - t0);
       const bool need_update = single || (c + 1 < u.n_chunks);
-      if (!wait(B.tfull(buf), (c >> 1) & 1u)) break;
+      if (!tc_wait_warp(B, B.qkfull(), c & 1u)) break;
       float xq[DK + 1], xk[DK + 1];
-      tc_load_x<DK>(smem + L.q(buf), t, xq);
-      tc_load_x<DK>(smem + L.k(buf), t, xk);
+      tc_load_x<DK>(smem + L.q(), t, xq);
+      tc_load_x<DK>(smem + L.k(), t, xk);
       xq[DK] = 1.0f;
       xk[DK] = (t < valid) ? 1.0f : 0.0f;
-      tc_warp_arrive(B.tempty(buf), lane);
-      if (!wait(B.qk(), c & 1u)) break;
+      tc_warp_arrive(B.qkempty(), lane);
+      if (!tc_wait_warp(B, B.qk(), c & 1u)) break;
       tc::fence_after_sync();
       // P = mask(T_n(A)) -> bf16 ring slot: (i/8)*2048 + (j/8)*128 + (i%8)*16
+      if (!ring.acquire(B, pos.s)) break;
       {
-        const int s = r & 1;
-        if (!ring.acquire(B, s)) break;
-        const uint32_t prow_off = (uint32_t)((i / 8) * 2048 + (i % 8) * 16);
-        uint8_t* prow_p = smem + L.ring(s) + prow_off;
-        for (int g = pga; g < pgb; ++g) {
-          const int j0 = 8 * g;
+        uint8_t* prow_p = smem + L.slot(pos.s) + (i / 8) * 2048 + (i % 8) * 16;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const int j0 = half * 64 + 8 * g;
           uint4 w = make_uint4(0u, 0u, 0u, 0u);
           if (j0 <= row_hi) {   // warp-uniform: groups above the diagonal are zero
             uint32_t rr[8];
@@ -629,23 +613,23 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
               pv[e] = (j0 + e <= i && i < valid) ? taylor_T<NT>(__uint_as_float(rr[e])) : 0.0f;
             w = tc_pack8(pv);
           }
-          *reinterpret_cast<uint4*>(prow_p + g * 128) = w;
-#pragma unroll
-          for (int q = 0; q < NS; ++q)
-            if (q != rank) tc::st_cluster_v4(rc0[q] + (uint32_t)s * 32768u + prow_off + g * 128, w);
+          *reinterpret_cast<uint4*>(prow_p + (j0 / 8) * 128) = w;
         }
-        ring.release(B, s, lane);
-        ++r;
       }
-      // feature blocks: phi(Q_0..NB-1) for the readout, then phi(K_0..NB-1)
+      ring.release(B, pos.s, lane);
+      pos.next();
+      // Feature uses: phi(Q_0..NB-1) for the readout, then phi(K_0..NB-1) for
+      // the update. The output is written once O is complete: after the first
+      // update tile (which goes in before O is done), or after the readouts
+      // when there is no update. One build call site keeps the code compact.
+      const int nuse = NB + (need_update ? NB : 0);
+      const int k_out = (NB + 1 < nuse) ? NB + 1 : nuse;
+      const int s_upd0 = (pos.s + NB) % pos.R;   // ring slot of update block 0
       bool ok = true;
-      const int r_upd = r + NB;
-      for (int k = 0; k < 2 * NB; ++k, ++r) {
-        const bool upd = (k >= NB);
-        const int f = upd ? k - NB : k;
-        if (k == NB) {
-          // O complete: out = O[:, :W] / O[:, W]
-          if (!(ok = wait(B.odone(), c & 1u))) break;
+      for (int k = 0; k <= nuse; ++k) {
+        if (k == k_out) {
+          // out = O[:, :W] / O[:, W]
+          if (!(ok = tc_wait_warp(B, B.odone(), c & 1u))) break;
           tc::fence_after_sync();
           uint32_t rr[16];
           tc::tmem_ld16(tm + lane_off + col_O + W, rr);
@@ -664,27 +648,27 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
             }
           }
           tc_warp_arrive(B.ofree(), lane);
-          if (!need_update) break;
         }
-        const int s = r & 1;
-        if (!(ok = ring.acquire(B, s))) break;
-        if (upd && f >= 2) {   // the slot's previous reader was the update of block f-2
+        if (k == nuse) break;
+        const bool upd = (k >= NB);
+        const int f = upd ? k - NB : k;
+        if (!(ok = ring.acquire(B, pos.s))) break;
+        if (upd && f >= pos.R) {   // the slot last held update f - R: convert that block
           tc::fence_after_sync();
-          convert_block(f - 2);
+          convert_block(f - pos.R);
         }
         float x[DK + 1];
 #pragma unroll
         for (int e = 0; e <= DK; ++e) x[e] = upd ? xk[e] : xq[e];
-        uint32_t rem[NS];
-#pragma unroll
-        for (int q = 0; q < NS; ++q) rem[q] = rc0[q] + (uint32_t)s * 32768u + (uint32_t)prow;
-        build_phi_rank<DK, NT, NS>(rank, f, half, x, smem + L.ring(s) + prow, rem);
-        ring.release(B, s, lane);
+        build_phi_rank<DK, NT, 1>(0, f, half, x, smem + L.slot(pos.s) + prow, nullptr);
+        ring.release(B, pos.s, lane);
+        pos.next();
       }
       if (!ok) break;
       if (need_update) {
-        for (int f = (NB >= 2 ? NB - 2 : 0); f < NB; ++f) {
-          if (!(ok = ring.acquire(B, (r_upd + f) & 1))) break;
+        for (int f = (NB > pos.R ? NB - pos.R : 0); f < NB; ++f) {
+          const int s = (s_upd0 + f) % pos.R;
+          if (!(ok = ring.acquire(B, s))) break;
           tc::fence_after_sync();
           convert_block(f);
         }
@@ -697,14 +681,13 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const bool aborted = *abort_flag != 0;
+  const bool aborted = *B.abort_flag() != 0;
   if (!aborted && single && tid < TC_WORKERS)
     tc_store_state<D, DPAD, NB>(p.states + (size_t)u.head * st_elems, tm, lane_off, nm, W, u.c0, p.dv,
                                 u.slice == 0, wq, lane, half);
   if (aborted && tid == 0) atomicExch(p.err, 1);
   tc::fence_before_sync();
   __syncthreads();
-  if constexpr (NS > 1) tc::cluster_sync();   // no peer still writes into this CTA
   if (warp == 0) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tm, 512);

@@ -15,7 +15,7 @@ tsa_status launch_prefill(const tsa_config* c, const tsa_plan& pl, PrefillParams
 
 // Tensor-core prefill (prefill_tc.cu).
 struct TcSlicing {
-  int nb, nmax, n_slices;
+  int nb, nmax, n_slices, ring;
   int c0[4], w[4];
   size_t smem;
 };
