@@ -1,0 +1,671 @@
+// prefill_tc32.cuh -- chunked causal prefill of fp32 q, k, v on the tensor
+// cores with split-bf16 operands.
+//
+// Same computation and chunk recurrence as prefill_tc.cuh (Expanding
+// Attention, arXiv 2610.20637 abstract; Hacker News thread on the paper:
+// (Q'K)V = Q'(KV) and the "+1" normaliser column), for inputs whose results
+// must match to 1e-4. Every operand x is split as x = hi + lo with
+// hi = bf16(x) and lo = bf16(x - hi) (16 significant bits together), and every
+// product as
+//     A B  ~  A_hi B_hi + A_hi B_lo + A_lo B_hi        (three kind::f16 MMAs)
+// into the same fp32 TMEM accumulator; the dropped A_lo B_lo term and the
+// rounding of lo are ~2^-16 relative.
+//
+// Per CTA (one head, one span, all value columns plus the normaliser group):
+// fp32 q, k, v tiles of a chunk land by TMA in a staging area; the worker
+// warps turn them into hi/lo bf16 operand tiles (q, k for Q K^T; v for
+// P [V,1] and the update) and keep each thread's q and k inputs in registers
+// for the feature map. Feature and P tiles travel through a ring of 32 KB
+// slots, each holding the hi and lo halves of a 128 x 64 bf16 tile:
+//   P use     : 128 query rows x 64 keys           (K-major A)
+//   readout   : 128 tokens x 64 features of a block (K-major A), K = 64 (or
+//               the block's last rows)
+//   update    : 64 tokens x 128 features of a block (MN-major A), K = 64
+// The bf16 hi/lo copies of the state hold only the rows the readout reads
+// (the last feature block is cut to a multiple of 16 rows). Warp roles and
+// bounded waits as in prefill_tc.cuh.
+#pragma once
+#include <cuda.h>
+#include "common.cuh"
+#include "tc_ptx.cuh"
+#include "feature_build.cuh"
+#include "prefill_tc.cuh"
+
+namespace tsa {
+
+template <int DK, int NT>
+struct Tc32Shape {
+  static constexpr int D = feat_dim(DK, NT);
+  static constexpr int NB = (D + 127) / 128;
+  // rows of the last block that the readout reads (a multiple of 16)
+  static constexpr int LAST_ROWS = round_up(D - 128 * (NB - 1), 16);
+  static constexpr int ROWS = 128 * (NB - 1) + LAST_ROWS;
+  __host__ __device__ static constexpr int rows(int f) { return f < NB - 1 ? 128 : LAST_ROWS; }
+  // 64-feature readout uses of block f
+  __host__ __device__ static constexpr int halves(int f) { return (rows(f) + 63) / 64; }
+};
+
+// Shared memory of the fp32 kernels (byte offsets, host and device).
+struct Tc32Smem {
+  size_t qs, ks, vs, qh, ql, kh, kl, vh, vl, ring0, sh, sl, bar, total;
+  int ring, nm;
+  __host__ __device__ Tc32Smem(int dk, int dv, int nm_, int rows, int ring_slots) {
+    ring = ring_slots;
+    nm = nm_;
+    const size_t x32 = (size_t)128 * dk * 4, x16 = (size_t)128 * dk * 2, v16 = (size_t)128 * nm_ * 2;
+    qs = 0;
+    ks = qs + x32;
+    vs = ks + x32;
+    qh = vs + (size_t)128 * dv * 4;
+    ql = qh + x16;
+    kh = ql + x16;
+    kl = kh + x16;
+    vh = kl + x16;
+    vl = vh + v16;
+    ring0 = vl + v16;
+    sh = ring0 + (size_t)ring * 32768;
+    sl = sh + (size_t)rows * nm_ * 2;
+    bar = sl + (size_t)rows * nm_ * 2;
+    total = bar + 256;
+  }
+  __host__ __device__ size_t slot(int r) const { return ring0 + (size_t)r * 32768; }
+};
+
+// mbarriers of the fp32 kernels (shared memory, in this order) and counts:
+//   sfull      staging tiles (fp32 q, k, v) of the chunk landed   (1 + tx)
+//   sfree      workers have consumed the staging                 (8)
+//   tiles      workers wrote the hi/lo operand tiles              (8)
+//   ring sfull[3] / sempty[3], qk, odone, ofree, conv, chunk, drain as in
+//   prefill_tc.cuh
+struct Tc32Bars {
+  uint64_t* b;
+  __device__ uint64_t* stg_full() const { return b + 0; }
+  __device__ uint64_t* stg_free() const { return b + 1; }
+  __device__ uint64_t* tiles() const { return b + 2; }
+  __device__ TcBars ring_bars() const { return TcBars{b}; }
+  __device__ void init() const {
+    const uint32_t cnt[16] = {1, 8, 8, 1, 8, 8, 8, 1, 1, 1, 1, 1, 8, 8, 1, 1};
+    for (int k = 0; k < 16; ++k) tc::mbar_init(b + k, cnt[k]);
+    *TcBars{b}.abort_flag() = 0;
+    tc::mbar_fence_init();
+  }
+};
+
+// hi and lo bf16 pairs of two fp32 values.
+__device__ __forceinline__ void tc32_split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = tc::pack_bf16x2(a, b);
+  const float ha = __uint_as_float(hi << 16), hb = __uint_as_float(hi & 0xFFFF0000u);
+  lo = tc::pack_bf16x2(a - ha, b - hb);
+}
+__device__ __forceinline__ void tc32_split8(const float* v, uint4& hi, uint4& lo) {
+  tc32_split2(v[0], v[1], hi.x, lo.x);
+  tc32_split2(v[2], v[3], hi.y, lo.y);
+  tc32_split2(v[4], v[5], hi.z, lo.z);
+  tc32_split2(v[6], v[7], hi.w, lo.w);
+}
+
+// Features [F*128 + 32*G, +32) of one token in fp32, split and stored: group
+// e (8 features at block offset a = 32*G + 8*e) goes to ((a & mask) / 8) * 128
+// bytes past `hi` and `lo` (mask 63 for a 64-wide tile, 127 for 128-wide).
+template <int DK, int NT, int F, int G, int E>
+struct Phi32Groups {
+  static __device__ __forceinline__ void run(const float (&x)[DK + 1], uint8_t* hi, uint8_t* lo, int mask) {
+    Phi32Groups<DK, NT, F, G, E - 1>::run(x, hi, lo, mask);
+    constexpr int a = 32 * G + 8 * (E - 1);
+    constexpr int A = F * 128 + a;
+    float v[8];
+    v[0] = feat_value<DK, NT, A + 0>(x); v[1] = feat_value<DK, NT, A + 1>(x);
+    v[2] = feat_value<DK, NT, A + 2>(x); v[3] = feat_value<DK, NT, A + 3>(x);
+    v[4] = feat_value<DK, NT, A + 4>(x); v[5] = feat_value<DK, NT, A + 5>(x);
+    v[6] = feat_value<DK, NT, A + 6>(x); v[7] = feat_value<DK, NT, A + 7>(x);
+    uint4 h, l;
+    tc32_split8(v, h, l);
+    const int off = ((a & mask) >> 3) * 128;
+    *reinterpret_cast<uint4*>(hi + off) = h;
+    *reinterpret_cast<uint4*>(lo + off) = l;
+  }
+};
+template <int DK, int NT, int F, int G>
+struct Phi32Groups<DK, NT, F, G, 0> {
+  static __device__ __forceinline__ void run(const float (&)[DK + 1], uint8_t*, uint8_t*, int) {}
+};
+
+// Runtime (block f, quarter g) -> instantiation; one call site per kernel.
+template <int DK, int NT, int F = 0>
+__device__ __forceinline__ void build_phi32(int f, int g, const float (&x)[DK + 1], uint8_t* hi, uint8_t* lo,
+                                            int mask) {
+  if constexpr (F < Tc32Shape<DK, NT>::NB) {
+    if (f == F) {
+      switch (g) {
+        case 0: Phi32Groups<DK, NT, F, 0, 4>::run(x, hi, lo, mask); break;
+        case 1: Phi32Groups<DK, NT, F, 1, 4>::run(x, hi, lo, mask); break;
+        case 2: Phi32Groups<DK, NT, F, 2, 4>::run(x, hi, lo, mask); break;
+        default: Phi32Groups<DK, NT, F, 3, 4>::run(x, hi, lo, mask); break;
+      }
+      return;
+    }
+    build_phi32<DK, NT, F + 1>(f, g, x, hi, lo, mask);
+  }
+}
+
+// 3-D tiled TMA load (fp32 staging tiles).
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5}], [%2];"
+      :: "r"(tc::smem_u32(dst)), "l"(tmap), "r"(tc::smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// Staging loads of one chunk: fp32 q (if tq), k and the W value columns.
+__device__ __forceinline__ void tc32_issue_staging(const Tc32Smem& L, uint8_t* smem, uint64_t* bar,
+                                                   const CUtensorMap* tq, const CUtensorMap* tk,
+                                                   const CUtensorMap* tv, long long t0, int head, int c0, int W,
+                                                   int dk) {
+  if (!tc::elect_one()) return;
+  tc::mbar_arrive_expect_tx(bar, (uint32_t)((tq ? 2 : 1) * 128 * dk * 4 + 128 * W * 4));
+  if (tq) tma_load_3d(smem + L.qs, tq, bar, 0, (int)t0, head);
+  tma_load_3d(smem + L.ks, tk, bar, 0, (int)t0, head);
+  tma_load_3d(smem + L.vs, tv, bar, c0, (int)t0, head);
+}
+
+// Three-term split product into one accumulator: A_hi B_hi + A_hi B_lo + A_lo B_hi.
+__device__ __forceinline__ void mma3(uint32_t d, uint64_t ah, uint64_t al, uint64_t bh, uint64_t bl, uint32_t id,
+                                     uint32_t acc) {
+  tc::mma_bf16_elect(d, ah, bh, id, acc);
+  tc::mma_bf16_elect(d, ah, bl, id, 1u);
+  tc::mma_bf16_elect(d, al, bh, id, 1u);
+}
+
+// Workers: fp32 staging -> hi/lo operand tiles. q, k: [e/8][t][8] (K-major);
+// v: [c/8][t][8] (MN-major), W value columns (the ones group stays as set up).
+// Thread (t = tid & 127, half = tid >> 7) converts half of its token's row.
+template <int DK>
+__device__ __forceinline__ void tc32_convert_x(const float* xs, uint8_t* th, uint8_t* tl, int t, int half) {
+#pragma unroll
+  for (int g = half * (DK / 16); g < (half + 1) * (DK / 16); ++g) {
+    float v[8];
+    const float4 a = *reinterpret_cast<const float4*>(xs + t * DK + 8 * g);
+    const float4 b = *reinterpret_cast<const float4*>(xs + t * DK + 8 * g + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    uint4 h, l;
+    tc32_split8(v, h, l);
+    *reinterpret_cast<uint4*>(th + g * 2048 + t * 16) = h;
+    *reinterpret_cast<uint4*>(tl + g * 2048 + t * 16) = l;
+  }
+}
+__device__ __forceinline__ void tc32_convert_v(const float* vs, uint8_t* th, uint8_t* tl, int W, int t, int half) {
+  for (int g = half * (W / 16); g < (half + 1) * (W / 16); ++g) {
+    float v[8];
+    const float4 a = *reinterpret_cast<const float4*>(vs + t * W + 8 * g);
+    const float4 b = *reinterpret_cast<const float4*>(vs + t * W + 8 * g + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    uint4 h, l;
+    tc32_split8(v, h, l);
+    *reinterpret_cast<uint4*>(th + g * 2048 + t * 16) = h;
+    *reinterpret_cast<uint4*>(tl + g * 2048 + t * 16) = l;
+  }
+}
+template <int DK>
+__device__ __forceinline__ void tc32_load_x(const float* xs, int t, float (&x)[DK + 1]) {
+#pragma unroll
+  for (int e = 0; e < DK; e += 4) {
+    const float4 a = *reinterpret_cast<const float4*>(xs + t * DK + e);
+    x[e] = a.x; x[e + 1] = a.y; x[e + 2] = a.z; x[e + 3] = a.w;
+  }
+}
+
+// TMEM state block f -> its hi/lo bf16 copies (rows_f rows, nm columns):
+// element (a, c) at (c/8) * rows_f*16 + a*16 + (c%8)*2 of block f's region.
+template <int DK, int NT>
+__device__ __forceinline__ void tc32_convert_state(uint8_t* sh, uint8_t* sl, uint32_t tm, uint32_t lane_off, int nm,
+                                                   int f, int i, int half) {
+  using S = Tc32Shape<DK, NT>;
+  const int rows = S::rows(f);
+  const size_t boff = (size_t)f * 128 * nm * 2;
+  for (int g = half; g < nm / 16; g += 2) {
+    uint32_t rr[16];
+    tc::tmem_ld16(tm + lane_off + f * nm + g * 16, rr);
+    tc::tmem_wait_ld();
+    if (i < rows) {
+      float v[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(rr[e]);
+      uint4 h0, l0, h1, l1;
+      tc32_split8(v, h0, l0);
+      tc32_split8(v + 8, h1, l1);
+      const size_t o0 = boff + (size_t)(2 * g) * rows * 16 + i * 16, o1 = o0 + (size_t)rows * 16;
+      *reinterpret_cast<uint4*>(sh + o0) = h0;
+      *reinterpret_cast<uint4*>(sl + o0) = l0;
+      *reinterpret_cast<uint4*>(sh + o1) = h1;
+      *reinterpret_cast<uint4*>(sl + o1) = l1;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// span_state_tc32: the state sum of one span -> scratch (fp32 inputs).
+// ---------------------------------------------------------------------------
+template <int DK, int NT>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+span_state_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v) {
+  using S = Tc32Shape<DK, NT>;
+  constexpr int D = S::D, NB = S::NB, DPAD = round_up(D, 4);
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const TcUnit u = tc_unit(p);
+  const int W = u.W, nm = u.nm;
+  const Tc32Smem L(DK, W, nm, S::ROWS, p.ring);
+  const Tc32Bars X{reinterpret_cast<uint64_t*>(smem + L.bar)};
+  const TcBars B = X.ring_bars();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wq = warp & 3, half = (warp >> 2) & 1;
+
+  if (warp == 0) tc::tmem_alloc(B.tmem_slot(), 512);
+  if (tid == 0) X.init();
+  if (tid < TC_WORKERS) {
+    tc_write_ones(smem + L.vh, W, tid);
+    for (int e = tid; e < 256; e += TC_WORKERS)
+      *reinterpret_cast<uint4*>(smem + L.vl + (W / 8 + (e & 1)) * 2048 + (e >> 1) * 16) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  tc::fence_proxy_async();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tm = *B.tmem_slot();
+  const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+  TcRingPos pos;
+  pos.R = p.ring;
+
+  if (warp == 8) {
+    const uint32_t id_up = tc::idesc_bf16(128, nm, true, true);
+    const uint64_t dVh = tc::sdesc(tc::smem_u32(smem + L.vh), 128, 2048);
+    const uint64_t dVl = tc::sdesc(tc::smem_u32(smem + L.vl), 128, 2048);
+    TcIssuerRing ring;
+    int req = 0, got = 0;
+    if (u.n_chunks > 0) {
+      tc32_issue_staging(L, smem, X.stg_full(), nullptr, &tm_k, &tm_v, u.t_begin, u.head, u.c0, W, DK);
+      req = 1;
+    }
+    bool ok = true;
+    for (int c = 0; c < u.n_chunks && ok; ++c) {
+      const long long t0 = u.t_begin + (long long)c * TC_C;
+      if (!(ok = tc_wait_warp(B, X.tiles(), c & 1u))) break;
+      ++got;
+      if (c + 1 < u.n_chunks) {
+        if (!(ok = tc_wait_warp(B, X.stg_free(), c & 1u))) break;
+        tc32_issue_staging(L, smem, X.stg_full(), nullptr, &tm_k, &tm_v, t0 + TC_C, u.head, u.c0, W, DK);
+        ++req;
+      }
+      for (int f = 0; f < NB && ok; ++f)
+        for (int h = 0; h < 2; ++h, pos.next()) {
+          if (!(ok = ring.take(B, pos.s))) break;
+          const uint32_t a = tc::smem_u32(smem + L.slot(pos.s));
+          const uint64_t dAh = tc::sdesc(a, 2048, 128), dAl = tc::sdesc(a + 16384, 2048, 128);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma3(tm + f * nm, dAh + (uint64_t)(k * 256), dAl + (uint64_t)(k * 256),
+                 dVh + (uint64_t)(64 * h + k * 16), dVl + (uint64_t)(64 * h + k * 16), id_up,
+                 (c > 0 || h > 0 || k > 0) ? 1u : 0u);
+          tc::mma_commit_elect(B.sempty(pos.s));
+        }
+      if (!ok) break;
+      tc::mma_commit_elect(B.chunk());
+    }
+    // drain: every MMA and every staging load that was requested
+    tc::mma_commit_elect(B.drain());
+    tc::mbar_wait(B.drain(), 0, TC_WAIT_NS);
+    for (; got < req; ++got) tc::mbar_wait(X.stg_full(), got & 1u, TC_WAIT_NS);
+  } else {
+    const int tq = tid & 63, qq = tid >> 6;   // update use: token 64h + tq, features 32qq..
+    const int urow = (tq / 8) * 2048 + (tq % 8) * 16;
+    TcWorkerRing ring;
+    for (int c = 0; c < u.n_chunks; ++c) {
+      const long long t0 = u.t_begin + (long long)c * TC_C;
+      const int valid = (int)min((long long)TC_C, u.t_end - t0);
+      if (!tc_wait_warp(B, X.stg_full(), c & 1u)) break;
+      if (c > 0 && !tc_wait_warp(B, B.chunk(), (c - 1) & 1u)) break;   // v tiles free
+      tc32_convert_v(reinterpret_cast<const float*>(smem + L.vs), smem + L.vh, smem + L.vl, W, tid & 127,
+                     half);
+      float xk[2][DK + 1];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        tc32_load_x<DK>(reinterpret_cast<const float*>(smem + L.ks), 64 * h + tq, xk[h]);
+        xk[h][DK] = (64 * h + tq < valid) ? 1.0f : 0.0f;
+      }
+      tc::fence_proxy_async();
+      tc_warp_arrive(X.stg_free(), lane);
+      tc_warp_arrive(X.tiles(), lane);
+      bool ok = true;
+      for (int f = 0; f < NB && ok; ++f)
+        for (int h = 0; h < 2; ++h, pos.next()) {
+          if (!(ok = ring.acquire(B, pos.s))) break;
+          if (32 * qq < S::rows(f)) {
+            float x[DK + 1];
+#pragma unroll
+            for (int e = 0; e <= DK; ++e) x[e] = h ? xk[1][e] : xk[0][e];
+            uint8_t* hi = smem + L.slot(pos.s) + urow;
+            build_phi32<DK, NT>(f, qq, x, hi, hi + 16384, 127);
+          }
+          ring.release(B, pos.s, lane);
+        }
+      if (!ok) break;
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const bool aborted = *B.abort_flag() != 0;
+  if (!aborted && tid < TC_WORKERS) {
+    float* dst = p.scratch + ((size_t)u.head * p.n_spans + u.span) * (size_t)DPAD * (p.dv + 1);
+    tc_store_state<D, DPAD, NB>(dst, tm, lane_off, nm, W, u.c0, p.dv, u.slice == 0, wq, lane, half);
+  }
+  if (aborted && tid == 0) atomicExch(p.err, 1);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tm, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// span_output_tc32: outputs of one span (fp32 inputs), state carried in TMEM.
+// Per chunk: the workers split the staged q, k, v into hi/lo tiles (and keep
+// their inputs in registers); the issuer runs Q K^T; the workers write P in
+// two key halves; the issuer runs P [V,1] and the readouts, the workers write
+// the output once O is complete, then the update tiles; after every MMA of
+// the chunk the workers split the updated state into its hi/lo copies.
+// ---------------------------------------------------------------------------
+template <int DK, int NT>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+  using S = Tc32Shape<DK, NT>;
+  constexpr int D = S::D, NB = S::NB, DPAD = round_up(D, 4);
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const TcUnit u = tc_unit(p);
+  const int W = u.W, nm = u.nm;
+  const Tc32Smem L(DK, W, nm, S::ROWS, p.ring);
+  const Tc32Bars X{reinterpret_cast<uint64_t*>(smem + L.bar)};
+  const TcBars B = X.ring_bars();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wq = warp & 3, half = (warp >> 2) & 1;
+  const bool single = (p.n_spans == 1);
+  const size_t st_elems = (size_t)DPAD * (p.dv + 1);
+
+  if (warp == 0) tc::tmem_alloc(B.tmem_slot(), 512);
+  if (tid == 0) X.init();
+  if (tid < TC_WORKERS) {
+    tc_write_ones(smem + L.vh, W, tid);
+    for (int e = tid; e < 256; e += TC_WORKERS)
+      *reinterpret_cast<uint4*>(smem + L.vl + (W / 8 + (e & 1)) * 2048 + (e >> 1) * 16) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tm = *B.tmem_slot();
+  const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+  const uint32_t col_O = (uint32_t)(NB * nm);
+  const int i = wq * 32 + lane;   // TMEM lane = query row / feature row of a block
+
+  // initial state -> TMEM, then its hi/lo copies
+  if (tid < TC_WORKERS) {
+    const float* src = nullptr;
+    if (!single) src = p.scratch + ((size_t)u.head * p.n_spans + u.span) * st_elems;
+    else if (p.accumulate) src = p.states + (size_t)u.head * st_elems;
+    for (int f = 0; f < NB; ++f) {
+      const int a = f * 128 + i;
+      for (int g = half; g < nm / 16; g += 2) {
+        uint32_t r[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int cc = g * 16 + e;
+          float x = 0.0f;
+          if (src != nullptr && a < D) {
+            if (cc < W) x = src[(size_t)a * p.dv + u.c0 + cc];
+            else if (cc == W) x = src[(size_t)DPAD * p.dv + a];
+          }
+          r[e] = __float_as_uint(x);
+        }
+        tc::tmem_st16(tm + lane_off + f * nm + g * 16, r);
+      }
+    }
+    tc::tmem_wait_st();
+    for (int f = 0; f < NB; ++f) tc32_convert_state<DK, NT>(smem + L.sh, smem + L.sl, tm, lane_off, nm, f, i, half);
+  }
+  tc::fence_proxy_async();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  TcRingPos pos;
+  pos.R = p.ring;
+
+  if (warp == 8) {
+    // ------------------------------ issuer ---------------------------------
+    const uint32_t id_qk = tc::idesc_bf16(128, 128, false, false);
+    const uint32_t id_pv = tc::idesc_bf16(128, nm, false, true);
+    const uint32_t id_up = tc::idesc_bf16(128, nm, true, true);
+    const uint64_t dQh = tc::sdesc(tc::smem_u32(smem + L.qh), 2048, 128);
+    const uint64_t dQl = tc::sdesc(tc::smem_u32(smem + L.ql), 2048, 128);
+    const uint64_t dKh = tc::sdesc(tc::smem_u32(smem + L.kh), 2048, 128);
+    const uint64_t dKl = tc::sdesc(tc::smem_u32(smem + L.kl), 2048, 128);
+    const uint64_t dVh = tc::sdesc(tc::smem_u32(smem + L.vh), 128, 2048);
+    const uint64_t dVl = tc::sdesc(tc::smem_u32(smem + L.vl), 128, 2048);
+    TcIssuerRing ring;
+    int req = 0, got = 0;
+    if (u.n_chunks > 0) {
+      tc32_issue_staging(L, smem, X.stg_full(), &tm_q, &tm_k, &tm_v, u.t_begin, u.head, u.c0, W, DK);
+      req = 1;
+    }
+    bool ok = true;
+    for (int c = 0; c < u.n_chunks && ok; ++c) {
+      const long long t0 = u.t_begin + (long long)c * TC_C;
+      const bool need_update = single || (c + 1 < u.n_chunks);
+      // the workers' tile conversion also follows their reading of O (A and O
+      // share their TMEM columns)
+      if (!(ok = tc_wait_warp(B, X.tiles(), c & 1u))) break;
+      ++got;
+      tc::fence_after_sync();
+#pragma unroll
+      for (int k = 0; k < DK / 16; ++k)
+        mma3(tm + col_O, dQh + (uint64_t)(k * 256), dQl + (uint64_t)(k * 256), dKh + (uint64_t)(k * 256),
+             dKl + (uint64_t)(k * 256), id_qk, k > 0 ? 1u : 0u);
+      tc::mma_commit_elect(B.qk());
+      if (c + 1 < u.n_chunks) {
+        if (!(ok = tc_wait_warp(B, X.stg_free(), c & 1u))) break;
+        tc32_issue_staging(L, smem, X.stg_full(), &tm_q, &tm_k, &tm_v, t0 + TC_C, u.head, u.c0, W, DK);
+        ++req;
+      }
+      // O = P [V, 1], keys in two halves
+      for (int kh2 = 0; kh2 < 2 && ok; ++kh2, pos.next()) {
+        if (!(ok = ring.take(B, pos.s))) break;
+        const uint32_t a = tc::smem_u32(smem + L.slot(pos.s));
+        const uint64_t dPh = tc::sdesc(a, 128, 1024), dPl = tc::sdesc(a + 16384, 128, 1024);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma3(tm + col_O, dPh + (uint64_t)(k * 16), dPl + (uint64_t)(k * 16), dVh + (uint64_t)(64 * kh2 + 16 * k),
+               dVl + (uint64_t)(64 * kh2 + 16 * k), id_pv, (kh2 > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit_elect(B.sempty(pos.s));
+      }
+      if (!ok) break;
+      if (c > 0 && !(ok = tc_wait_warp(B, B.conv(), (c - 1) & 1u))) break;
+      // O += phi(Q_f) [S_f, z_f], 64 features at a time
+      for (int f = 0; f < NB && ok; ++f) {
+        const int rows = S::rows(f);
+        const uint32_t sb = (uint32_t)((size_t)f * 128 * nm * 2);
+        const uint64_t dSh = tc::sdesc(tc::smem_u32(smem + L.sh) + sb, 128, (uint32_t)rows * 16);
+        const uint64_t dSl = tc::sdesc(tc::smem_u32(smem + L.sl) + sb, 128, (uint32_t)rows * 16);
+        for (int h = 0; h < S::halves(f); ++h, pos.next()) {
+          if (!(ok = ring.take(B, pos.s))) break;
+          const uint32_t a = tc::smem_u32(smem + L.slot(pos.s));
+          const uint64_t dAh = tc::sdesc(a, 128, 1024), dAl = tc::sdesc(a + 16384, 128, 1024);
+          const int ks = min(64, rows - 64 * h) / 16;
+          for (int k = 0; k < ks; ++k)
+            mma3(tm + col_O, dAh + (uint64_t)(k * 16), dAl + (uint64_t)(k * 16), dSh + (uint64_t)(64 * h + 16 * k),
+                 dSl + (uint64_t)(64 * h + 16 * k), id_pv, 1u);
+          tc::mma_commit_elect(B.sempty(pos.s));
+        }
+      }
+      if (!ok) break;
+      tc::mma_commit_elect(B.odone());
+      // S_f += phi(K_f)^T [V, 1], 64 tokens at a time
+      if (need_update) {
+        for (int f = 0; f < NB && ok; ++f)
+          for (int h = 0; h < 2; ++h, pos.next()) {
+            if (!(ok = ring.take(B, pos.s))) break;
+            const uint32_t a = tc::smem_u32(smem + L.slot(pos.s));
+            const uint64_t dAh = tc::sdesc(a, 2048, 128), dAl = tc::sdesc(a + 16384, 2048, 128);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma3(tm + f * nm, dAh + (uint64_t)(k * 256), dAl + (uint64_t)(k * 256),
+                   dVh + (uint64_t)(64 * h + 16 * k), dVl + (uint64_t)(64 * h + 16 * k), id_up, 1u);
+            tc::mma_commit_elect(B.sempty(pos.s));
+          }
+        if (!ok) break;
+      }
+      tc::mma_commit_elect(B.chunk());
+    }
+    tc::mma_commit_elect(B.drain());
+    tc::mbar_wait(B.drain(), 0, TC_WAIT_NS);
+    for (; got < req; ++got) tc::mbar_wait(X.stg_full(), got & 1u, TC_WAIT_NS);
+  } else {
+    // ------------------------------ workers --------------------------------
+    const int t = tid & 127, tq = tid & 63, qq = tid >> 6;
+    const int rrow = (t / 8) * 1024 + (t % 8) * 16;      // 128-token, 64-wide tiles
+    const int urow = (tq / 8) * 2048 + (tq % 8) * 16;    // 64-token, 128-wide tiles
+    const int row_hi = wq * 32 + 31;
+    float* og = static_cast<float*>(p.out) + (size_t)u.head * p.N * p.dv + u.c0;
+    TcWorkerRing ring;
+    for (int c = 0; c < u.n_chunks; ++c) {
+      const long long t0 = u.t_begin + (long long)c * TC_C;
+      const int valid = (int)min((long long)TC_C, u.t_end - t0);
+      const bool need_update = single || (c + 1 < u.n_chunks);
+      if (!tc_wait_warp(B, X.stg_full(), c & 1u)) break;
+      if (c > 0 && !tc_wait_warp(B, B.chunk(), (c - 1) & 1u)) break;   // operand tiles free
+      const float* qs = reinterpret_cast<const float*>(smem + L.qs);
+      const float* ks = reinterpret_cast<const float*>(smem + L.ks);
+      tc32_convert_x<DK>(qs, smem + L.qh, smem + L.ql, t, half);
+      tc32_convert_x<DK>(ks, smem + L.kh, smem + L.kl, t, half);
+      tc32_convert_v(reinterpret_cast<const float*>(smem + L.vs), smem + L.vh, smem + L.vl, W, t, half);
+      float xq[DK + 1], xk[2][DK + 1];
+      tc32_load_x<DK>(qs, t, xq);
+      xq[DK] = 1.0f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        tc32_load_x<DK>(ks, 64 * h + tq, xk[h]);
+        xk[h][DK] = (64 * h + tq < valid) ? 1.0f : 0.0f;
+      }
+      tc::fence_proxy_async();
+      tc_warp_arrive(X.stg_free(), lane);
+      tc_warp_arrive(X.tiles(), lane);
+      if (!tc_wait_warp(B, B.qk(), c & 1u)) break;
+      tc::fence_after_sync();
+      // P = mask(T_n(A)) in two key halves (two ring slots): row i, keys
+      // 64*kh2 + 32*half + ... Both halves are written before either is
+      // published, because P [V,1] of the first half overwrites A (A and O
+      // share their TMEM columns).
+      bool ok = true;
+      const int ps0 = pos.s;
+      pos.next();
+      const int ps1 = pos.s;
+      pos.next();
+      ok = ring.acquire(B, ps0);
+      ok = ok && ring.acquire(B, ps1);
+      if (!ok) break;
+      for (int kh2 = 0; kh2 < 2; ++kh2) {
+        uint8_t* ph = smem + L.slot(kh2 ? ps1 : ps0) + (i / 8) * 1024 + (i % 8) * 16;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int jl = 32 * half + 8 * g, j0 = 64 * kh2 + jl;
+          uint4 h4 = make_uint4(0u, 0u, 0u, 0u), l4 = h4;
+          if (j0 <= row_hi) {   // warp-uniform: groups above the diagonal are zero
+            uint32_t rr[8];
+            tc::tmem_ld8(tm + lane_off + col_O + j0, rr);
+            tc::tmem_wait_ld();
+            float pv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              pv[e] = (j0 + e <= i && i < valid) ? taylor_T<NT>(__uint_as_float(rr[e])) : 0.0f;
+            tc32_split8(pv, h4, l4);
+          }
+          *reinterpret_cast<uint4*>(ph + (jl / 8) * 128) = h4;
+          *reinterpret_cast<uint4*>(ph + 16384 + (jl / 8) * 128) = l4;
+        }
+      }
+      ring.release(B, ps0, lane);
+      ring.release(B, ps1, lane);
+      // feature tiles: readout (token t, quarter 2h + half) then update
+      // (token 64h + tq, quarter qq); one build call site
+      const int n_ro = [] { int n = 0; for (int f = 0; f < NB; ++f) n += S::halves(f); return n; }();
+      const int nuse = n_ro + (need_update ? 2 * NB : 0);
+      int f = 0, h = 0;
+      for (int k = 0; k <= nuse; ++k) {
+        if (k == n_ro) {
+          // out = O[:, :W] / O[:, W]
+          if (!(ok = tc_wait_warp(B, B.odone(), c & 1u))) break;
+          tc::fence_after_sync();
+          uint32_t rr[16];
+          tc::tmem_ld16(tm + lane_off + col_O + W, rr);
+          tc::tmem_wait_ld();
+          const float inv = 1.0f / __uint_as_float(rr[0]);
+          for (int g = half; g < W / 16; g += 2) {
+            tc::tmem_ld16(tm + lane_off + col_O + g * 16, rr);
+            tc::tmem_wait_ld();
+            if (i < valid) {
+              float* dst = og + (size_t)(t0 + i) * p.dv + g * 16;
+#pragma unroll
+              for (int e = 0; e < 16; e += 4)
+                *reinterpret_cast<float4*>(dst + e) =
+                    make_float4(__uint_as_float(rr[e]) * inv, __uint_as_float(rr[e + 1]) * inv,
+                                __uint_as_float(rr[e + 2]) * inv, __uint_as_float(rr[e + 3]) * inv);
+            }
+          }
+          tc_warp_arrive(B.ofree(), lane);
+          f = 0;
+          h = 0;
+        }
+        if (k == nuse) break;
+        const bool upd = (k >= n_ro);
+        if (!(ok = ring.acquire(B, pos.s))) break;
+        const int g = upd ? qq : 2 * h + half;
+        if (32 * g < S::rows(f)) {
+          float x[DK + 1];
+#pragma unroll
+          for (int e = 0; e <= DK; ++e) x[e] = upd ? (h ? xk[1][e] : xk[0][e]) : xq[e];
+          uint8_t* hi = smem + L.slot(pos.s) + (upd ? urow : rrow);
+          build_phi32<DK, NT>(f, g, x, hi, hi + 16384, upd ? 127 : 63);
+        }
+        ring.release(B, pos.s, lane);
+        pos.next();
+        // next (f, h): readouts walk the block's 64-feature halves, updates
+        // its two 64-token halves
+        if (++h == (upd ? 2 : S::halves(f))) { h = 0; ++f; }
+      }
+      if (!ok) break;
+      // every MMA of the chunk done -> hi/lo copies of the updated state
+      if (need_update) {
+        if (!tc_wait_warp(B, B.chunk(), c & 1u)) break;
+        tc::fence_after_sync();
+        for (int fb = 0; fb < NB; ++fb)
+          tc32_convert_state<DK, NT>(smem + L.sh, smem + L.sl, tm, lane_off, nm, fb, i, half);
+      }
+      tc::fence_proxy_async();
+      tc_warp_arrive(B.conv(), lane);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const bool aborted = *B.abort_flag() != 0;
+  if (!aborted && single && tid < TC_WORKERS)
+    tc_store_state<D, DPAD, NB>(p.states + (size_t)u.head * st_elems, tm, lane_off, nm, W, u.c0, p.dv,
+                                u.slice == 0, wq, lane, half);
+  if (aborted && tid == 0) atomicExch(p.err, 1);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tm, 512);
+  }
+}
+
+}  // namespace tsa

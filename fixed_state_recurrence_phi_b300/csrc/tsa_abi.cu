@@ -127,7 +127,7 @@ static constexpr size_t kSmemPerSm = 228 * 1024;
 // TMEM budget, one CTA per SM. A span-state chunk costs about half an output
 // chunk (phi(K) and the update only).
 static tsa_status make_plan_tc(const tsa_config* c, long long N, int num_sms, const TcSlicing& ts,
-                               tsa_plan* pl) {
+                               tsa_plan* pl, int path) {
   const int chunk = 128;
   const long long heads = (long long)c->B * c->H;
   const long long n_chunks = (N + chunk - 1) / chunk;
@@ -160,7 +160,7 @@ static tsa_status make_plan_tc(const tsa_config* c, long long N, int num_sms, co
   pl->ctas_per_sm = 1;
   pl->scratch_bytes = best_s > 1 ? (size_t)heads * best_s * state_floats_per_head(c) * 4 : 0;
   pl->launches = best_s > 1 ? 3 : 1;
-  pl->path = TSA_PATH_TC;
+  pl->path = path;
   return TSA_OK;
 }
 
@@ -171,8 +171,18 @@ tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl
     if (tc_slicing(c->d_k, c->n_terms, c->d_v, &ts)) {
       if (c->chunk != 0 && c->chunk != 128)
         return fail(TSA_ERR_UNSUPPORTED, "chunk=%d not built for bf16 (0 or 128)", c->chunk);
-      return make_plan_tc(c, N, num_sms, ts, pl);
+      return make_plan_tc(c, N, num_sms, ts, pl, TSA_PATH_TC);
     }
+  }
+  if (c->dtype == TSA_F32 && tc32_fits(c->d_k, c->n_terms, c->d_v) && (c->chunk == 0 || c->chunk == 128)) {
+    TcSlicing ts;
+    memset(&ts, 0, sizeof(ts));
+    ts.nb = (feat_dim(c->d_k, c->n_terms) + 127) / 128;
+    ts.n_slices = 1;
+    ts.w[0] = c->d_v;
+    ts.nmax = c->d_v + 16;
+    ts.smem = tc32_smem(c->d_k, c->n_terms, c->d_v);
+    return make_plan_tc(c, N, num_sms, ts, pl, TSA_PATH_TC_F32);
   }
   const int chunk = 64;
   if (c->chunk != 0 && c->chunk != chunk)
@@ -264,6 +274,7 @@ static tsa_status dispatch_prefill(const tsa_config* c, const tsa_plan& pl, Pref
 tsa_status launch_prefill(const tsa_config* c, const tsa_plan& pl, PrefillParams p,
                           cudaStream_t s) {
   if (pl.path == TSA_PATH_TC) return launch_prefill_tc(c, pl, p, s);
+  if (pl.path == TSA_PATH_TC_F32) return launch_prefill_tc32(c, pl, p, s);
   return (c->dtype == TSA_F32) ? dispatch_prefill<float>(c, pl, p, s)
                                : dispatch_prefill<__nv_bfloat16>(c, pl, p, s);
 }

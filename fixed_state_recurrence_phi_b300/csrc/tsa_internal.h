@@ -23,5 +23,9 @@ bool tc_supported(int dk, int nt);
 bool tc_slicing(int dk, int nt, int dv, TcSlicing* ts);
 tsa_status launch_prefill_tc(const tsa_config* c, const tsa_plan& pl, const PrefillParams& p, cudaStream_t s);
 tsa_status device_error_word(int** out);
+// fp32 tensor-core prefill with split-bf16 operands (prefill_tc32.cu).
+bool tc32_fits(int dk, int nt, int dv);
+size_t tc32_smem(int dk, int nt, int dv);
+tsa_status launch_prefill_tc32(const tsa_config* c, const tsa_plan& pl, const PrefillParams& p, cudaStream_t s);
 tsa_status take_device_error();
 }  // namespace tsa

@@ -100,10 +100,13 @@ tsa_status tsa_feature_index(int d_k, int n_terms, int* idx, float* weight);
  * slice_width columns. With n_spans > 1 the call launches a span-state pass,
  * an exclusive scan over spans and the output pass (`launches` = 3), and takes
  * scratch_bytes of stream-ordered scratch from the library's pool.
- * path: TSA_PATH_SIMT (fp32 FFMA on the CUDA cores) or TSA_PATH_TC (bf16
- * tcgen05 tensor cores with fp32 TMEM accumulators; bf16 inputs). */
+ * path: TSA_PATH_SIMT (fp32 FFMA on the CUDA cores), TSA_PATH_TC (bf16
+ * inputs on the tcgen05 tensor cores, fp32 TMEM accumulators) or
+ * TSA_PATH_TC_F32 (fp32 inputs on the tensor cores: every operand split into
+ * bf16 hi + lo parts and every product taken as three MMAs). */
 #define TSA_PATH_SIMT 0
 #define TSA_PATH_TC 1
+#define TSA_PATH_TC_F32 2
 typedef struct {
   int chunk;
   int slice_width;

@@ -43,7 +43,11 @@ def test_bf16_uses_tensor_core_path(G):
     for d, dv, n in [(16, 64, 3), (16, 64, 4), (32, 128, 3), (16, 128, 3), (32, 64, 2), (16, 32, 1)]:
         p = T.prefill_plan(T.Config(2, 4, d, dv, n, "bf16"), 4096)
         assert p["path"] == T.TSA_PATH_TC and p["chunk"] == 128, (d, dv, n, p)
-    assert T.prefill_plan(T.Config(1, 8, 16, 64, 3, "f32"), 8192)["path"] == T.TSA_PATH_SIMT
+    # fp32 inputs: split-bf16 tensor-core path where one CTA holds the head,
+    # the CUDA-core path otherwise
+    assert T.prefill_plan(T.Config(1, 8, 16, 64, 3, "f32"), 8192)["path"] == T.TSA_PATH_TC_F32
+    assert T.prefill_plan(T.Config(1, 1, 16, 64, 3, "f32"), 256)["path"] == T.TSA_PATH_TC_F32
+    assert T.prefill_plan(T.Config(1, 2, 16, 64, 4, "f32"), 333)["path"] == T.TSA_PATH_SIMT
 
 
 @pytest.mark.parametrize("N", [1, 2, 127, 128, 129, 255, 256, 257, 1000])
