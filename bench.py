@@ -96,7 +96,8 @@ def _algorithmic_decode_bytes(w) -> int:
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled while the timed work runs."""
+    """nvidia-smi clocks and throttle reasons, sampled (every 100 ms) while the
+    timed work runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -108,9 +109,12 @@ class ClockSampler:
 
     def __enter__(self):
         try:
+            # 100 ms polling at the lowest CPU priority: faster polling (20 ms)
+            # slowed every host-side CUDA call of this process several-fold
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "20"],
-                                      stdout=self.f, stderr=subprocess.DEVNULL)
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL,
+                                      preexec_fn=lambda: os.nice(19))
             time.sleep(0.3)
         except Exception:
             self.p = None
@@ -237,7 +241,7 @@ def run_ours(args):
     gpu = torch.cuda.current_device()
     do_pre = args.only in ("all", "prefill")
     do_dec = args.only in ("all", "decode")
-    ms = e2e_ms = float("nan"); h2d = d2h = 0
+    ms = e2e_ms = host_us = float("nan"); h2d = d2h = 0
     dec_us = eager_us = long_prefill_ms = merge_ms = float("nan")
     steps, reps = 1024, 3
     dw = DECODE
@@ -258,6 +262,15 @@ def run_ours(args):
           barrier()
           step_ms = [a.elapsed_time(b) for a, b in evs]
           ms = max_over_ranks(statistics.mean(step_ms))
+          # host time of one call (argument checks, plan, tensor maps, launches)
+          hs = []
+          for _ in range(5):
+              torch.cuda.synchronize()
+              h0 = time.perf_counter()
+              prefill_step()
+              hs.append((time.perf_counter() - h0) * 1e6)
+          torch.cuda.synchronize()
+          host_us = statistics.median(hs)
 
           # -------- e2e: pinned host buffers in, host result out, through the ABI
           qh = q.cpu().pin_memory(); kh = k.cpu().pin_memory(); vh = v.cpu().pin_memory()
@@ -414,7 +427,9 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w["workload"], "B": w["B"], "H": w["H"], "N": w["N"], "d_k": w["d_k"],
                    "d_v": w["d_v"], "n_terms": w["n_terms"], "chunk": plan["chunk"],
-                   "n_spans": plan["n_spans"], "l2": "flushed between timed steps (256 MB write)"},
+                   "n_spans": plan["n_spans"], "path": ["simt", "tc", "tc_f32"][plan["path"]],
+                   "l2": "flushed between timed steps (256 MB write)"},
+        "host_us_per_call": host_us,
         "roofline": {"bound": "hbm", "kernel": "tsa_prefill (all launches of the call)",
                      "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
                      "peak_source": f"{peak_src} (copy bandwidth)",

@@ -270,6 +270,23 @@ span_scan_kernel(float* __restrict__ states, float* __restrict__ scratch, int he
   st[e] = run;
 }
 
+// Launch the span scan. Its carveout is pinned to the shared-memory maximum,
+// like the prefill kernels around it, so that the SMs do not repartition
+// L1/shared memory between the three launches of a multi-span prefill.
+static inline cudaError_t launch_span_scan(float* states, float* scratch, int heads, int n_spans, int elems4,
+                                           int accumulate, cudaStream_t s) {
+  static bool carveout_set = false;
+  if (!carveout_set) {
+    cudaError_t e = cudaFuncSetAttribute(span_scan_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    carveout_set = true;
+  }
+  dim3 g2((elems4 + 255) / 256, heads);
+  span_scan_kernel<<<g2, 256, 0, s>>>(states, scratch, heads, n_spans, elems4, accumulate);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------------------
 // span_output: outputs of one span (one dv slice), state carried on chip.
 // ---------------------------------------------------------------------------

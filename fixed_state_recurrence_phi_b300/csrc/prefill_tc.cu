@@ -143,7 +143,7 @@ tsa_status make_tmap(CUtensorMap* m, const void* base, int inner, long long N, i
 
 template <typename Kern>
 cudaError_t set_smem(Kern kernel, int smem) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  return set_smem_once((const void*)kernel, smem);
 }
 
 template <int DK, int NT>
@@ -171,9 +171,7 @@ tsa_status launch_tc(const tsa_plan& pl, const TcSlicing& ts, const PrefillParam
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch span_state_tc");
     const int elems4 = (int)(round_up(feat_dim(DK, NT), 4) * (pp.dv + 1) / 4);
-    dim3 g2((elems4 + 255) / 256, pp.heads);
-    span_scan_kernel<<<g2, 256, 0, s>>>(pp.states, pp.scratch, pp.heads, pl.n_spans, elems4, pp.accumulate);
-    e = cudaGetLastError();
+    e = launch_span_scan(pp.states, pp.scratch, pp.heads, pl.n_spans, elems4, pp.accumulate, s);
     if (e != cudaSuccess) return cuda_fail(e, "launch span_scan");
   }
   e = set_smem(span_output_tc_kernel<__nv_bfloat16, DK, NT>, smem);

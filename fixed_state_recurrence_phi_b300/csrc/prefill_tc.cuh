@@ -600,20 +600,27 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
       {
         uint8_t* prow_p = smem + L.slot(pos.s) + (i / 8) * 2048 + (i % 8) * 16;
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const int j0 = half * 64 + 8 * g;
-          uint4 w = make_uint4(0u, 0u, 0u, 0u);
-          if (j0 <= row_hi) {   // warp-uniform: groups above the diagonal are zero
-            uint32_t rr[8];
-            tc::tmem_ld8(tm + lane_off + col_O + j0, rr);
+        for (int q2 = 0; q2 < 2; ++q2) {
+          const int jb = half * 64 + 32 * q2;
+          if (jb <= row_hi) {   // warp-uniform: 32 keys above the diagonal are zero
+            uint32_t rr[32];
+            tc::tmem_ld32(tm + lane_off + col_O + jb, rr);
             tc::tmem_wait_ld();
-            float pv[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              pv[e] = (j0 + e <= i && i < valid) ? taylor_T<NT>(__uint_as_float(rr[e])) : 0.0f;
-            w = tc_pack8(pv);
+            for (int g = 0; g < 4; ++g) {
+              float pv[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int j = jb + 8 * g + e;
+                pv[e] = (j <= i && i < valid) ? taylor_T<NT>(__uint_as_float(rr[8 * g + e])) : 0.0f;
+              }
+              *reinterpret_cast<uint4*>(prow_p + ((jb + 8 * g) / 8) * 128) = tc_pack8(pv);
+            }
+          } else {
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              *reinterpret_cast<uint4*>(prow_p + ((jb + 8 * g) / 8) * 128) = make_uint4(0u, 0u, 0u, 0u);
           }
-          *reinterpret_cast<uint4*>(prow_p + (j0 / 8) * 128) = w;
         }
       }
       ring.release(B, pos.s, lane);

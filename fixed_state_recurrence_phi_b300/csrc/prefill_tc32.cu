@@ -47,16 +47,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
-// [heads][N][inner] fp32 as 3-D (inner, N, heads); box (cols, 128, 1) lands
-// as a row-major [token][cols] fp32 tile.
+// [heads][N][inner] fp32 as 4-D (4, N, inner/4, heads); box (4, 128, cols/4, 1)
+// lands as a [col/4][token][4] fp32 tile.
 tsa_status make_tmap32(CUtensorMap* m, const void* base, int inner, long long N, int heads, int cols) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   if (!enc) return fail(TSA_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
-  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)N, (cuuint64_t)heads};
-  cuuint64_t strides[2] = {(cuuint64_t)inner * 4, (cuuint64_t)N * inner * 4};
-  cuuint32_t box[3] = {(cuuint32_t)cols, (cuuint32_t)TC_C, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+  cuuint64_t dims[4] = {4, (cuuint64_t)N, (cuuint64_t)(inner / 4), (cuuint64_t)heads};
+  cuuint64_t strides[3] = {(cuuint64_t)inner * 4, 16, (cuuint64_t)N * inner * 4};
+  cuuint32_t box[4] = {4, (cuuint32_t)TC_C, (cuuint32_t)(cols / 4), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(TSA_ERR_CUDA, "cuTensorMapEncodeTiled (fp32) failed (%d)", (int)r);
@@ -84,18 +84,16 @@ tsa_status launch32(const tsa_plan& pl, const PrefillParams& pp, cudaStream_t s)
   const unsigned grid = (unsigned)((long long)pp.heads * pl.n_spans);
   cudaError_t e;
   if (pl.n_spans > 1) {
-    e = cudaFuncSetAttribute(span_state_tc32_kernel<DK, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = set_smem_once((const void*)span_state_tc32_kernel<DK, NT>, smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_state_tc32)");
     span_state_tc32_kernel<DK, NT><<<grid, TC_THREADS, smem, s>>>(p, mk, mv);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch span_state_tc32");
     const int elems4 = (int)(round_up(S::D, 4) * (pp.dv + 1) / 4);
-    dim3 g2((elems4 + 255) / 256, pp.heads);
-    span_scan_kernel<<<g2, 256, 0, s>>>(pp.states, pp.scratch, pp.heads, pl.n_spans, elems4, pp.accumulate);
-    e = cudaGetLastError();
+    e = launch_span_scan(pp.states, pp.scratch, pp.heads, pl.n_spans, elems4, pp.accumulate, s);
     if (e != cudaSuccess) return cuda_fail(e, "launch span_scan");
   }
-  e = cudaFuncSetAttribute(span_output_tc32_kernel<DK, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = set_smem_once((const void*)span_output_tc32_kernel<DK, NT>, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_output_tc32)");
   span_output_tc32_kernel<DK, NT><<<grid, TC_THREADS, smem, s>>>(p, mq, mk, mv);
   e = cudaGetLastError();
@@ -111,7 +109,7 @@ tsa_status launch32(const tsa_plan& pl, const PrefillParams& pp, cudaStream_t s)
 bool tc32_fits(int dk, int nt, int dv) {
   if (!tc_supported(dk, nt) || dv % 16 != 0) return false;
   const int D = feat_dim(dk, nt), nb = (D + 127) / 128, nm = dv + 16;
-  if (nb * nm + std::max(128, nm) > 512) return false;
+  if (nb * nm + nm + 128 > 512) return false;   // state, O and A in separate columns
   const size_t sm = smem_for(dk, nt, dv, 2);
   return sm > 0 && sm <= kSmemLimit;
 }

@@ -148,25 +148,18 @@ __device__ __forceinline__ void build_phi32(int f, int g, const float (&x)[DK + 
   }
 }
 
-// 3-D tiled TMA load (fp32 staging tiles).
-__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%3, %4, %5}], [%2];"
-      :: "r"(tc::smem_u32(dst)), "l"(tmap), "r"(tc::smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
-// Staging loads of one chunk: fp32 q (if tq), k and the W value columns.
+// Staging loads of one chunk: fp32 q (if tq), k and the W value columns, each
+// as a [col/4][token][4] tile (4-D tensor maps; box (4, 128, cols/4, 1)), so
+// that consecutive threads (tokens) read consecutive 16-byte pieces.
 __device__ __forceinline__ void tc32_issue_staging(const Tc32Smem& L, uint8_t* smem, uint64_t* bar,
                                                    const CUtensorMap* tq, const CUtensorMap* tk,
                                                    const CUtensorMap* tv, long long t0, int head, int c0, int W,
                                                    int dk) {
   if (!tc::elect_one()) return;
   tc::mbar_arrive_expect_tx(bar, (uint32_t)((tq ? 2 : 1) * 128 * dk * 4 + 128 * W * 4));
-  if (tq) tma_load_3d(smem + L.qs, tq, bar, 0, (int)t0, head);
-  tma_load_3d(smem + L.ks, tk, bar, 0, (int)t0, head);
-  tma_load_3d(smem + L.vs, tv, bar, c0, (int)t0, head);
+  if (tq) tc::tma_load_4d(smem + L.qs, tq, bar, 0, (int)t0, 0, head);
+  tc::tma_load_4d(smem + L.ks, tk, bar, 0, (int)t0, 0, head);
+  tc::tma_load_4d(smem + L.vs, tv, bar, 0, (int)t0, c0 / 4, head);
 }
 
 // Three-term split product into one accumulator: A_hi B_hi + A_hi B_lo + A_lo B_hi.
@@ -177,28 +170,16 @@ __device__ __forceinline__ void mma3(uint32_t d, uint64_t ah, uint64_t al, uint6
   tc::mma_bf16_elect(d, al, bh, id, 1u);
 }
 
-// Workers: fp32 staging -> hi/lo operand tiles. q, k: [e/8][t][8] (K-major);
-// v: [c/8][t][8] (MN-major), W value columns (the ones group stays as set up).
-// Thread (t = tid & 127, half = tid >> 7) converts half of its token's row.
-template <int DK>
-__device__ __forceinline__ void tc32_convert_x(const float* xs, uint8_t* th, uint8_t* tl, int t, int half) {
-#pragma unroll
-  for (int g = half * (DK / 16); g < (half + 1) * (DK / 16); ++g) {
+// Workers: fp32 staging ([col/4][t][4]) -> hi/lo operand tiles. q, k:
+// [e/8][t][8] (K-major); v: [c/8][t][8] (MN-major), W value columns (the
+// ones group stays as set up). Thread (t = tid & 127, half = tid >> 7)
+// converts half of its token's row.
+__device__ __forceinline__ void tc32_convert_rows(const uint8_t* xs, uint8_t* th, uint8_t* tl, int cols, int t,
+                                                  int half) {
+  for (int g = half * (cols / 16); g < (half + 1) * (cols / 16); ++g) {
     float v[8];
-    const float4 a = *reinterpret_cast<const float4*>(xs + t * DK + 8 * g);
-    const float4 b = *reinterpret_cast<const float4*>(xs + t * DK + 8 * g + 4);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    uint4 h, l;
-    tc32_split8(v, h, l);
-    *reinterpret_cast<uint4*>(th + g * 2048 + t * 16) = h;
-    *reinterpret_cast<uint4*>(tl + g * 2048 + t * 16) = l;
-  }
-}
-__device__ __forceinline__ void tc32_convert_v(const float* vs, uint8_t* th, uint8_t* tl, int W, int t, int half) {
-  for (int g = half * (W / 16); g < (half + 1) * (W / 16); ++g) {
-    float v[8];
-    const float4 a = *reinterpret_cast<const float4*>(vs + t * W + 8 * g);
-    const float4 b = *reinterpret_cast<const float4*>(vs + t * W + 8 * g + 4);
+    const float4 a = *reinterpret_cast<const float4*>(xs + (2 * g) * 2048 + t * 16);
+    const float4 b = *reinterpret_cast<const float4*>(xs + (2 * g + 1) * 2048 + t * 16);
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     uint4 h, l;
     tc32_split8(v, h, l);
@@ -207,10 +188,10 @@ __device__ __forceinline__ void tc32_convert_v(const float* vs, uint8_t* th, uin
   }
 }
 template <int DK>
-__device__ __forceinline__ void tc32_load_x(const float* xs, int t, float (&x)[DK + 1]) {
+__device__ __forceinline__ void tc32_load_x(const uint8_t* xs, int t, float (&x)[DK + 1]) {
 #pragma unroll
   for (int e = 0; e < DK; e += 4) {
-    const float4 a = *reinterpret_cast<const float4*>(xs + t * DK + e);
+    const float4 a = *reinterpret_cast<const float4*>(xs + (e / 4) * 2048 + t * 16);
     x[e] = a.x; x[e + 1] = a.y; x[e + 2] = a.z; x[e + 3] = a.w;
   }
 }
@@ -324,12 +305,11 @@ span_state_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_
       const int valid = (int)min((long long)TC_C, u.t_end - t0);
       if (!tc_wait_warp(B, X.stg_full(), c & 1u)) break;
       if (c > 0 && !tc_wait_warp(B, B.chunk(), (c - 1) & 1u)) break;   // v tiles free
-      tc32_convert_v(reinterpret_cast<const float*>(smem + L.vs), smem + L.vh, smem + L.vl, W, tid & 127,
-                     half);
+      tc32_convert_rows(smem + L.vs, smem + L.vh, smem + L.vl, W, tid & 127, half);
       float xk[2][DK + 1];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        tc32_load_x<DK>(reinterpret_cast<const float*>(smem + L.ks), 64 * h + tq, xk[h]);
+        tc32_load_x<DK>(smem + L.ks, 64 * h + tq, xk[h]);
         xk[h][DK] = (64 * h + tq < valid) ? 1.0f : 0.0f;
       }
       tc::fence_proxy_async();
@@ -405,6 +385,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
   const uint32_t tm = *B.tmem_slot();
   const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
   const uint32_t col_O = (uint32_t)(NB * nm);
+  const uint32_t col_A = col_O + (uint32_t)nm;   // A has its own columns (no overlap with O)
   const int i = wq * 32 + lane;   // TMEM lane = query row / feature row of a block
 
   // initial state -> TMEM, then its hi/lo copies
@@ -460,14 +441,13 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
     for (int c = 0; c < u.n_chunks && ok; ++c) {
       const long long t0 = u.t_begin + (long long)c * TC_C;
       const bool need_update = single || (c + 1 < u.n_chunks);
-      // the workers' tile conversion also follows their reading of O (A and O
-      // share their TMEM columns)
+      // the workers' tile conversion follows their reading of O and of A
       if (!(ok = tc_wait_warp(B, X.tiles(), c & 1u))) break;
       ++got;
       tc::fence_after_sync();
 #pragma unroll
       for (int k = 0; k < DK / 16; ++k)
-        mma3(tm + col_O, dQh + (uint64_t)(k * 256), dQl + (uint64_t)(k * 256), dKh + (uint64_t)(k * 256),
+        mma3(tm + col_A, dQh + (uint64_t)(k * 256), dQl + (uint64_t)(k * 256), dKh + (uint64_t)(k * 256),
              dKl + (uint64_t)(k * 256), id_qk, k > 0 ? 1u : 0u);
       tc::mma_commit_elect(B.qk());
       if (c + 1 < u.n_chunks) {
@@ -475,20 +455,8 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
         tc32_issue_staging(L, smem, X.stg_full(), &tm_q, &tm_k, &tm_v, t0 + TC_C, u.head, u.c0, W, DK);
         ++req;
       }
-      // O = P [V, 1], keys in two halves
-      for (int kh2 = 0; kh2 < 2 && ok; ++kh2, pos.next()) {
-        if (!(ok = ring.take(B, pos.s))) break;
-        const uint32_t a = tc::smem_u32(smem + L.slot(pos.s));
-        const uint64_t dPh = tc::sdesc(a, 128, 1024), dPl = tc::sdesc(a + 16384, 128, 1024);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma3(tm + col_O, dPh + (uint64_t)(k * 16), dPl + (uint64_t)(k * 16), dVh + (uint64_t)(64 * kh2 + 16 * k),
-               dVl + (uint64_t)(64 * kh2 + 16 * k), id_pv, (kh2 > 0 || k > 0) ? 1u : 0u);
-        tc::mma_commit_elect(B.sempty(pos.s));
-      }
-      if (!ok) break;
       if (c > 0 && !(ok = tc_wait_warp(B, B.conv(), (c - 1) & 1u))) break;
-      // O += phi(Q_f) [S_f, z_f], 64 features at a time
+      // O = phi(Q_f) [S_f, z_f] summed over blocks, 64 features at a time
       for (int f = 0; f < NB && ok; ++f) {
         const int rows = S::rows(f);
         const uint32_t sb = (uint32_t)((size_t)f * 128 * nm * 2);
@@ -501,9 +469,21 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
           const int ks = min(64, rows - 64 * h) / 16;
           for (int k = 0; k < ks; ++k)
             mma3(tm + col_O, dAh + (uint64_t)(k * 16), dAl + (uint64_t)(k * 16), dSh + (uint64_t)(64 * h + 16 * k),
-                 dSl + (uint64_t)(64 * h + 16 * k), id_pv, 1u);
+                 dSl + (uint64_t)(64 * h + 16 * k), id_pv, (f > 0 || h > 0 || k > 0) ? 1u : 0u);
           tc::mma_commit_elect(B.sempty(pos.s));
         }
+      }
+      if (!ok) break;
+      // O += P [V, 1], keys in two halves
+      for (int kh2 = 0; kh2 < 2 && ok; ++kh2, pos.next()) {
+        if (!(ok = ring.take(B, pos.s))) break;
+        const uint32_t a = tc::smem_u32(smem + L.slot(pos.s));
+        const uint64_t dPh = tc::sdesc(a, 128, 1024), dPl = tc::sdesc(a + 16384, 128, 1024);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma3(tm + col_O, dPh + (uint64_t)(k * 16), dPl + (uint64_t)(k * 16), dVh + (uint64_t)(64 * kh2 + 16 * k),
+               dVl + (uint64_t)(64 * kh2 + 16 * k), id_pv, 1u);
+        tc::mma_commit_elect(B.sempty(pos.s));
       }
       if (!ok) break;
       tc::mma_commit_elect(B.odone());
@@ -541,11 +521,11 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
       const bool need_update = single || (c + 1 < u.n_chunks);
       if (!tc_wait_warp(B, X.stg_full(), c & 1u)) break;
       if (c > 0 && !tc_wait_warp(B, B.chunk(), (c - 1) & 1u)) break;   // operand tiles free
-      const float* qs = reinterpret_cast<const float*>(smem + L.qs);
-      const float* ks = reinterpret_cast<const float*>(smem + L.ks);
-      tc32_convert_x<DK>(qs, smem + L.qh, smem + L.ql, t, half);
-      tc32_convert_x<DK>(ks, smem + L.kh, smem + L.kl, t, half);
-      tc32_convert_v(reinterpret_cast<const float*>(smem + L.vs), smem + L.vh, smem + L.vl, W, t, half);
+      const uint8_t* qs = smem + L.qs;
+      const uint8_t* ks = smem + L.ks;
+      tc32_convert_rows(qs, smem + L.qh, smem + L.ql, DK, t, half);
+      tc32_convert_rows(ks, smem + L.kh, smem + L.kl, DK, t, half);
+      tc32_convert_rows(smem + L.vs, smem + L.vh, smem + L.vl, W, t, half);
       float xq[DK + 1], xk[2][DK + 1];
       tc32_load_x<DK>(qs, t, xq);
       xq[DK] = 1.0f;
@@ -557,49 +537,56 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
       tc::fence_proxy_async();
       tc_warp_arrive(X.stg_free(), lane);
       tc_warp_arrive(X.tiles(), lane);
-      if (!tc_wait_warp(B, B.qk(), c & 1u)) break;
-      tc::fence_after_sync();
-      // P = mask(T_n(A)) in two key halves (two ring slots): row i, keys
-      // 64*kh2 + 32*half + ... Both halves are written before either is
-      // published, because P [V,1] of the first half overwrites A (A and O
-      // share their TMEM columns).
-      bool ok = true;
-      const int ps0 = pos.s;
-      pos.next();
-      const int ps1 = pos.s;
-      pos.next();
-      ok = ring.acquire(B, ps0);
-      ok = ok && ring.acquire(B, ps1);
-      if (!ok) break;
-      for (int kh2 = 0; kh2 < 2; ++kh2) {
-        uint8_t* ph = smem + L.slot(kh2 ? ps1 : ps0) + (i / 8) * 1024 + (i % 8) * 16;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int jl = 32 * half + 8 * g, j0 = 64 * kh2 + jl;
-          uint4 h4 = make_uint4(0u, 0u, 0u, 0u), l4 = h4;
-          if (j0 <= row_hi) {   // warp-uniform: groups above the diagonal are zero
-            uint32_t rr[8];
-            tc::tmem_ld8(tm + lane_off + col_O + j0, rr);
-            tc::tmem_wait_ld();
-            float pv[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              pv[e] = (j0 + e <= i && i < valid) ? taylor_T<NT>(__uint_as_float(rr[e])) : 0.0f;
-            tc32_split8(pv, h4, l4);
-          }
-          *reinterpret_cast<uint4*>(ph + (jl / 8) * 128) = h4;
-          *reinterpret_cast<uint4*>(ph + 16384 + (jl / 8) * 128) = l4;
-        }
-      }
-      ring.release(B, ps0, lane);
-      ring.release(B, ps1, lane);
       // feature tiles: readout (token t, quarter 2h + half) then update
       // (token 64h + tq, quarter qq); one build call site
       const int n_ro = [] { int n = 0; for (int f = 0; f < NB; ++f) n += S::halves(f); return n; }();
       const int nuse = n_ro + (need_update ? 2 * NB : 0);
       int f = 0, h = 0;
+      bool ok = true;
       for (int k = 0; k <= nuse; ++k) {
         if (k == n_ro) {
+          // P = mask(T_n(A)) in two key halves (two ring slots): row i, keys
+          // 64*kh2 + 32*half + ...; built after the readout tiles, while the
+          // readout MMAs run
+          if (!(ok = tc_wait_warp(B, B.qk(), c & 1u))) break;
+          tc::fence_after_sync();
+          const int ps0 = pos.s;
+          pos.next();
+          const int ps1 = pos.s;
+          pos.next();
+          ok = ring.acquire(B, ps0);
+          ok = ok && ring.acquire(B, ps1);
+          if (!ok) break;
+          for (int kh2 = 0; kh2 < 2; ++kh2) {
+            uint8_t* ph = smem + L.slot(kh2 ? ps1 : ps0) + (i / 8) * 1024 + (i % 8) * 16;
+            const int jl0 = 32 * half, jb = 64 * kh2 + jl0;
+            if (jb <= row_hi) {   // warp-uniform: all 32 keys above the diagonal -> zeros
+              uint32_t rr[32];
+              tc::tmem_ld32(tm + lane_off + col_A + jb, rr);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                float pv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const int j = jb + 8 * g + e;
+                  pv[e] = (j <= i && i < valid) ? taylor_T<NT>(__uint_as_float(rr[8 * g + e])) : 0.0f;
+                }
+                uint4 h4, l4;
+                tc32_split8(pv, h4, l4);
+                *reinterpret_cast<uint4*>(ph + ((jl0 + 8 * g) / 8) * 128) = h4;
+                *reinterpret_cast<uint4*>(ph + 16384 + ((jl0 + 8 * g) / 8) * 128) = l4;
+              }
+            } else {
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                *reinterpret_cast<uint4*>(ph + ((jl0 + 8 * g) / 8) * 128) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(ph + 16384 + ((jl0 + 8 * g) / 8) * 128) = make_uint4(0u, 0u, 0u, 0u);
+              }
+            }
+          }
+          ring.release(B, ps0, lane);
+          ring.release(B, ps1, lane);
           // out = O[:, :W] / O[:, W]
           if (!(ok = tc_wait_warp(B, B.odone(), c & 1u))) break;
           tc::fence_after_sync();

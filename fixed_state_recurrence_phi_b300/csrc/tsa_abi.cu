@@ -10,6 +10,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <unordered_map>
 
 #include "../../include/tsa.h"
 #include "tsa_internal.h"
@@ -98,6 +99,21 @@ tsa_status scratch_free(void* p, cudaStream_t s) {
   cudaError_t e = cudaFreeAsync(p, s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync");
   return TSA_OK;
+}
+
+cudaError_t set_smem_once(const void* kernel, int smem) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, int> done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = done[dev].find(kernel);
+  if (it != done[dev].end() && it->second >= smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) done[dev][kernel] = smem;
+  return e;
 }
 
 int device_sm_count() {
@@ -231,20 +247,16 @@ static tsa_status launch_prefill_simt(const tsa_plan& pl, PrefillParams p, cudaS
   const unsigned grid = (unsigned)((long long)p.heads * pl.n_slices * pl.n_spans);
   cudaError_t e;
   if (pl.n_spans > 1) {
-    e = cudaFuncSetAttribute(span_state_kernel<T, DK, NT, W>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
+    e = set_smem_once((const void*)span_state_kernel<T, DK, NT, W>, (int)L::bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_state)");
     span_state_kernel<T, DK, NT, W><<<grid, 256, L::bytes, s>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch span_state");
     const int elems4 = (int)(L::DPAD * (p.dv + 1) / 4);
-    dim3 g2((elems4 + 255) / 256, p.heads);
-    span_scan_kernel<<<g2, 256, 0, s>>>(p.states, p.scratch, p.heads, pl.n_spans, elems4, p.accumulate);
-    e = cudaGetLastError();
+    e = launch_span_scan(p.states, p.scratch, p.heads, pl.n_spans, elems4, p.accumulate, s);
     if (e != cudaSuccess) return cuda_fail(e, "launch span_scan");
   }
-  e = cudaFuncSetAttribute(span_output_kernel<T, DK, NT, W>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
+  e = set_smem_once((const void*)span_output_kernel<T, DK, NT, W>, (int)L::bytes);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_output)");
   span_output_kernel<T, DK, NT, W><<<grid, 256, L::bytes, s>>>(p);
   e = cudaGetLastError();

@@ -10,6 +10,9 @@ tsa_status cuda_fail(cudaError_t e, const char* what);
 tsa_status check_config(const tsa_config* c);
 size_t state_floats_per_head(const tsa_config* c);
 int device_sm_count();
+// Raise a kernel's dynamic shared-memory limit to `smem` bytes once per device
+// (the attribute call costs microseconds of host time per prefill otherwise).
+cudaError_t set_smem_once(const void* kernel, int smem);
 tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl);
 tsa_status launch_prefill(const tsa_config* c, const tsa_plan& pl, PrefillParams p, cudaStream_t s);
 
