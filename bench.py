@@ -96,50 +96,77 @@ def _algorithmic_decode_bytes(w) -> int:
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled (every 100 ms) while the
-    timed work runs."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms; the summary
+    keeps the samples taken between __enter__ and __exit__ (the timed work).
+
+    The sampler process must be started before this process initialises CUDA:
+    a child process started after that slowed every later host-side CUDA call
+    of the parent about twofold (kernel launches, event records), whatever it
+    queried, while one started before had no effect."""
+    Q = ("timestamp,index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, local_rank: int):
+        vis = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+        self.gpu = vis[local_rank] if local_rank < len(vis) else str(local_rank)
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         self.p = None
+        self.t0 = self.t1 = None
 
-    def __enter__(self):
+    def start(self):
         try:
-            # 100 ms polling at the lowest CPU priority: faster polling (20 ms)
-            # slowed every host-side CUDA call of this process several-fold
-            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "100"],
-                                      stdout=self.f, stderr=subprocess.DEVNULL,
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                       "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL,
                                       preexec_fn=lambda: os.nice(19))
-            time.sleep(0.3)
         except Exception:
             self.p = None
         return self
 
-    def __exit__(self, *a):
+    def stop(self):
         if self.p is not None:
-            time.sleep(0.1)
             self.p.terminate()
             try:
                 self.p.wait(timeout=5)
             except Exception:
                 self.p.kill()
+            self.p = None
+
+    def __enter__(self):
+        time.sleep(0.25)
+        self.t0 = time.time()
+        return self
+
+    def __exit__(self, *a):
+        self.t1 = time.time()
+        time.sleep(0.15)
+
+    def _mine(self, rows):
+        """Rows of the GPU this rank uses: by uuid, by index, or the only one."""
+        if self.gpu.startswith("GPU-"):
+            return [r for r in rows if r[2].strip() == self.gpu]
+        idx = {r[1].strip() for r in rows}
+        if len(idx) == 1:
+            return rows
+        return [r for r in rows if r[1].strip() == self.gpu]
 
     def summary(self):
+        from datetime import datetime
+        self.stop()
         self.f.flush()
         self.f.seek(0)
         rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
         os.unlink(self.f.name)
+        rows = [r for r in rows if len(r) >= 11]
         sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
+        for r in self._mine(rows):
             try:
-                sm.append(float(r[1])); mx = max(mx, float(r[2]))
-                for nm, val in zip(names, r[5:9]):
+                ts = datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                if self.t0 is None or not (self.t0 <= ts <= self.t1):
+                    continue
+                sm.append(float(r[3])); mx = max(mx, float(r[4]))
+                for nm, val in zip(names, r[7:11]):
                     if "Active" in val and "Not" not in val:
                         reasons.add(nm)
             except (ValueError, IndexError):
@@ -147,7 +174,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "every_ms": 100}
 
 
 def cpu_baseline_prefill(w, max_heads=None):
@@ -196,6 +223,19 @@ def run_reference(args):
 
 
 def run_ours(args):
+    ws, rank, local = _dist()
+    # the extension build (a compiler subprocess when sources changed) and the
+    # clock sampler both start before CUDA is initialised (ClockSampler)
+    from fixed_state_recurrence_phi_b300 import build as tsa_build
+    tsa_build.build()
+    clk = ClockSampler(local).start()
+    try:
+        _run_ours(args, clk)
+    finally:
+        clk.stop()
+
+
+def _run_ours(args, clk):
     import torch
     ws, rank, local = _dist()
     if ws > 1:
@@ -205,8 +245,6 @@ def run_ours(args):
     else:
         torch.cuda.set_device(0)
     dev = torch.device("cuda", torch.cuda.current_device())
-    from fixed_state_recurrence_phi_b300 import build as tsa_build
-    tsa_build.build()
     from fixed_state_recurrence_phi_b300 import tsa as T
     from fixed_state_recurrence_phi_b300.inputs import torch_qkv
 
@@ -238,7 +276,6 @@ def run_ours(args):
     def prefill_step():
         T.prefill(cfg, w["N"], q, k, v, out, st, stream=stream)
 
-    gpu = torch.cuda.current_device()
     do_pre = args.only in ("all", "prefill")
     do_dec = args.only in ("all", "decode")
     ms = e2e_ms = host_us = float("nan"); h2d = d2h = 0
@@ -246,7 +283,7 @@ def run_ours(args):
     steps, reps = 1024, 3
     dw = DECODE
     dcfg = T.Config(dw["B"], dw["H"], dw["d_k"], dw["d_v"], dw["n_terms"], dw["dtype"])
-    with ClockSampler(gpu) as clk:
+    with clk:
       if do_pre:
           for _ in range(max(3, args.warmup)):
               flush.fill_(1.0)

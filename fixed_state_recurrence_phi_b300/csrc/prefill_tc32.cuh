@@ -419,6 +419,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
   tc::fence_after_sync();
   TcRingPos pos;
   pos.R = p.ring;
+  TSA_TRACE_DECL
 
   if (warp == 8) {
     // ------------------------------ issuer ---------------------------------
@@ -444,6 +445,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
       // the workers' tile conversion follows their reading of O and of A
       if (!(ok = tc_wait_warp(B, X.tiles(), c & 1u))) break;
       ++got;
+      TSA_TRACE_EVENT(1, c);
       tc::fence_after_sync();
 #pragma unroll
       for (int k = 0; k < DK / 16; ++k)
@@ -456,6 +458,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
         ++req;
       }
       if (c > 0 && !(ok = tc_wait_warp(B, B.conv(), (c - 1) & 1u))) break;
+      TSA_TRACE_EVENT(2, c);
       // O = phi(Q_f) [S_f, z_f] summed over blocks, 64 features at a time
       for (int f = 0; f < NB && ok; ++f) {
         const int rows = S::rows(f);
@@ -487,6 +490,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
       }
       if (!ok) break;
       tc::mma_commit_elect(B.odone());
+      TSA_TRACE_EVENT(3, c);
       // S_f += phi(K_f)^T [V, 1], 64 tokens at a time
       if (need_update) {
         for (int f = 0; f < NB && ok; ++f)
@@ -503,6 +507,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
         if (!ok) break;
       }
       tc::mma_commit_elect(B.chunk());
+      TSA_TRACE_EVENT(4, c);
     }
     tc::mma_commit_elect(B.drain());
     tc::mbar_wait(B.drain(), 0, TC_WAIT_NS);
@@ -519,8 +524,10 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
       const long long t0 = u.t_begin + (long long)c * TC_C;
       const int valid = (int)min((long long)TC_C, u.t_end - t0);
       const bool need_update = single || (c + 1 < u.n_chunks);
+      TSA_TRACE_EVENT(10, c);
       if (!tc_wait_warp(B, X.stg_full(), c & 1u)) break;
       if (c > 0 && !tc_wait_warp(B, B.chunk(), (c - 1) & 1u)) break;   // operand tiles free
+      TSA_TRACE_EVENT(11, c);
       const uint8_t* qs = smem + L.qs;
       const uint8_t* ks = smem + L.ks;
       tc32_convert_rows(qs, smem + L.qh, smem + L.ql, DK, t, half);
@@ -537,6 +544,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
       tc::fence_proxy_async();
       tc_warp_arrive(X.stg_free(), lane);
       tc_warp_arrive(X.tiles(), lane);
+      TSA_TRACE_EVENT(12, c);
       // feature tiles: readout (token t, quarter 2h + half) then update
       // (token 64h + tq, quarter qq); one build call site
       const int n_ro = [] { int n = 0; for (int f = 0; f < NB; ++f) n += S::halves(f); return n; }();
@@ -549,6 +557,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
           // 64*kh2 + 32*half + ...; built after the readout tiles, while the
           // readout MMAs run
           if (!(ok = tc_wait_warp(B, B.qk(), c & 1u))) break;
+          TSA_TRACE_EVENT(13, c);
           tc::fence_after_sync();
           const int ps0 = pos.s;
           pos.next();
@@ -587,32 +596,15 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
           }
           ring.release(B, ps0, lane);
           ring.release(B, ps1, lane);
-          // out = O[:, :W] / O[:, W]
-          if (!(ok = tc_wait_warp(B, B.odone(), c & 1u))) break;
-          tc::fence_after_sync();
-          uint32_t rr[16];
-          tc::tmem_ld16(tm + lane_off + col_O + W, rr);
-          tc::tmem_wait_ld();
-          const float inv = 1.0f / __uint_as_float(rr[0]);
-          for (int g = half; g < W / 16; g += 2) {
-            tc::tmem_ld16(tm + lane_off + col_O + g * 16, rr);
-            tc::tmem_wait_ld();
-            if (i < valid) {
-              float* dst = og + (size_t)(t0 + i) * p.dv + g * 16;
-#pragma unroll
-              for (int e = 0; e < 16; e += 4)
-                *reinterpret_cast<float4*>(dst + e) =
-                    make_float4(__uint_as_float(rr[e]) * inv, __uint_as_float(rr[e + 1]) * inv,
-                                __uint_as_float(rr[e + 2]) * inv, __uint_as_float(rr[e + 3]) * inv);
-            }
-          }
-          tc_warp_arrive(B.ofree(), lane);
+          TSA_TRACE_EVENT(14, c);
           f = 0;
           h = 0;
         }
         if (k == nuse) break;
         const bool upd = (k >= n_ro);
+        TSA_TRACE_EVENT(20, k);
         if (!(ok = ring.acquire(B, pos.s))) break;
+        TSA_TRACE_EVENT(21, k);
         const int g = upd ? qq : 2 * h + half;
         if (32 * g < S::rows(f)) {
           float x[DK + 1];
@@ -621,6 +613,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
           uint8_t* hi = smem + L.slot(pos.s) + (upd ? urow : rrow);
           build_phi32<DK, NT>(f, g, x, hi, hi + 16384, upd ? 127 : 63);
         }
+        TSA_TRACE_EVENT(22, k);
         ring.release(B, pos.s, lane);
         pos.next();
         // next (f, h): readouts walk the block's 64-feature halves, updates
@@ -628,13 +621,57 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
         if (++h == (upd ? 2 : S::halves(f))) { h = 0; ++f; }
       }
       if (!ok) break;
+      // out = O[:, :W] / O[:, W], after the update tiles so that the wait for O
+      // and the stores overlap the update MMAs. Thread row i, its half of W.
+      if (!tc_wait_warp(B, B.odone(), c & 1u)) break;
+      TSA_TRACE_EVENT(15, c);
+      tc::fence_after_sync();
+      {
+        uint32_t rd[16];
+        tc::tmem_ld16(tm + lane_off + col_O + W, rd);
+        const int cw = W / 2;   // columns of this half: [half*cw, +cw), cw = 8..64
+        float* dst = og + (size_t)(t0 + i) * p.dv + half * cw;
+        if (cw == 32) {
+          uint32_t rr[32];
+          tc::tmem_ld32(tm + lane_off + col_O + half * cw, rr);
+          tc::tmem_wait_ld();
+          const float inv = 1.0f / __uint_as_float(rd[0]);
+          if (i < valid) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(dst + e) =
+                  make_float4(__uint_as_float(rr[e]) * inv, __uint_as_float(rr[e + 1]) * inv,
+                              __uint_as_float(rr[e + 2]) * inv, __uint_as_float(rr[e + 3]) * inv);
+          }
+        } else {
+          tc::tmem_wait_ld();
+          const float inv = 1.0f / __uint_as_float(rd[0]);
+          for (int e0 = 0; e0 < cw; e0 += 8) {
+            uint32_t rr[8];
+            tc::tmem_ld8(tm + lane_off + col_O + half * cw + e0, rr);
+            tc::tmem_wait_ld();
+            if (i < valid) {
+#pragma unroll
+              for (int e = 0; e < 8; e += 4)
+                *reinterpret_cast<float4*>(dst + e0 + e) =
+                    make_float4(__uint_as_float(rr[e]) * inv, __uint_as_float(rr[e + 1]) * inv,
+                                __uint_as_float(rr[e + 2]) * inv, __uint_as_float(rr[e + 3]) * inv);
+            }
+          }
+        }
+      }
+      tc_warp_arrive(B.ofree(), lane);
+      TSA_TRACE_EVENT(16, c);
       // every MMA of the chunk done -> hi/lo copies of the updated state
       if (need_update) {
+        TSA_TRACE_EVENT(23, c);
         if (!tc_wait_warp(B, B.chunk(), c & 1u)) break;
+        TSA_TRACE_EVENT(24, c);
         tc::fence_after_sync();
         for (int fb = 0; fb < NB; ++fb)
           tc32_convert_state<DK, NT>(smem + L.sh, smem + L.sl, tm, lane_off, nm, fb, i, half);
       }
+      TSA_TRACE_EVENT(25, c);
       tc::fence_proxy_async();
       tc_warp_arrive(B.conv(), lane);
     }

@@ -19,6 +19,14 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+// Timeline trace points. They expand to nothing unless a diagnostic build
+// defines TSA_TRACE_DECL (declared once per kernel thread) and
+// TSA_TRACE_EVENT(event, arg) before including this header.
+#ifndef TSA_TRACE_DECL
+#define TSA_TRACE_DECL
+#define TSA_TRACE_EVENT(ev, a) ((void)0)
+#endif
+
 namespace tsa {
 namespace tc {
 
