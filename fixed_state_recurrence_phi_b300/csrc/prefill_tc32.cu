@@ -47,14 +47,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
-// [heads][N][inner] fp32 as 4-D (4, N, inner/4, heads); box (4, 128, cols/4, 1)
-// lands as a [col/4][token][4] fp32 tile.
-tsa_status make_tmap32(CUtensorMap* m, const void* base, int inner, long long N, int heads, int cols) {
+// [heads][N][inner] fp32 as 4-D (4, N, inner/4, heads); a box (4, rows,
+// cols/4, 1) is a [col/4][token][4] fp32 tile in shared memory.
+tsa_status make_tmap32(CUtensorMap* m, const void* base, int inner, long long N, int heads, int cols,
+                       int rows = TC_C) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   if (!enc) return fail(TSA_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
   cuuint64_t dims[4] = {4, (cuuint64_t)N, (cuuint64_t)(inner / 4), (cuuint64_t)heads};
   cuuint64_t strides[3] = {(cuuint64_t)inner * 4, 16, (cuuint64_t)N * inner * 4};
-  cuuint32_t box[4] = {4, (cuuint32_t)TC_C, (cuuint32_t)(cols / 4), 1};
+  cuuint32_t box[4] = {4, (cuuint32_t)rows, (cuuint32_t)(cols / 4), 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -77,10 +78,15 @@ tsa_status launch32(const tsa_plan& pl, const PrefillParams& pp, cudaStream_t s)
   const int smem = (int)smem_tc32<DK, NT>(pp.dv, p.ring);
   tsa_status st = device_error_word(&p.err);
   if (st != TSA_OK) return st;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if ((st = make_tmap32(&mq, pp.q, DK, pp.N, pp.heads, DK)) != TSA_OK) return st;
   if ((st = make_tmap32(&mk, pp.k, DK, pp.N, pp.heads, DK)) != TSA_OK) return st;
   if ((st = make_tmap32(&mv, pp.v, pp.dv, pp.N, pp.heads, pp.dv)) != TSA_OK) return st;
+  // output stores: one 32-token x dv/2 box per worker warp
+  memset(&mo, 0, sizeof(mo));
+  if (tc32_out_tma(S::ROWS, pp.dv + 16, pp.dv) &&
+      (st = make_tmap32(&mo, pp.out, pp.dv, pp.N, pp.heads, pp.dv / 2, 32)) != TSA_OK)
+    return st;
   const unsigned grid = (unsigned)((long long)pp.heads * pl.n_spans);
   cudaError_t e;
   if (pl.n_spans > 1) {
@@ -95,7 +101,7 @@ tsa_status launch32(const tsa_plan& pl, const PrefillParams& pp, cudaStream_t s)
   }
   e = set_smem_once((const void*)span_output_tc32_kernel<DK, NT>, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_output_tc32)");
-  span_output_tc32_kernel<DK, NT><<<grid, TC_THREADS, smem, s>>>(p, mq, mk, mv);
+  span_output_tc32_kernel<DK, NT><<<grid, TC_THREADS, smem, s>>>(p, mq, mk, mv, mo);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch span_output_tc32");
   return TSA_OK;

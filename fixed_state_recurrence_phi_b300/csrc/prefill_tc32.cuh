@@ -75,6 +75,7 @@ struct Tc32Smem {
 //   sfull      staging tiles (fp32 q, k, v) of the chunk landed   (1 + tx)
 //   sfree      workers have consumed the staging                 (8)
 //   tiles      workers wrote the hi/lo operand tiles              (8)
+//   ostored    output stores have read their staging              (8)
 //   ring sfull[3] / sempty[3], qk, odone, ofree, conv, chunk, drain as in
 //   prefill_tc.cuh
 struct Tc32Bars {
@@ -82,14 +83,22 @@ struct Tc32Bars {
   __device__ uint64_t* stg_full() const { return b + 0; }
   __device__ uint64_t* stg_free() const { return b + 1; }
   __device__ uint64_t* tiles() const { return b + 2; }
+  // every worker warp's output store has read its staging piece    (8)
+  __device__ uint64_t* ostored() const { return b + 3; }
   __device__ TcBars ring_bars() const { return TcBars{b}; }
   __device__ void init() const {
-    const uint32_t cnt[16] = {1, 8, 8, 1, 8, 8, 8, 1, 1, 1, 1, 1, 8, 8, 1, 1};
+    const uint32_t cnt[16] = {1, 8, 8, 8, 8, 8, 8, 1, 1, 1, 1, 1, 8, 8, 1, 1};
     for (int k = 0; k < 16; ++k) tc::mbar_init(b + k, cnt[k]);
     *TcBars{b}.abort_flag() = 0;
     tc::mbar_fence_init();
   }
 };
+
+// The output kernel stages each chunk's output tile (128 x W fp32) in the
+// state copies' area and writes it with TMA stores when that area holds it.
+__host__ __device__ constexpr bool tc32_out_tma(int rows, int nm, int W) {
+  return (size_t)rows * nm * 4 >= (size_t)128 * W * 4;
+}
 
 // hi and lo bf16 pairs of two fp32 values.
 __device__ __forceinline__ void tc32_split2(float a, float b, uint32_t& hi, uint32_t& lo) {
@@ -359,7 +368,8 @@ span_state_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_
 template <int DK, int NT>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q,
-                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_o) {
   using S = Tc32Shape<DK, NT>;
   constexpr int D = S::D, NB = S::NB, DPAD = round_up(D, 4);
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -387,6 +397,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
   const uint32_t col_O = (uint32_t)(NB * nm);
   const uint32_t col_A = col_O + (uint32_t)nm;   // A has its own columns (no overlap with O)
   const int i = wq * 32 + lane;   // TMEM lane = query row / feature row of a block
+  const bool out_tma = tc32_out_tma(S::ROWS, nm, W);
 
   // initial state -> TMEM, then its hi/lo copies
   if (tid < TC_WORKERS) {
@@ -627,32 +638,41 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
       TSA_TRACE_EVENT(15, c);
       tc::fence_after_sync();
       {
+        const int cw = W / 2;   // columns of this half: [half*cw, +cw), cw = 16, 32 or 64
         uint32_t rd[16];
         tc::tmem_ld16(tm + lane_off + col_O + W, rd);
-        const int cw = W / 2;   // columns of this half: [half*cw, +cw), cw = 8..64
-        float* dst = og + (size_t)(t0 + i) * p.dv + half * cw;
-        if (cw == 32) {
-          uint32_t rr[32];
-          tc::tmem_ld32(tm + lane_off + col_O + half * cw, rr);
-          tc::tmem_wait_ld();
-          const float inv = 1.0f / __uint_as_float(rd[0]);
-          if (i < valid) {
+        tc::tmem_wait_ld();
+        const float inv = 1.0f / __uint_as_float(rd[0]);
+        if (out_tma) {
+          // the warp's 32 rows x cw columns -> its staging piece [cw/4][32][4]
+          // in the state copies' area (idle from odone to the conversion),
+          // then one TMA store; rows past the sequence end are clipped
+          uint8_t* piece = smem + L.sh + (size_t)warp * 128 * cw;
+          for (int e0 = 0; e0 < cw; e0 += 16) {
+            uint32_t rr[16];
+            tc::tmem_ld16(tm + lane_off + col_O + half * cw + e0, rr);
+            tc::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4*>(dst + e) =
+            for (int e = 0; e < 16; e += 4)
+              *reinterpret_cast<float4*>(piece + ((e0 + e) / 4) * 512 + lane * 16) =
                   make_float4(__uint_as_float(rr[e]) * inv, __uint_as_float(rr[e + 1]) * inv,
                               __uint_as_float(rr[e + 2]) * inv, __uint_as_float(rr[e + 3]) * inv);
           }
+          tc::fence_proxy_async();
+          __syncwarp();
+          if (lane == 0 && t0 + wq * 32 < u.t_end) {
+            tc::tma_store_4d(&tm_o, piece, 0, (int)(t0 + wq * 32), (u.c0 + half * cw) / 4, u.head);
+            tc::bulk_commit();
+          }
         } else {
-          tc::tmem_wait_ld();
-          const float inv = 1.0f / __uint_as_float(rd[0]);
-          for (int e0 = 0; e0 < cw; e0 += 8) {
-            uint32_t rr[8];
-            tc::tmem_ld8(tm + lane_off + col_O + half * cw + e0, rr);
+          float* dst = og + (size_t)(t0 + i) * p.dv + half * cw;
+          for (int e0 = 0; e0 < cw; e0 += 16) {
+            uint32_t rr[16];
+            tc::tmem_ld16(tm + lane_off + col_O + half * cw + e0, rr);
             tc::tmem_wait_ld();
             if (i < valid) {
 #pragma unroll
-              for (int e = 0; e < 8; e += 4)
+              for (int e = 0; e < 16; e += 4)
                 *reinterpret_cast<float4*>(dst + e0 + e) =
                     make_float4(__uint_as_float(rr[e]) * inv, __uint_as_float(rr[e + 1]) * inv,
                                 __uint_as_float(rr[e + 2]) * inv, __uint_as_float(rr[e + 3]) * inv);
@@ -666,6 +686,12 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
       if (need_update) {
         TSA_TRACE_EVENT(23, c);
         if (!tc_wait_warp(B, B.chunk(), c & 1u)) break;
+        if (out_tma) {
+          // every warp's output store has read its piece of the area
+          if (lane == 0) tc::bulk_wait_read();
+          tc_warp_arrive(X.ostored(), lane);
+          if (!tc_wait_warp(B, X.ostored(), c & 1u)) break;
+        }
         TSA_TRACE_EVENT(24, c);
         tc::fence_after_sync();
         for (int fb = 0; fb < NB; ++fb)
@@ -676,6 +702,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
       tc_warp_arrive(B.conv(), lane);
     }
   }
+  if (out_tma && tid < TC_WORKERS && lane == 0) tc::bulk_wait_all();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
