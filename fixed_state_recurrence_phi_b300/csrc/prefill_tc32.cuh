@@ -76,6 +76,7 @@ struct Tc32Smem {
 //   sfree      workers have consumed the staging                 (8)
 //   tiles      workers wrote the hi/lo operand tiles              (8)
 //   ostored    output stores have read their staging              (8)
+//   pready     P written into TMEM over the scores A              (8)
 //   ring sfull[3] / sempty[3], qk, odone, ofree, conv, chunk, drain as in
 //   prefill_tc.cuh
 struct Tc32Bars {
@@ -85,6 +86,9 @@ struct Tc32Bars {
   __device__ uint64_t* tiles() const { return b + 2; }
   // every worker warp's output store has read its staging piece    (8)
   __device__ uint64_t* ostored() const { return b + 3; }
+  // every worker warp wrote its P pieces into TMEM (the ring's ofree slot,
+  // which these kernels do not otherwise use)                        (8)
+  __device__ uint64_t* pready() const { return b + 12; }
   __device__ TcBars ring_bars() const { return TcBars{b}; }
   __device__ void init() const {
     const uint32_t cnt[16] = {1, 8, 8, 8, 8, 8, 8, 1, 1, 1, 1, 1, 8, 8, 1, 1};
@@ -178,6 +182,21 @@ __device__ __forceinline__ void mma3(uint32_t d, uint64_t ah, uint64_t al, uint6
   tc::mma_bf16_elect(d, ah, bl, id, 1u);
   tc::mma_bf16_elect(d, al, bh, id, 1u);
 }
+
+// The same with A in TMEM (hi and lo halves at a_hi and a_lo).
+__device__ __forceinline__ void mma3_ts(uint32_t d, uint32_t ah, uint32_t al, uint64_t bh, uint64_t bl, uint32_t id,
+                                        uint32_t acc) {
+  tc::mma_bf16_ts_elect(d, ah, bh, id, acc);
+  tc::mma_bf16_ts_elect(d, ah, bl, id, 1u);
+  tc::mma_bf16_ts_elect(d, al, bh, id, 1u);
+}
+
+// P in TMEM, written over the scores A: the worker warp of half h owns keys
+// [32h, 32h + 32) and [64 + 32h, 64 + 32h + 32) of its rows and puts the hi and
+// lo bf16 pairs of each 32-key piece in the piece's own 32 columns (hi in the
+// first 16, lo in the last 16). Keys [16k, 16k + 16) are then 8 columns at
+// tc32_p_col(k) (hi) and tc32_p_col(k) + 16 (lo) past the start of A.
+__host__ __device__ constexpr int tc32_p_col(int k) { return 32 * (k / 2) + 8 * (k % 2); }
 
 // Workers: fp32 staging ([col/4][t][4]) -> hi/lo operand tiles. q, k:
 // [e/8][t][8] (K-major); v: [c/8][t][8] (MN-major), W value columns (the
@@ -463,11 +482,6 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
         mma3(tm + col_A, dQh + (uint64_t)(k * 256), dQl + (uint64_t)(k * 256), dKh + (uint64_t)(k * 256),
              dKl + (uint64_t)(k * 256), id_qk, k > 0 ? 1u : 0u);
       tc::mma_commit_elect(B.qk());
-      if (c + 1 < u.n_chunks) {
-        if (!(ok = tc_wait_warp(B, X.stg_free(), c & 1u))) break;
-        tc32_issue_staging(L, smem, X.stg_full(), &tm_q, &tm_k, &tm_v, t0 + TC_C, u.head, u.c0, W, DK);
-        ++req;
-      }
       if (c > 0 && !(ok = tc_wait_warp(B, B.conv(), (c - 1) & 1u))) break;
       TSA_TRACE_EVENT(2, c);
       // O = phi(Q_f) [S_f, z_f] summed over blocks, 64 features at a time
@@ -488,18 +502,20 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
         }
       }
       if (!ok) break;
-      // O += P [V, 1], keys in two halves
-      for (int kh2 = 0; kh2 < 2 && ok; ++kh2, pos.next()) {
-        if (!(ok = ring.take(B, pos.s))) break;
-        const uint32_t a = tc::smem_u32(smem + L.slot(pos.s));
-        const uint64_t dPh = tc::sdesc(a, 128, 1024), dPl = tc::sdesc(a + 16384, 128, 1024);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma3(tm + col_O, dPh + (uint64_t)(k * 16), dPl + (uint64_t)(k * 16), dVh + (uint64_t)(64 * kh2 + 16 * k),
-               dVl + (uint64_t)(64 * kh2 + 16 * k), id_pv, 1u);
-        tc::mma_commit_elect(B.sempty(pos.s));
+      // the workers have converted the staged chunk: fetch the next one
+      if (c + 1 < u.n_chunks) {
+        if (!(ok = tc_wait_warp(B, X.stg_free(), c & 1u))) break;
+        tc32_issue_staging(L, smem, X.stg_full(), &tm_q, &tm_k, &tm_v, t0 + TC_C, u.head, u.c0, W, DK);
+        ++req;
       }
-      if (!ok) break;
+      // O += P [V, 1], P from TMEM, 16 keys per step
+      if (!(ok = tc_wait_warp(B, X.pready(), c & 1u))) break;
+      tc::fence_after_sync();
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t ph = tm + col_A + (uint32_t)tc32_p_col(k);
+        mma3_ts(tm + col_O, ph, ph + 16u, dVh + (uint64_t)(16 * k), dVl + (uint64_t)(16 * k), id_pv, 1u);
+      }
       tc::mma_commit_elect(B.odone());
       TSA_TRACE_EVENT(3, c);
       // S_f += phi(K_f)^T [V, 1], 64 tokens at a time
@@ -536,14 +552,14 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
       const int valid = (int)min((long long)TC_C, u.t_end - t0);
       const bool need_update = single || (c + 1 < u.n_chunks);
       TSA_TRACE_EVENT(10, c);
+      // q, k of the chunk -> hi/lo tiles for Q K^T (the previous Q K^T is done:
+      // its P was read) and this thread's feature inputs
       if (!tc_wait_warp(B, X.stg_full(), c & 1u)) break;
-      if (c > 0 && !tc_wait_warp(B, B.chunk(), (c - 1) & 1u)) break;   // operand tiles free
       TSA_TRACE_EVENT(11, c);
       const uint8_t* qs = smem + L.qs;
       const uint8_t* ks = smem + L.ks;
       tc32_convert_rows(qs, smem + L.qh, smem + L.ql, DK, t, half);
       tc32_convert_rows(ks, smem + L.kh, smem + L.kl, DK, t, half);
-      tc32_convert_rows(smem + L.vs, smem + L.vh, smem + L.vl, W, t, half);
       float xq[DK + 1], xk[2][DK + 1];
       tc32_load_x<DK>(qs, t, xq);
       xq[DK] = 1.0f;
@@ -553,7 +569,6 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
         xk[h][DK] = (64 * h + tq < valid) ? 1.0f : 0.0f;
       }
       tc::fence_proxy_async();
-      tc_warp_arrive(X.stg_free(), lane);
       tc_warp_arrive(X.tiles(), lane);
       TSA_TRACE_EVENT(12, c);
       // feature tiles: readout (token t, quarter 2h + half) then update
@@ -562,51 +577,64 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
       const int nuse = n_ro + (need_update ? 2 * NB : 0);
       int f = 0, h = 0;
       bool ok = true;
+      // the previous chunk's state -> hi/lo copies once the first readout
+      // tiles are built (while that chunk's update MMAs ran): no later than
+      // the ring is full, as the readout MMAs that free it wait for the copies
+      const int k_conv = min(n_ro, p.ring);
       for (int k = 0; k <= nuse; ++k) {
+        if (k == k_conv) {
+          if (c > 0) {
+            TSA_TRACE_EVENT(23, c);
+            if (!(ok = tc_wait_warp(B, B.chunk(), (c - 1) & 1u))) break;
+            if (out_tma) {
+              // every warp's output store has read its piece of the area
+              if (lane == 0) tc::bulk_wait_read();
+              tc_warp_arrive(X.ostored(), lane);
+              if (!(ok = tc_wait_warp(B, X.ostored(), (c - 1) & 1u))) break;
+            }
+            TSA_TRACE_EVENT(24, c);
+            tc::fence_after_sync();
+            for (int fb = 0; fb < NB; ++fb)
+              tc32_convert_state<DK, NT>(smem + L.sh, smem + L.sl, tm, lane_off, nm, fb, i, half);
+            tc::fence_proxy_async();
+            tc_warp_arrive(B.conv(), lane);
+            TSA_TRACE_EVENT(25, c);
+          }
+        }
         if (k == n_ro) {
-          // P = mask(T_n(A)) in two key halves (two ring slots): row i, keys
-          // 64*kh2 + 32*half + ...; built after the readout tiles, while the
-          // readout MMAs run
+          // readout tiles built: v -> hi/lo tiles (the previous chunk's
+          // update MMAs, which read v, are done), then P
+          tc32_convert_rows(smem + L.vs, smem + L.vh, smem + L.vl, W, t, half);
+          tc::fence_proxy_async();
+          tc_warp_arrive(X.stg_free(), lane);
+          // P = mask(T_n(A)) written over A in TMEM (tc32_p_col): row i, the
+          // warp's two 32-key pieces, while the readout MMAs run
           if (!(ok = tc_wait_warp(B, B.qk(), c & 1u))) break;
           TSA_TRACE_EVENT(13, c);
           tc::fence_after_sync();
-          const int ps0 = pos.s;
-          pos.next();
-          const int ps1 = pos.s;
-          pos.next();
-          ok = ring.acquire(B, ps0);
-          ok = ok && ring.acquire(B, ps1);
-          if (!ok) break;
           for (int kh2 = 0; kh2 < 2; ++kh2) {
-            uint8_t* ph = smem + L.slot(kh2 ? ps1 : ps0) + (i / 8) * 1024 + (i % 8) * 16;
-            const int jl0 = 32 * half, jb = 64 * kh2 + jl0;
+            const int jb = 64 * kh2 + 32 * half;
+            uint32_t ph[16], pl[16];
             if (jb <= row_hi) {   // warp-uniform: all 32 keys above the diagonal -> zeros
               uint32_t rr[32];
               tc::tmem_ld32(tm + lane_off + col_A + jb, rr);
               tc::tmem_wait_ld();
 #pragma unroll
-              for (int g = 0; g < 4; ++g) {
-                float pv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  const int j = jb + 8 * g + e;
-                  pv[e] = (j <= i && i < valid) ? taylor_T<NT>(__uint_as_float(rr[8 * g + e])) : 0.0f;
-                }
-                uint4 h4, l4;
-                tc32_split8(pv, h4, l4);
-                *reinterpret_cast<uint4*>(ph + ((jl0 + 8 * g) / 8) * 128) = h4;
-                *reinterpret_cast<uint4*>(ph + 16384 + ((jl0 + 8 * g) / 8) * 128) = l4;
+              for (int e = 0; e < 16; ++e) {
+                const int j = jb + 2 * e;
+                const float p0 = (j <= i && i < valid) ? taylor_T<NT>(__uint_as_float(rr[2 * e])) : 0.0f;
+                const float p1 = (j + 1 <= i && i < valid) ? taylor_T<NT>(__uint_as_float(rr[2 * e + 1])) : 0.0f;
+                tc32_split2(p0, p1, ph[e], pl[e]);
               }
             } else {
 #pragma unroll
-              for (int g = 0; g < 4; ++g) {
-                *reinterpret_cast<uint4*>(ph + ((jl0 + 8 * g) / 8) * 128) = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(ph + 16384 + ((jl0 + 8 * g) / 8) * 128) = make_uint4(0u, 0u, 0u, 0u);
-              }
+              for (int e = 0; e < 16; ++e) ph[e] = pl[e] = 0u;
             }
+            tc::tmem_st16(tm + lane_off + col_A + jb, ph);
+            tc::tmem_st16(tm + lane_off + col_A + jb + 16, pl);
           }
-          ring.release(B, ps0, lane);
-          ring.release(B, ps1, lane);
+          tc::tmem_wait_st();
+          tc_warp_arrive(X.pready(), lane);
           TSA_TRACE_EVENT(14, c);
           f = 0;
           h = 0;
@@ -680,26 +708,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
           }
         }
       }
-      tc_warp_arrive(B.ofree(), lane);
       TSA_TRACE_EVENT(16, c);
-      // every MMA of the chunk done -> hi/lo copies of the updated state
-      if (need_update) {
-        TSA_TRACE_EVENT(23, c);
-        if (!tc_wait_warp(B, B.chunk(), c & 1u)) break;
-        if (out_tma) {
-          // every warp's output store has read its piece of the area
-          if (lane == 0) tc::bulk_wait_read();
-          tc_warp_arrive(X.ostored(), lane);
-          if (!tc_wait_warp(B, X.ostored(), c & 1u)) break;
-        }
-        TSA_TRACE_EVENT(24, c);
-        tc::fence_after_sync();
-        for (int fb = 0; fb < NB; ++fb)
-          tc32_convert_state<DK, NT>(smem + L.sh, smem + L.sl, tm, lane_off, nm, fb, i, half);
-      }
-      TSA_TRACE_EVENT(25, c);
-      tc::fence_proxy_async();
-      tc_warp_arrive(B.conv(), lane);
     }
   }
   if (out_tma && tid < TC_WORKERS && lane == 0) tc::bulk_wait_all();

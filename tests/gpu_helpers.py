@@ -35,6 +35,7 @@ def gpu_prefill(cfg, q, k, v, states=None, accumulate=False):
     if states is None:
         states = T.new_states(cfg, q.device)
     T.prefill(cfg, N, q, k, v, out, states, accumulate=accumulate)
+    T.sync_status()   # a kernel that gave up on a wait reports it here
     return out, states
 
 
