@@ -101,7 +101,7 @@ tsa_status launch32(const tsa_plan& pl, const PrefillParams& pp, cudaStream_t s)
   }
   e = set_smem_once((const void*)span_output_tc32_kernel<DK, NT>, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_output_tc32)");
-  span_output_tc32_kernel<DK, NT><<<grid, TC_THREADS, smem, s>>>(p, mq, mk, mv, mo);
+  span_output_tc32_kernel<DK, NT><<<grid, TC32_OUT_THREADS, smem, s>>>(p, mq, mk, mv, mo);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch span_output_tc32");
   return TSA_OK;
@@ -115,7 +115,8 @@ tsa_status launch32(const tsa_plan& pl, const PrefillParams& pp, cudaStream_t s)
 bool tc32_fits(int dk, int nt, int dv) {
   if (!tc_supported(dk, nt) || dv % 16 != 0) return false;
   const int D = feat_dim(dk, nt), nb = (D + 127) / 128, nm = dv + 16;
-  if (nb * nm + nm + 128 > 512) return false;   // state, O and A in separate columns
+  // state, O, A and at least one readout feature tile in separate TMEM columns
+  if (tc32_ro_bufs(nb, nm) == 0) return false;
   const size_t sm = smem_for(dk, nt, dv, 2);
   return sm > 0 && sm <= kSmemLimit;
 }

@@ -77,6 +77,8 @@ struct Tc32Smem {
 //   tiles      workers wrote the hi/lo operand tiles              (8)
 //   ostored    output stores have read their staging              (8)
 //   pready     P written into TMEM over the scores A              (8)
+//   stload, rofull[2] / roempty[2]  initial state copy, readout tiles in
+//              TMEM (after the TMEM allocation word and the abort flag)
 //   ring sfull[3] / sempty[3], qk, odone, ofree, conv, chunk, drain as in
 //   prefill_tc.cuh
 struct Tc32Bars {
@@ -89,20 +91,68 @@ struct Tc32Bars {
   // every worker warp wrote its P pieces into TMEM (the ring's ofree slot,
   // which these kernels do not otherwise use)                        (8)
   __device__ uint64_t* pready() const { return b + 12; }
+  // the span's initial state copied into the ring area            (1 + tx)
+  __device__ uint64_t* stload() const { return b + 17; }
+  // readout feature tile r of the TMEM double buffer written           (8)
+  __device__ uint64_t* rofull(int r) const { return b + 18 + r; }
+  // ... and read by its MMAs                                          (1)
+  __device__ uint64_t* roempty(int r) const { return b + 20 + r; }
   __device__ TcBars ring_bars() const { return TcBars{b}; }
-  __device__ void init() const {
-    const uint32_t cnt[16] = {1, 8, 8, 8, 8, 8, 8, 1, 1, 1, 1, 1, 8, 8, 1, 1};
+  // stg_users: warps that read the staging (8, or 16 in the output kernel)
+  __device__ void init(uint32_t stg_users = 8) const {
+    const uint32_t cnt[16] = {1, stg_users, 8, 8, 8, 8, 8, 1, 1, 1, 1, 1, 8, 8, 1, 1};
     for (int k = 0; k < 16; ++k) tc::mbar_init(b + k, cnt[k]);
+    for (int r = 0; r < 2; ++r) {
+      tc::mbar_init(rofull(r), 8);
+      tc::mbar_init(roempty(r), 1);
+    }
+    tc::mbar_init(stload(), 1);
     *TcBars{b}.abort_flag() = 0;
     tc::mbar_fence_init();
   }
 };
+
+// The output kernel's warps: 8 TMEM warps (0-7: operand and state
+// conversions, P, the output), 8 builder warps (8-15: feature tiles) and the
+// MMA issuer (16).
+// (17 warps put 5 on one SM sub-partition, whose 16,384 registers then
+// allow 96 per thread)
+constexpr int TC32_OUT_THREADS = 544;
+constexpr int TC32_BUILDER0 = 256;   // first builder thread
+constexpr int TC32_ISSUER_WARP = 16;
 
 // The output kernel stages each chunk's output tile (128 x W fp32) in the
 // state copies' area and writes it with TMA stores when that area holds it.
 __host__ __device__ constexpr bool tc32_out_tma(int rows, int nm, int W) {
   return (size_t)rows * nm * 4 >= (size_t)128 * W * 4;
 }
+
+// TMEM columns of the output kernel: the state blocks (nb x nm), O (nm), the
+// scores A / P (128), then 1 or 2 readout feature tiles of 64 columns (hi and
+// lo bf16 pairs of 64 features).
+__host__ __device__ constexpr int tc32_ro_bufs(int nb, int nm) {
+  return nb * nm + nm + 128 + 128 <= 512 ? 2 : (nb * nm + nm + 128 + 64 <= 512 ? 1 : 0);
+}
+
+// A worker warp's side of a ring of n slots with explicit barriers (full:
+// the warps wrote the slot; empty: its MMAs are done).
+struct Tc32Ring {
+  uint32_t eph = 0, pend = 0;
+  int s = 0, n = 2;
+  __device__ __forceinline__ bool acquire(const TcBars& B, uint64_t* empty) {
+    if (!((pend >> s) & 1u)) return true;
+    const bool ok = tc_wait_warp(B, empty, (eph >> s) & 1u);
+    eph ^= 1u << s;
+    pend &= ~(1u << s);
+    return ok;
+  }
+  __device__ __forceinline__ void release_tmem(uint64_t* full, int lane) {
+    tc::tmem_wait_st();
+    tc_warp_arrive(full, lane);
+    pend |= 1u << s;
+    s = (s + 1 == n) ? 0 : s + 1;
+  }
+};
 
 // hi and lo bf16 pairs of two fp32 values.
 __device__ __forceinline__ void tc32_split2(float a, float b, uint32_t& hi, uint32_t& lo) {
@@ -142,6 +192,70 @@ template <int DK, int NT, int F, int G>
 struct Phi32Groups<DK, NT, F, G, 0> {
   static __device__ __forceinline__ void run(const float (&)[DK + 1], uint8_t*, uint8_t*, int) {}
 };
+
+// Features [F*128 + 32*G, +32) of one token in fp32, split into hi and lo
+// bf16 pairs in registers: pair e (features 2e, 2e + 1 of the quarter) in
+// hi[e] and lo[e] (element 2e in the low half).
+template <int DK, int NT, int F, int G, int E>
+struct Phi32Reg {
+  static __device__ __forceinline__ void run(const float (&x)[DK + 1], uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+    Phi32Reg<DK, NT, F, G, E - 1>::run(x, hi, lo);
+    constexpr int A = F * 128 + 32 * G + 2 * (E - 1);
+    tc32_split2(feat_value<DK, NT, A>(x), feat_value<DK, NT, A + 1>(x), hi[E - 1], lo[E - 1]);
+  }
+};
+template <int DK, int NT, int F, int G>
+struct Phi32Reg<DK, NT, F, G, 0> {
+  static __device__ __forceinline__ void run(const float (&)[DK + 1], uint32_t (&)[16], uint32_t (&)[16]) {}
+};
+
+// Runtime (block f, quarter g) -> instantiation; one call site per kernel.
+template <int DK, int NT, int F = 0>
+__device__ __forceinline__ void build_phi32_regs(int f, int g, const float (&x)[DK + 1], uint32_t (&hi)[16],
+                                                 uint32_t (&lo)[16]) {
+  if constexpr (F < Tc32Shape<DK, NT>::NB) {
+    if (f == F) {
+      switch (g) {
+        case 0: Phi32Reg<DK, NT, F, 0, 16>::run(x, hi, lo); break;
+        case 1: Phi32Reg<DK, NT, F, 1, 16>::run(x, hi, lo); break;
+        case 2: Phi32Reg<DK, NT, F, 2, 16>::run(x, hi, lo); break;
+        default: Phi32Reg<DK, NT, F, 3, 16>::run(x, hi, lo); break;
+      }
+      return;
+    }
+    build_phi32_regs<DK, NT, F + 1>(f, g, x, hi, lo);
+  }
+}
+
+// One group of 8 features (block F, group G8: features F*128 + 8*G8 ..) of one
+// token, split and stored at `off` bytes past hi and lo.
+template <int DK, int NT, int F, int G8>
+__device__ __forceinline__ void phi32_group(const float (&x)[DK + 1], uint8_t* hi, uint8_t* lo, int off) {
+  constexpr int A = F * 128 + 8 * G8;
+  float v[8];
+  v[0] = feat_value<DK, NT, A + 0>(x); v[1] = feat_value<DK, NT, A + 1>(x);
+  v[2] = feat_value<DK, NT, A + 2>(x); v[3] = feat_value<DK, NT, A + 3>(x);
+  v[4] = feat_value<DK, NT, A + 4>(x); v[5] = feat_value<DK, NT, A + 5>(x);
+  v[6] = feat_value<DK, NT, A + 6>(x); v[7] = feat_value<DK, NT, A + 7>(x);
+  uint4 h, l;
+  tc32_split8(v, h, l);
+  *reinterpret_cast<uint4*>(hi + off) = h;
+  *reinterpret_cast<uint4*>(lo + off) = l;
+}
+
+// Groups gb + g0, gb + g0 + stride, ... below ge of the last feature block
+// (fewer than 128 rows), so that every builder thread of a tile takes a share
+// of its few rows.
+template <int DK, int NT, int G8 = 0>
+__device__ __forceinline__ void build_phi32_last(int gb, int ge, int g0, int stride, const float (&x)[DK + 1],
+                                                 uint8_t* hi, uint8_t* lo, int mask) {
+  using S = Tc32Shape<DK, NT>;
+  if constexpr (G8 < S::LAST_ROWS / 8) {
+    if (G8 >= gb && G8 < ge && (G8 - gb) % stride == g0)
+      phi32_group<DK, NT, S::NB - 1, G8>(x, hi, lo, (((8 * G8) & mask) >> 3) * 128);
+    build_phi32_last<DK, NT, G8 + 1>(gb, ge, g0, stride, x, hi, lo, mask);
+  }
+}
 
 // Runtime (block f, quarter g) -> instantiation; one call site per kernel.
 template <int DK, int NT, int F = 0>
@@ -385,7 +499,7 @@ span_state_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_
 // the chunk the workers split the updated state into its hi/lo copies.
 // ---------------------------------------------------------------------------
 template <int DK, int NT>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+__global__ void __launch_bounds__(TC32_OUT_THREADS, 1)
 span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_o) {
@@ -400,9 +514,30 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wq = warp & 3, half = (warp >> 2) & 1;
   const bool single = (p.n_spans == 1);
   const size_t st_elems = (size_t)DPAD * (p.dv + 1);
+  TSA_TRACE_DECL
+  TSA_TRACE_EVENT(30, 0);
+  // the span's initial state: the span pass's prefix (several spans), the
+  // caller's state (ACCUMULATE) or zero
+  const float* st_src = nullptr;
+  if (!single) st_src = p.scratch + ((size_t)u.head * p.n_spans + u.span) * st_elems;
+  else if (p.accumulate) st_src = p.states + (size_t)u.head * st_elems;
+  const uint32_t st_bytes = (uint32_t)(st_elems * 4);
+  // one bulk copy into the (still idle) ring area when it fits there
+  const bool st_bulk = st_src != nullptr && st_bytes % 16 == 0 && st_bytes <= (uint32_t)p.ring * 32768u;
 
   if (warp == 0) tc::tmem_alloc(B.tmem_slot(), 512);
-  if (tid == 0) X.init();
+  if (tid == 0) X.init(16);
+  if (warp == 0) {
+    // first loads at once, overlapping the set-up below
+    __syncwarp();
+    if (st_bulk && tc::elect_one()) {
+      tc::mbar_arrive_expect_tx(X.stload(), st_bytes);
+      tc::bulk_load(smem + L.ring0, st_src, st_bytes, X.stload());
+    }
+    __syncwarp();
+    if (u.n_chunks > 0)
+      tc32_issue_staging(L, smem, X.stg_full(), &tm_q, &tm_k, &tm_v, u.t_begin, u.head, u.c0, W, DK);
+  }
   if (tid < TC_WORKERS) {
     tc_write_ones(smem + L.vh, W, tid);
     for (int e = tid; e < 256; e += TC_WORKERS)
@@ -415,43 +550,53 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
   const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
   const uint32_t col_O = (uint32_t)(NB * nm);
   const uint32_t col_A = col_O + (uint32_t)nm;   // A has its own columns (no overlap with O)
+  const uint32_t col_R = col_A + 128u;            // readout feature tiles, RB x 64 columns
+  const int RB = tc32_ro_bufs(NB, nm);
   const int i = wq * 32 + lane;   // TMEM lane = query row / feature row of a block
   const bool out_tma = tc32_out_tma(S::ROWS, nm, W);
 
+  TSA_TRACE_EVENT(31, 0);
   // initial state -> TMEM, then its hi/lo copies
   if (tid < TC_WORKERS) {
-    const float* src = nullptr;
-    if (!single) src = p.scratch + ((size_t)u.head * p.n_spans + u.span) * st_elems;
-    else if (p.accumulate) src = p.states + (size_t)u.head * st_elems;
+    const float* src = st_src;
+    if (st_bulk) {
+      // a failed wait leaves the abort flag set: every later wait gives up
+      tc_wait_warp(B, X.stload(), 0u);
+      src = reinterpret_cast<const float*>(smem + L.ring0);
+    }
     for (int f = 0; f < NB; ++f) {
       const int a = f * 128 + i;
       for (int g = half; g < nm / 16; g += 2) {
         uint32_t r[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int cc = g * 16 + e;
-          float x = 0.0f;
+        for (int e4 = 0; e4 < 4; ++e4) {
+          const int cc = g * 16 + 4 * e4;
+          float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
           if (src != nullptr && a < D) {
-            if (cc < W) x = src[(size_t)a * p.dv + u.c0 + cc];
-            else if (cc == W) x = src[(size_t)DPAD * p.dv + a];
+            if (cc < W) x = *reinterpret_cast<const float4*>(src + (size_t)a * p.dv + u.c0 + cc);
+            else if (cc == W) x.x = src[(size_t)DPAD * p.dv + a];
           }
-          r[e] = __float_as_uint(x);
+          r[4 * e4] = __float_as_uint(x.x);
+          r[4 * e4 + 1] = __float_as_uint(x.y);
+          r[4 * e4 + 2] = __float_as_uint(x.z);
+          r[4 * e4 + 3] = __float_as_uint(x.w);
         }
         tc::tmem_st16(tm + lane_off + f * nm + g * 16, r);
       }
     }
     tc::tmem_wait_st();
+    TSA_TRACE_EVENT(32, 0);
     for (int f = 0; f < NB; ++f) tc32_convert_state<DK, NT>(smem + L.sh, smem + L.sl, tm, lane_off, nm, f, i, half);
   }
   tc::fence_proxy_async();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  TSA_TRACE_EVENT(33, 0);
   TcRingPos pos;
   pos.R = p.ring;
-  TSA_TRACE_DECL
 
-  if (warp == 8) {
+  if (warp == TC32_ISSUER_WARP) {
     // ------------------------------ issuer ---------------------------------
     const uint32_t id_qk = tc::idesc_bf16(128, 128, false, false);
     const uint32_t id_pv = tc::idesc_bf16(128, nm, false, true);
@@ -463,11 +608,9 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
     const uint64_t dVh = tc::sdesc(tc::smem_u32(smem + L.vh), 128, 2048);
     const uint64_t dVl = tc::sdesc(tc::smem_u32(smem + L.vl), 128, 2048);
     TcIssuerRing ring;
-    int req = 0, got = 0;
-    if (u.n_chunks > 0) {
-      tc32_issue_staging(L, smem, X.stg_full(), &tm_q, &tm_k, &tm_v, u.t_begin, u.head, u.c0, W, DK);
-      req = 1;
-    }
+    int ro_s = 0;
+    uint32_t ro_ph = 0;
+    int req = u.n_chunks > 0 ? 1 : 0, got = 0;   // the first staging load was issued above
     bool ok = true;
     for (int c = 0; c < u.n_chunks && ok; ++c) {
       const long long t0 = u.t_begin + (long long)c * TC_C;
@@ -484,21 +627,26 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
       tc::mma_commit_elect(B.qk());
       if (c > 0 && !(ok = tc_wait_warp(B, B.conv(), (c - 1) & 1u))) break;
       TSA_TRACE_EVENT(2, c);
-      // O = phi(Q_f) [S_f, z_f] summed over blocks, 64 features at a time
+      // O = phi(Q_f) [S_f, z_f] summed over blocks, 64 features at a time,
+      // the feature tiles read from TMEM
       for (int f = 0; f < NB && ok; ++f) {
         const int rows = S::rows(f);
         const uint32_t sb = (uint32_t)((size_t)f * 128 * nm * 2);
         const uint64_t dSh = tc::sdesc(tc::smem_u32(smem + L.sh) + sb, 128, (uint32_t)rows * 16);
         const uint64_t dSl = tc::sdesc(tc::smem_u32(smem + L.sl) + sb, 128, (uint32_t)rows * 16);
-        for (int h = 0; h < S::halves(f); ++h, pos.next()) {
-          if (!(ok = ring.take(B, pos.s))) break;
-          const uint32_t a = tc::smem_u32(smem + L.slot(pos.s));
-          const uint64_t dAh = tc::sdesc(a, 128, 1024), dAl = tc::sdesc(a + 16384, 128, 1024);
+        for (int h = 0; h < S::halves(f); ++h) {
+          if (!(ok = tc_wait_warp(B, X.rofull(ro_s), (ro_ph >> ro_s) & 1u))) break;
+          ro_ph ^= 1u << ro_s;
+          tc::fence_after_sync();
+          const uint32_t a = tm + col_R + 64u * (uint32_t)ro_s;
           const int ks = min(64, rows - 64 * h) / 16;
-          for (int k = 0; k < ks; ++k)
-            mma3(tm + col_O, dAh + (uint64_t)(k * 16), dAl + (uint64_t)(k * 16), dSh + (uint64_t)(64 * h + 16 * k),
-                 dSl + (uint64_t)(64 * h + 16 * k), id_pv, (f > 0 || h > 0 || k > 0) ? 1u : 0u);
-          tc::mma_commit_elect(B.sempty(pos.s));
+          for (int k = 0; k < ks; ++k) {
+            const uint32_t ah = a + (uint32_t)tc32_p_col(k);
+            mma3_ts(tm + col_O, ah, ah + 16u, dSh + (uint64_t)(64 * h + 16 * k), dSl + (uint64_t)(64 * h + 16 * k),
+                    id_pv, (f > 0 || h > 0 || k > 0) ? 1u : 0u);
+          }
+          tc::mma_commit_elect(X.roempty(ro_s));
+          ro_s = (ro_s + 1 == RB) ? 0 : ro_s + 1;
         }
       }
       if (!ok) break;
@@ -539,129 +687,76 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
     tc::mma_commit_elect(B.drain());
     tc::mbar_wait(B.drain(), 0, TC_WAIT_NS);
     for (; got < req; ++got) tc::mbar_wait(X.stg_full(), got & 1u, TC_WAIT_NS);
-  } else {
-    // ------------------------------ workers --------------------------------
-    const int t = tid & 127, tq = tid & 63, qq = tid >> 6;
-    const int rrow = (t / 8) * 1024 + (t % 8) * 16;      // 128-token, 64-wide tiles
-    const int urow = (tq / 8) * 2048 + (tq % 8) * 16;    // 64-token, 128-wide tiles
+  } else if (tid < TC_WORKERS) {
+    // ---------------------------- TMEM warps -------------------------------
+    // q, k, v and the state -> hi/lo operands, P, the output; thread = TMEM
+    // lane i (query row / feature row), its half of the columns
+    const int t = tid & 127;
     const int row_hi = wq * 32 + 31;
     float* og = static_cast<float*>(p.out) + (size_t)u.head * p.N * p.dv + u.c0;
-    TcWorkerRing ring;
     for (int c = 0; c < u.n_chunks; ++c) {
       const long long t0 = u.t_begin + (long long)c * TC_C;
       const int valid = (int)min((long long)TC_C, u.t_end - t0);
-      const bool need_update = single || (c + 1 < u.n_chunks);
       TSA_TRACE_EVENT(10, c);
-      // q, k of the chunk -> hi/lo tiles for Q K^T (the previous Q K^T is done:
-      // its P was read) and this thread's feature inputs
+      // q, k -> hi/lo tiles for Q K^T (the previous Q K^T is done: its P was
+      // read; the previous output is written: O may be overwritten)
       if (!tc_wait_warp(B, X.stg_full(), c & 1u)) break;
-      TSA_TRACE_EVENT(11, c);
-      const uint8_t* qs = smem + L.qs;
-      const uint8_t* ks = smem + L.ks;
-      tc32_convert_rows(qs, smem + L.qh, smem + L.ql, DK, t, half);
-      tc32_convert_rows(ks, smem + L.kh, smem + L.kl, DK, t, half);
-      float xq[DK + 1], xk[2][DK + 1];
-      tc32_load_x<DK>(qs, t, xq);
-      xq[DK] = 1.0f;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        tc32_load_x<DK>(ks, 64 * h + tq, xk[h]);
-        xk[h][DK] = (64 * h + tq < valid) ? 1.0f : 0.0f;
-      }
+      tc32_convert_rows(smem + L.qs, smem + L.qh, smem + L.ql, DK, t, half);
+      tc32_convert_rows(smem + L.ks, smem + L.kh, smem + L.kl, DK, t, half);
       tc::fence_proxy_async();
       tc_warp_arrive(X.tiles(), lane);
       TSA_TRACE_EVENT(12, c);
-      // feature tiles: readout (token t, quarter 2h + half) then update
-      // (token 64h + tq, quarter qq); one build call site
-      const int n_ro = [] { int n = 0; for (int f = 0; f < NB; ++f) n += S::halves(f); return n; }();
-      const int nuse = n_ro + (need_update ? 2 * NB : 0);
-      int f = 0, h = 0;
-      bool ok = true;
-      // the previous chunk's state -> hi/lo copies once the first readout
-      // tiles are built (while that chunk's update MMAs ran): no later than
-      // the ring is full, as the readout MMAs that free it wait for the copies
-      const int k_conv = min(n_ro, p.ring);
-      for (int k = 0; k <= nuse; ++k) {
-        if (k == k_conv) {
-          if (c > 0) {
-            TSA_TRACE_EVENT(23, c);
-            if (!(ok = tc_wait_warp(B, B.chunk(), (c - 1) & 1u))) break;
-            if (out_tma) {
-              // every warp's output store has read its piece of the area
-              if (lane == 0) tc::bulk_wait_read();
-              tc_warp_arrive(X.ostored(), lane);
-              if (!(ok = tc_wait_warp(B, X.ostored(), (c - 1) & 1u))) break;
-            }
-            TSA_TRACE_EVENT(24, c);
-            tc::fence_after_sync();
-            for (int fb = 0; fb < NB; ++fb)
-              tc32_convert_state<DK, NT>(smem + L.sh, smem + L.sl, tm, lane_off, nm, fb, i, half);
-            tc::fence_proxy_async();
-            tc_warp_arrive(B.conv(), lane);
-            TSA_TRACE_EVENT(25, c);
-          }
+      if (c > 0) {
+        // the previous chunk's state -> hi/lo copies for this chunk's readouts
+        if (!tc_wait_warp(B, B.chunk(), (c - 1) & 1u)) break;
+        if (out_tma) {
+          // every warp's output store has read its piece of the area
+          if (lane == 0) tc::bulk_wait_read();
+          tc_warp_arrive(X.ostored(), lane);
+          if (!tc_wait_warp(B, X.ostored(), (c - 1) & 1u)) break;
         }
-        if (k == n_ro) {
-          // readout tiles built: v -> hi/lo tiles (the previous chunk's
-          // update MMAs, which read v, are done), then P
-          tc32_convert_rows(smem + L.vs, smem + L.vh, smem + L.vl, W, t, half);
-          tc::fence_proxy_async();
-          tc_warp_arrive(X.stg_free(), lane);
-          // P = mask(T_n(A)) written over A in TMEM (tc32_p_col): row i, the
-          // warp's two 32-key pieces, while the readout MMAs run
-          if (!(ok = tc_wait_warp(B, B.qk(), c & 1u))) break;
-          TSA_TRACE_EVENT(13, c);
-          tc::fence_after_sync();
-          for (int kh2 = 0; kh2 < 2; ++kh2) {
-            const int jb = 64 * kh2 + 32 * half;
-            uint32_t ph[16], pl[16];
-            if (jb <= row_hi) {   // warp-uniform: all 32 keys above the diagonal -> zeros
-              uint32_t rr[32];
-              tc::tmem_ld32(tm + lane_off + col_A + jb, rr);
-              tc::tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const int j = jb + 2 * e;
-                const float p0 = (j <= i && i < valid) ? taylor_T<NT>(__uint_as_float(rr[2 * e])) : 0.0f;
-                const float p1 = (j + 1 <= i && i < valid) ? taylor_T<NT>(__uint_as_float(rr[2 * e + 1])) : 0.0f;
-                tc32_split2(p0, p1, ph[e], pl[e]);
-              }
-            } else {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) ph[e] = pl[e] = 0u;
-            }
-            tc::tmem_st16(tm + lane_off + col_A + jb, ph);
-            tc::tmem_st16(tm + lane_off + col_A + jb + 16, pl);
-          }
-          tc::tmem_wait_st();
-          tc_warp_arrive(X.pready(), lane);
-          TSA_TRACE_EVENT(14, c);
-          f = 0;
-          h = 0;
-        }
-        if (k == nuse) break;
-        const bool upd = (k >= n_ro);
-        TSA_TRACE_EVENT(20, k);
-        if (!(ok = ring.acquire(B, pos.s))) break;
-        TSA_TRACE_EVENT(21, k);
-        const int g = upd ? qq : 2 * h + half;
-        if (32 * g < S::rows(f)) {
-          float x[DK + 1];
-#pragma unroll
-          for (int e = 0; e <= DK; ++e) x[e] = upd ? (h ? xk[1][e] : xk[0][e]) : xq[e];
-          uint8_t* hi = smem + L.slot(pos.s) + (upd ? urow : rrow);
-          build_phi32<DK, NT>(f, g, x, hi, hi + 16384, upd ? 127 : 63);
-        }
-        TSA_TRACE_EVENT(22, k);
-        ring.release(B, pos.s, lane);
-        pos.next();
-        // next (f, h): readouts walk the block's 64-feature halves, updates
-        // its two 64-token halves
-        if (++h == (upd ? 2 : S::halves(f))) { h = 0; ++f; }
+        TSA_TRACE_EVENT(24, c);
+        tc::fence_after_sync();
+        for (int fb = 0; fb < NB; ++fb)
+          tc32_convert_state<DK, NT>(smem + L.sh, smem + L.sl, tm, lane_off, nm, fb, i, half);
+        tc::fence_proxy_async();
+        tc_warp_arrive(B.conv(), lane);
+        TSA_TRACE_EVENT(25, c);
       }
-      if (!ok) break;
-      // out = O[:, :W] / O[:, W], after the update tiles so that the wait for O
-      // and the stores overlap the update MMAs. Thread row i, its half of W.
+      // v -> hi/lo tiles (the previous chunk's MMAs, which read v, are done)
+      tc32_convert_rows(smem + L.vs, smem + L.vh, smem + L.vl, W, t, half);
+      tc::fence_proxy_async();
+      tc_warp_arrive(X.stg_free(), lane);
+      // P = mask(T_n(A)) written over A in TMEM (tc32_p_col): row i, the
+      // warp's two 32-key pieces, while the readout MMAs run
+      if (!tc_wait_warp(B, B.qk(), c & 1u)) break;
+      TSA_TRACE_EVENT(13, c);
+      tc::fence_after_sync();
+      for (int kh2 = 0; kh2 < 2; ++kh2) {
+        const int jb = 64 * kh2 + 32 * half;
+        uint32_t ph[16], pl[16];
+        if (jb <= row_hi) {   // warp-uniform: all 32 keys above the diagonal -> zeros
+          uint32_t rr[32];
+          tc::tmem_ld32(tm + lane_off + col_A + jb, rr);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int j = jb + 2 * e;
+            const float p0 = (j <= i && i < valid) ? taylor_T<NT>(__uint_as_float(rr[2 * e])) : 0.0f;
+            const float p1 = (j + 1 <= i && i < valid) ? taylor_T<NT>(__uint_as_float(rr[2 * e + 1])) : 0.0f;
+            tc32_split2(p0, p1, ph[e], pl[e]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ph[e] = pl[e] = 0u;
+        }
+        tc::tmem_st16(tm + lane_off + col_A + jb, ph);
+        tc::tmem_st16(tm + lane_off + col_A + jb + 16, pl);
+      }
+      tc::tmem_wait_st();
+      tc_warp_arrive(X.pready(), lane);
+      TSA_TRACE_EVENT(14, c);
+      // out = O[:, :W] / O[:, W]; thread row i, its half of W
       if (!tc_wait_warp(B, B.odone(), c & 1u)) break;
       TSA_TRACE_EVENT(15, c);
       tc::fence_after_sync();
@@ -710,6 +805,90 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
       }
       TSA_TRACE_EVENT(16, c);
     }
+  } else {
+    // --------------------------- builder warps ------------------------------
+    // readout tiles (token t = this thread's TMEM lane, quarter 2h + half of
+    // a 64-feature half h) into TMEM, then update tiles (token 64h + tq,
+    // quarter qq) through the shared-memory ring; the feature arithmetic has
+    // one call site
+    const int bt = tid - TC32_BUILDER0;
+    const int t = bt & 127, tq = bt & 63, qq = bt >> 6;
+    const int urow = (tq / 8) * 2048 + (tq % 8) * 16;    // 64-token, 128-wide tiles
+    Tc32Ring ro;
+    ro.n = RB;
+    TcWorkerRing ring;
+    for (int c = 0; c < u.n_chunks; ++c) {
+      const long long t0 = u.t_begin + (long long)c * TC_C;
+      const int valid = (int)min((long long)TC_C, u.t_end - t0);
+      const bool need_update = single || (c + 1 < u.n_chunks);
+      if (!tc_wait_warp(B, X.stg_full(), c & 1u)) break;
+      TSA_TRACE_EVENT(11, c);
+      float xk[2][DK + 1];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        tc32_load_x<DK>(smem + L.ks, 64 * h + tq, xk[h]);
+        xk[h][DK] = (64 * h + tq < valid) ? 1.0f : 0.0f;
+      }
+      const int n_ro = [] { int n = 0; for (int f = 0; f < NB; ++f) n += S::halves(f); return n; }();
+      const int nuse = n_ro + (need_update ? 2 * NB : 0);
+      int f = 0, h = 0;
+      bool ok = true;
+      for (int k = 0; k < nuse; ++k) {
+        if (k == n_ro) {
+          // q and k of the staging are read
+          tc_warp_arrive(X.stg_free(), lane);
+          f = 0;
+          h = 0;
+        }
+        const bool upd = (k >= n_ro);
+        const int g = upd ? qq : 2 * h + half;
+        TSA_TRACE_EVENT(20, k);
+        if (!(ok = upd ? ring.acquire(B, pos.s) : ro.acquire(B, X.roempty(ro.s)))) break;
+        TSA_TRACE_EVENT(21, k);
+        float x[DK + 1];
+        if (upd) {
+#pragma unroll
+          for (int e = 0; e <= DK; ++e) x[e] = h ? xk[1][e] : xk[0][e];
+        } else {
+          tc32_load_x<DK>(smem + L.qs, t, x);
+          x[DK] = 1.0f;
+        }
+        if (upd && S::rows(f) < 128) {
+          // the last block's few rows, spread over the 4 threads of a token
+          uint8_t* hi = smem + L.slot(pos.s) + urow;
+          build_phi32_last<DK, NT>(0, S::LAST_ROWS / 8, qq, 4, x, hi, hi + 16384, 127);
+        } else if (32 * g < S::rows(f)) {
+          uint32_t hv[16], lv[16];
+          build_phi32_regs<DK, NT>(f, g, x, hv, lv);
+          if (upd) {
+            uint8_t* hi = smem + L.slot(pos.s) + urow;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int off = (4 * g + e) * 128;
+              *reinterpret_cast<uint4*>(hi + off) = make_uint4(hv[4 * e], hv[4 * e + 1], hv[4 * e + 2], hv[4 * e + 3]);
+              *reinterpret_cast<uint4*>(hi + 16384 + off) =
+                  make_uint4(lv[4 * e], lv[4 * e + 1], lv[4 * e + 2], lv[4 * e + 3]);
+            }
+          } else {
+            const uint32_t col = tm + lane_off + col_R + 64u * (uint32_t)ro.s + 32u * (uint32_t)half;
+            tc::tmem_st16(col, hv);
+            tc::tmem_st16(col + 16u, lv);
+          }
+        }
+        TSA_TRACE_EVENT(22, k);
+        if (upd) {
+          ring.release(B, pos.s, lane);
+          pos.next();
+        } else {
+          ro.release_tmem(X.rofull(ro.s), lane);
+        }
+        // next (f, h): readouts walk the block's 64-feature halves, updates
+        // its two 64-token halves
+        if (++h == (upd ? 2 : S::halves(f))) { h = 0; ++f; }
+      }
+      if (!ok) break;
+      if (!need_update) tc_warp_arrive(X.stg_free(), lane);
+    }
   }
   if (out_tma && tid < TC_WORKERS && lane == 0) tc::bulk_wait_all();
   tc::fence_before_sync();
@@ -726,6 +905,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
     tc::fence_after_sync();
     tc::tmem_dealloc(tm, 512);
   }
+  TSA_TRACE_EVENT(40, 0);
 }
 
 }  // namespace tsa
