@@ -24,6 +24,7 @@
 // On chip (shared memory, fp32): the state slice S[DROWS][W] and z[DROWS]; the
 // features are built DT at a time: phiQ^T[DT][C] and phiK[C][DT(+4)].
 #pragma once
+#include <cstring>
 #include "common.cuh"
 #include "prefill_params.h"
 
@@ -243,18 +244,22 @@ span_state_kernel(PrefillParams p) {
 // span_scan: exclusive prefix of span states, per head and element; the
 // running total after the last span is the final state.
 // ---------------------------------------------------------------------------
-static __global__ void __launch_bounds__(256)
+static __global__ void __launch_bounds__(128)
 span_scan_kernel(float* __restrict__ states, float* __restrict__ scratch, int heads, int n_spans,
                  int elems4, int accumulate) {
+  // the output pass may be launched now; it waits for this grid before it
+  // reads the prefixes. This grid waits for the span pass likewise.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int head = blockIdx.y;
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= elems4 || head >= heads) return;
   float4* st = reinterpret_cast<float4*>(states) + (size_t)head * elems4;
   float4* sc = reinterpret_cast<float4*>(scratch) + (size_t)head * n_spans * elems4;
   float4 run = accumulate ? st[e] : make_float4(0.f, 0.f, 0.f, 0.f);
-  // spans in groups of 8: all loads of a group are issued before its stores,
+  // spans in groups of 16: all loads of a group are issued before its stores,
   // so the memory latency is paid once per group rather than once per span
-  constexpr int G = 8;
+  constexpr int G = 16;
   for (int s0 = 0; s0 < n_spans; s0 += G) {
     float4 x[G];
 #pragma unroll
@@ -282,8 +287,19 @@ static inline cudaError_t launch_span_scan(float* states, float* scratch, int he
     if (e != cudaSuccess) return e;
     carveout_set = true;
   }
-  dim3 g2((elems4 + 255) / 256, heads);
-  span_scan_kernel<<<g2, 256, 0, s>>>(states, scratch, heads, n_spans, elems4, accumulate);
+  // launched with a programmatic dependency on the span pass before it
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((elems4 + 127) / 128, heads);
+  cfg.blockDim = dim3(128);
+  cfg.stream = s;
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, span_scan_kernel, states, scratch, heads, n_spans, elems4, accumulate);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

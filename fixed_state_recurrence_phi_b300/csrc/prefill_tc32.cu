@@ -101,7 +101,22 @@ tsa_status launch32(const tsa_plan& pl, const PrefillParams& pp, cudaStream_t s)
   }
   e = set_smem_once((const void*)span_output_tc32_kernel<DK, NT>, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_output_tc32)");
-  span_output_tc32_kernel<DK, NT><<<grid, TC32_OUT_THREADS, smem, s>>>(p, mq, mk, mv, mo);
+  // after the scan: launched with a programmatic dependency, so that its
+  // set-up and first input loads overlap the scan (it waits for the scan
+  // before reading the prefixes)
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(TC32_OUT_THREADS);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = pl.n_spans > 1 ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, span_output_tc32_kernel<DK, NT>, p, mq, mk, mv, mo);
+  if (e != cudaSuccess) return cuda_fail(e, "launch span_output_tc32");
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch span_output_tc32");
   return TSA_OK;

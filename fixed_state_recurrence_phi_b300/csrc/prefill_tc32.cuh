@@ -93,6 +93,8 @@ struct Tc32Bars {
   __device__ uint64_t* pready() const { return b + 12; }
   // the span's initial state copied into the ring area            (1 + tx)
   __device__ uint64_t* stload() const { return b + 17; }
+  // span pass: v tile buffer r free again (its MMAs are done)         (1)
+  __device__ uint64_t* vfree(int r) const { return b + 20 + r; }
   // readout feature tile r of the TMEM double buffer written           (8)
   __device__ uint64_t* rofull(int r) const { return b + 18 + r; }
   // ... and read by its MMAs                                          (1)
@@ -382,13 +384,27 @@ span_state_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_
   const Tc32Bars X{reinterpret_cast<uint64_t*>(smem + L.bar)};
   const TcBars B = X.ring_bars();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wq = warp & 3, half = (warp >> 2) & 1;
+  // v tiles in two buffers when the (here unused) state-copy area holds the
+  // second, so that the workers convert the next chunk's v while this
+  // chunk's MMAs still read the other
+  const bool v2 = S::ROWS >= 128;
+  auto vh_b = [&](int vb) { return vb ? smem + L.sh : smem + L.vh; };
+  auto vl_b = [&](int vb) { return vb ? smem + L.sh + (size_t)128 * nm * 2 : smem + L.vl; };
 
+  tc::grid_dep_launch();   // the scan after this pass may be launched now
   if (warp == 0) tc::tmem_alloc(B.tmem_slot(), 512);
   if (tid == 0) X.init();
+  if (warp == 0) {
+    __syncwarp();   // the first inputs at once, overlapping the set-up
+    if (u.n_chunks > 0)
+      tc32_issue_staging(L, smem, X.stg_full(), nullptr, &tm_k, &tm_v, u.t_begin, u.head, u.c0, W, DK);
+  }
   if (tid < TC_WORKERS) {
-    tc_write_ones(smem + L.vh, W, tid);
-    for (int e = tid; e < 256; e += TC_WORKERS)
-      *reinterpret_cast<uint4*>(smem + L.vl + (W / 8 + (e & 1)) * 2048 + (e >> 1) * 16) = make_uint4(0u, 0u, 0u, 0u);
+    for (int vb = 0; vb < (v2 ? 2 : 1); ++vb) {
+      tc_write_ones(vh_b(vb), W, tid);
+      for (int e = tid; e < 256; e += TC_WORKERS)
+        *reinterpret_cast<uint4*>(vl_b(vb) + (W / 8 + (e & 1)) * 2048 + (e >> 1) * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
   tc::fence_proxy_async();
   tc::fence_before_sync();
@@ -401,17 +417,14 @@ span_state_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_
 
   if (warp == 8) {
     const uint32_t id_up = tc::idesc_bf16(128, nm, true, true);
-    const uint64_t dVh = tc::sdesc(tc::smem_u32(smem + L.vh), 128, 2048);
-    const uint64_t dVl = tc::sdesc(tc::smem_u32(smem + L.vl), 128, 2048);
     TcIssuerRing ring;
-    int req = 0, got = 0;
-    if (u.n_chunks > 0) {
-      tc32_issue_staging(L, smem, X.stg_full(), nullptr, &tm_k, &tm_v, u.t_begin, u.head, u.c0, W, DK);
-      req = 1;
-    }
+    int req = u.n_chunks > 0 ? 1 : 0, got = 0;   // the first staging load was issued above
     bool ok = true;
     for (int c = 0; c < u.n_chunks && ok; ++c) {
       const long long t0 = u.t_begin + (long long)c * TC_C;
+      const int vb = v2 ? (c & 1) : 0;
+      const uint64_t dVh = tc::sdesc(tc::smem_u32(vh_b(vb)), 128, 2048);
+      const uint64_t dVl = tc::sdesc(tc::smem_u32(vl_b(vb)), 128, 2048);
       if (!(ok = tc_wait_warp(B, X.tiles(), c & 1u))) break;
       ++got;
       if (c + 1 < u.n_chunks) {
@@ -432,6 +445,7 @@ span_state_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_
           tc::mma_commit_elect(B.sempty(pos.s));
         }
       if (!ok) break;
+      if (v2) tc::mma_commit_elect(X.vfree(vb));
       tc::mma_commit_elect(B.chunk());
     }
     // drain: every MMA and every staging load that was requested
@@ -445,9 +459,14 @@ span_state_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_
     for (int c = 0; c < u.n_chunks; ++c) {
       const long long t0 = u.t_begin + (long long)c * TC_C;
       const int valid = (int)min((long long)TC_C, u.t_end - t0);
+      const int vb = v2 ? (c & 1) : 0;
       if (!tc_wait_warp(B, X.stg_full(), c & 1u)) break;
-      if (c > 0 && !tc_wait_warp(B, B.chunk(), (c - 1) & 1u)) break;   // v tiles free
-      tc32_convert_rows(smem + L.vs, smem + L.vh, smem + L.vl, W, tid & 127, half);
+      // the v buffer is free: (two buffers) the MMAs of chunk c - 2 are done,
+      // one barrier per buffer so that each wait is for its next phase;
+      // (one buffer) the MMAs of chunk c - 1 are done
+      if (v2 && c >= 2 && !tc_wait_warp(B, X.vfree(vb), ((c >> 1) - 1) & 1u)) break;
+      if (!v2 && c > 0 && !tc_wait_warp(B, B.chunk(), (c - 1) & 1u)) break;
+      tc32_convert_rows(smem + L.vs, vh_b(vb), vl_b(vb), W, tid & 127, half);
       float xk[2][DK + 1];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -461,13 +480,14 @@ span_state_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_
       for (int f = 0; f < NB && ok; ++f)
         for (int h = 0; h < 2; ++h, pos.next()) {
           if (!(ok = ring.acquire(B, pos.s))) break;
-          if (32 * qq < S::rows(f)) {
-            float x[DK + 1];
+          float x[DK + 1];
 #pragma unroll
-            for (int e = 0; e <= DK; ++e) x[e] = h ? xk[1][e] : xk[0][e];
-            uint8_t* hi = smem + L.slot(pos.s) + urow;
+          for (int e = 0; e <= DK; ++e) x[e] = h ? xk[1][e] : xk[0][e];
+          uint8_t* hi = smem + L.slot(pos.s) + urow;
+          if (S::rows(f) < 128)   // the last block's few rows, over the 4 threads of a token
+            build_phi32_last<DK, NT>(0, S::LAST_ROWS / 8, qq, 4, x, hi, hi + 16384, 127);
+          else
             build_phi32<DK, NT>(f, qq, x, hi, hi + 16384, 127);
-          }
           ring.release(B, pos.s, lane);
         }
       if (!ok) break;
@@ -528,15 +548,18 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
   if (warp == 0) tc::tmem_alloc(B.tmem_slot(), 512);
   if (tid == 0) X.init(16);
   if (warp == 0) {
-    // first loads at once, overlapping the set-up below
+    // first loads at once, overlapping the set-up below: the chunk's inputs
+    // (ready before this call's first launch), then, once the grid this one
+    // depends on (the scan) is done, the span's initial state
     __syncwarp();
+    if (u.n_chunks > 0)
+      tc32_issue_staging(L, smem, X.stg_full(), &tm_q, &tm_k, &tm_v, u.t_begin, u.head, u.c0, W, DK);
+    __syncwarp();
+    tc::grid_dep_wait();
     if (st_bulk && tc::elect_one()) {
       tc::mbar_arrive_expect_tx(X.stload(), st_bytes);
       tc::bulk_load(smem + L.ring0, st_src, st_bytes, X.stload());
     }
-    __syncwarp();
-    if (u.n_chunks > 0)
-      tc32_issue_staging(L, smem, X.stg_full(), &tm_q, &tm_k, &tm_v, u.t_begin, u.head, u.c0, W, DK);
   }
   if (tid < TC_WORKERS) {
     tc_write_ones(smem + L.vh, W, tid);
@@ -558,6 +581,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
   TSA_TRACE_EVENT(31, 0);
   // initial state -> TMEM, then its hi/lo copies
   if (tid < TC_WORKERS) {
+    tc::grid_dep_wait();
     const float* src = st_src;
     if (st_bulk) {
       // a failed wait leaves the abort flag set: every later wait gives up
