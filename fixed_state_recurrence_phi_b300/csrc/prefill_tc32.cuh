@@ -711,6 +711,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
     tc::mma_commit_elect(B.drain());
     tc::mbar_wait(B.drain(), 0, TC_WAIT_NS);
     for (; got < req; ++got) tc::mbar_wait(X.stg_full(), got & 1u, TC_WAIT_NS);
+    if (st_bulk) tc::mbar_wait(X.stload(), 0, TC_WAIT_NS);   // the initial-state copy, too
   } else if (tid < TC_WORKERS) {
     // ---------------------------- TMEM warps -------------------------------
     // q, k, v and the state -> hi/lo operands, P, the output; thread = TMEM
