@@ -43,6 +43,14 @@ struct Tc32Shape {
   __host__ __device__ static constexpr int rows(int f) { return f < NB - 1 ? 128 : LAST_ROWS; }
   // 64-feature readout uses of block f
   __host__ __device__ static constexpr int halves(int f) { return (rows(f) + 63) / 64; }
+  // The last block's update tile holds all 128 tokens of its few rows (at
+  // most 64) in one ring slot: feature group g8 of token t at
+  // (t/8)*GL*128 + g8*128 + (t%8)*16 bytes (hi; lo 16 KB further).
+  static constexpr int GL = LAST_ROWS / 8;
+  static constexpr bool COMPACT = LAST_ROWS <= 64;
+  // update tiles of block f: two 64-token tiles, or the one compact tile
+  __host__ __device__ static constexpr int upd_tiles(int f) { return (COMPACT && f == NB - 1) ? 1 : 2; }
+  __host__ __device__ static constexpr int n_upd() { return 2 * NB - (COMPACT ? 1 : 0); }
 };
 
 // Shared memory of the fp32 kernels (byte offsets, host and device).
@@ -368,6 +376,53 @@ __device__ __forceinline__ void tc32_convert_state(uint8_t* sh, uint8_t* sl, uin
   }
 }
 
+// Update MMAs of one tile (ring slot at shared address a) into the state
+// block at TMEM column d: a 64-token tile (tokens 64h..) of a full block, or
+// the compact 128-token tile of the last block's GL feature groups.
+__device__ __forceinline__ void tc32_issue_update(uint32_t d, uint32_t a, uint64_t dVh, uint64_t dVl, uint32_t id_up,
+                                                  bool compact, int GL, int h, bool acc0) {
+  if (!compact) {
+    const uint64_t dAh = tc::sdesc(a, 2048, 128), dAl = tc::sdesc(a + 16384, 2048, 128);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      mma3(d, dAh + (uint64_t)(k * 256), dAl + (uint64_t)(k * 256), dVh + (uint64_t)(64 * h + k * 16),
+           dVl + (uint64_t)(64 * h + k * 16), id_up, (acc0 || k > 0) ? 1u : 0u);
+  } else {
+    // token groups GL*128 bytes apart (K direction), feature groups 128 apart
+    const uint32_t lbo = (uint32_t)GL * 128u;
+    const uint64_t dAh = tc::sdesc(a, lbo, 128), dAl = tc::sdesc(a + 16384, lbo, 128);
+    for (int k = 0; k < 8; ++k)
+      mma3(d, dAh + (uint64_t)(k * 2 * lbo / 16), dAl + (uint64_t)(k * 2 * lbo / 16), dVh + (uint64_t)(16 * k),
+           dVl + (uint64_t)(16 * k), id_up, (acc0 || k > 0) ? 1u : 0u);
+  }
+}
+
+// One worker thread's share (of 256) of an update tile: a 64-token tile of a
+// full block (token 64h + (w & 63), quarter w >> 6), or the compact tile of
+// the last block (token w & 127, groups (w >> 7), (w >> 7) + 2, ..).
+// xk holds the thread's inputs for tokens (w & 63) and 64 + (w & 63).
+template <int DK, int NT>
+__device__ __forceinline__ void tc32_build_update(uint8_t* slot, int f, int h, int w, const float (&xk)[2][DK + 1]) {
+  using S = Tc32Shape<DK, NT>;
+  float x[DK + 1];
+  if (S::upd_tiles(f) == 1) {
+    const int t = w & 127;
+#pragma unroll
+    for (int e = 0; e <= DK; ++e) x[e] = ((w >> 6) & 1) ? xk[1][e] : xk[0][e];
+    uint8_t* hi = slot + (t / 8) * (S::GL * 128) + (t % 8) * 16;
+    build_phi32_last<DK, NT>(0, S::GL, w >> 7, 2, x, hi, hi + 16384, 127);
+  } else {
+    const int tq = w & 63, qq = w >> 6;
+#pragma unroll
+    for (int e = 0; e <= DK; ++e) x[e] = h ? xk[1][e] : xk[0][e];
+    uint8_t* hi = slot + (tq / 8) * 2048 + (tq % 8) * 16;
+    if (S::rows(f) < 128)   // a last block of more than 64 rows: over the 4 threads of a token
+      build_phi32_last<DK, NT>(0, S::GL, qq, 4, x, hi, hi + 16384, 127);
+    else
+      build_phi32<DK, NT>(f, qq, x, hi, hi + 16384, 127);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // span_state_tc32: the state sum of one span -> scratch (fp32 inputs).
 // ---------------------------------------------------------------------------
@@ -433,15 +488,10 @@ span_state_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_
         ++req;
       }
       for (int f = 0; f < NB && ok; ++f)
-        for (int h = 0; h < 2; ++h, pos.next()) {
+        for (int h = 0; h < S::upd_tiles(f); ++h, pos.next()) {
           if (!(ok = ring.take(B, pos.s))) break;
-          const uint32_t a = tc::smem_u32(smem + L.slot(pos.s));
-          const uint64_t dAh = tc::sdesc(a, 2048, 128), dAl = tc::sdesc(a + 16384, 2048, 128);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma3(tm + f * nm, dAh + (uint64_t)(k * 256), dAl + (uint64_t)(k * 256),
-                 dVh + (uint64_t)(64 * h + k * 16), dVl + (uint64_t)(64 * h + k * 16), id_up,
-                 (c > 0 || h > 0 || k > 0) ? 1u : 0u);
+          tc32_issue_update(tm + f * nm, tc::smem_u32(smem + L.slot(pos.s)), dVh, dVl, id_up,
+                            S::upd_tiles(f) == 1, S::GL, h, c > 0 || h > 0);
           tc::mma_commit_elect(B.sempty(pos.s));
         }
       if (!ok) break;
@@ -453,8 +503,7 @@ span_state_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_
     tc::mbar_wait(B.drain(), 0, TC_WAIT_NS);
     for (; got < req; ++got) tc::mbar_wait(X.stg_full(), got & 1u, TC_WAIT_NS);
   } else {
-    const int tq = tid & 63, qq = tid >> 6;   // update use: token 64h + tq, features 32qq..
-    const int urow = (tq / 8) * 2048 + (tq % 8) * 16;
+    const int tq = tid & 63;   // update inputs: tokens tq and 64 + tq
     TcWorkerRing ring;
     for (int c = 0; c < u.n_chunks; ++c) {
       const long long t0 = u.t_begin + (long long)c * TC_C;
@@ -478,16 +527,9 @@ span_state_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_
       tc_warp_arrive(X.tiles(), lane);
       bool ok = true;
       for (int f = 0; f < NB && ok; ++f)
-        for (int h = 0; h < 2; ++h, pos.next()) {
+        for (int h = 0; h < S::upd_tiles(f); ++h, pos.next()) {
           if (!(ok = ring.acquire(B, pos.s))) break;
-          float x[DK + 1];
-#pragma unroll
-          for (int e = 0; e <= DK; ++e) x[e] = h ? xk[1][e] : xk[0][e];
-          uint8_t* hi = smem + L.slot(pos.s) + urow;
-          if (S::rows(f) < 128)   // the last block's few rows, over the 4 threads of a token
-            build_phi32_last<DK, NT>(0, S::LAST_ROWS / 8, qq, 4, x, hi, hi + 16384, 127);
-          else
-            build_phi32<DK, NT>(f, qq, x, hi, hi + 16384, 127);
+          tc32_build_update<DK, NT>(smem + L.slot(pos.s), f, h, tid, xk);
           ring.release(B, pos.s, lane);
         }
       if (!ok) break;
@@ -693,14 +735,10 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
       // S_f += phi(K_f)^T [V, 1], 64 tokens at a time
       if (need_update) {
         for (int f = 0; f < NB && ok; ++f)
-          for (int h = 0; h < 2; ++h, pos.next()) {
+          for (int h = 0; h < S::upd_tiles(f); ++h, pos.next()) {
             if (!(ok = ring.take(B, pos.s))) break;
-            const uint32_t a = tc::smem_u32(smem + L.slot(pos.s));
-            const uint64_t dAh = tc::sdesc(a, 2048, 128), dAl = tc::sdesc(a + 16384, 2048, 128);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma3(tm + f * nm, dAh + (uint64_t)(k * 256), dAl + (uint64_t)(k * 256),
-                   dVh + (uint64_t)(64 * h + 16 * k), dVl + (uint64_t)(64 * h + 16 * k), id_up, 1u);
+            tc32_issue_update(tm + f * nm, tc::smem_u32(smem + L.slot(pos.s)), dVh, dVl, id_up,
+                              S::upd_tiles(f) == 1, S::GL, h, true);
             tc::mma_commit_elect(B.sempty(pos.s));
           }
         if (!ok) break;
@@ -855,7 +893,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
         xk[h][DK] = (64 * h + tq < valid) ? 1.0f : 0.0f;
       }
       const int n_ro = [] { int n = 0; for (int f = 0; f < NB; ++f) n += S::halves(f); return n; }();
-      const int nuse = n_ro + (need_update ? 2 * NB : 0);
+      const int nuse = n_ro + (need_update ? S::n_upd() : 0);
       int f = 0, h = 0;
       bool ok = true;
       for (int k = 0; k < nuse; ++k) {
@@ -870,21 +908,23 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
         TSA_TRACE_EVENT(20, k);
         if (!(ok = upd ? ring.acquire(B, pos.s) : ro.acquire(B, X.roempty(ro.s)))) break;
         TSA_TRACE_EVENT(21, k);
-        float x[DK + 1];
-        if (upd) {
-#pragma unroll
-          for (int e = 0; e <= DK; ++e) x[e] = h ? xk[1][e] : xk[0][e];
-        } else {
-          tc32_load_x<DK>(smem + L.qs, t, x);
-          x[DK] = 1.0f;
-        }
         if (upd && S::rows(f) < 128) {
-          // the last block's few rows, spread over the 4 threads of a token
-          uint8_t* hi = smem + L.slot(pos.s) + urow;
-          build_phi32_last<DK, NT>(0, S::LAST_ROWS / 8, qq, 4, x, hi, hi + 16384, 127);
+          // the last block: its compact tile (or, above 64 rows, its rows
+          // spread over the 4 threads of a token)
+          tc32_build_update<DK, NT>(smem + L.slot(pos.s), f, h, bt, xk);
         } else if (32 * g < S::rows(f)) {
+          float x[DK + 1];
+          if (upd) {
+#pragma unroll
+            for (int e = 0; e <= DK; ++e) x[e] = h ? xk[1][e] : xk[0][e];
+          } else {
+            tc32_load_x<DK>(smem + L.qs, t, x);
+            x[DK] = 1.0f;
+          }
           uint32_t hv[16], lv[16];
+          TSA_TRACE_EVENT(26, k);
           build_phi32_regs<DK, NT>(f, g, x, hv, lv);
+          TSA_TRACE_EVENT(27, k);
           if (upd) {
             uint8_t* hi = smem + L.slot(pos.s) + urow;
 #pragma unroll
@@ -907,9 +947,10 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
         } else {
           ro.release_tmem(X.rofull(ro.s), lane);
         }
+        TSA_TRACE_EVENT(28, k);
         // next (f, h): readouts walk the block's 64-feature halves, updates
-        // its two 64-token halves
-        if (++h == (upd ? 2 : S::halves(f))) { h = 0; ++f; }
+        // its update tiles
+        if (++h == (upd ? S::upd_tiles(f) : S::halves(f))) { h = 0; ++f; }
       }
       if (!ok) break;
       if (!need_update) tc_warp_arrive(X.stg_free(), lane);
