@@ -73,6 +73,11 @@ constexpr FeatTab<DK, NT> make_feat_tab() {
 // The table of each (d_k, n) lives in constant memory, built at compile time.
 template <int DK, int NT>
 __constant__ FeatTab<DK, NT> c_feat = make_feat_tab<DK, NT>();
+// The same table in global memory, for reads where every thread of a warp
+// takes a different entry (coalesced through L1 rather than serialised by
+// the constant cache).
+template <int DK, int NT>
+__device__ const FeatTab<DK, NT> g_feat = make_feat_tab<DK, NT>();
 
 // Truncated exponential T_n(x) = sum_{m<n} x^m/m!, evaluated in Horner form
 // 1 + x(1 + x/2(1 + x/3(...))).

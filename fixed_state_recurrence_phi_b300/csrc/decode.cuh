@@ -25,15 +25,22 @@ struct DecodeParams {
 // One CTA (256 threads) per head. The S part [DPAD][DV] is walked as float4
 // column groups: thread t owns column group cg = t % (DV/4) and rows
 // r0 + RP*it, so its partial sums always belong to the same 4 columns.
+// Small states (up to 160 x 64): 8 CTAs per SM (32 registers a thread), so
+// that a batch of 1024 heads is one wave on 148 SMs; larger states keep the
+// registers their longer walk needs.
+__host__ __device__ constexpr int decode_min_ctas(int dk, int nt, int dv) {
+  return round_up(feat_dim(dk, nt), 4) * dv <= 160 * 64 ? 8 : 1;
+}
 template <typename T, int DK, int NT, int DV>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, decode_min_ctas(DK, NT, DV))
 decode_kernel(DecodeParams p) {
   constexpr int D = feat_dim(DK, NT);
   constexpr int DPAD = round_up(D, 4);
   constexpr int CG = DV / 4;          // float4 column groups per row
   constexpr int RP = 256 / CG;        // rows per pass
   constexpr int NIT = (DPAD + RP - 1) / RP;
-  constexpr int UNR = NIT < 12 ? NIT : 8;
+  constexpr int U0 = NIT < 4 ? NIT : 4;          // rows requested at entry
+  constexpr int UNR = (NIT - U0) < 8 ? ((NIT - U0) > 0 ? NIT - U0 : 1) : 8;   // then per batch
   constexpr int NW = 8;
   static_assert(256 % CG == 0, "DV/4 must divide 256");
 
@@ -52,6 +59,18 @@ decode_kernel(DecodeParams p) {
   const T* kg = static_cast<const T*>(p.k) + (size_t)head * DK;
   const T* vg = static_cast<const T*>(p.v) + (size_t)head * DV;
   float* st = p.states + (size_t)head * DPAD * (DV + 1);
+  const int cg = tid % CG, r0 = tid / CG;
+  float4* S4 = reinterpret_cast<float4*>(st);
+
+  // The first U0 state rows of this thread are requested before anything
+  // else: they do not depend on the feature maps, so the state stream starts
+  // at once and the feature maps are built while it is in flight.
+  float4 s0[U0];
+#pragma unroll
+  for (int u = 0; u < U0; ++u) {
+    const int a = r0 + RP * u;
+    if (u < NIT && a < DPAD) s0[u] = S4[(size_t)a * CG + cg];
+  }
 
   if (tid < DK) { xq[tid] = Elem<T>::load1(qg + tid); xk[tid] = Elem<T>::load1(kg + tid); }
   if (tid == 0) { xq[DK] = 1.0f; xk[DK] = 1.0f; }
@@ -60,9 +79,9 @@ decode_kernel(DecodeParams p) {
   for (int a = tid; a < DPAD; a += 256) {
     float fq = 0.f, fk = 0.f;
     if (a < D) {
-      const uint32_t cd = c_feat<DK, NT>.code[a];
+      const uint32_t cd = __ldg(&g_feat<DK, NT>.code[a]);
       const int i = cd & 255, j = (cd >> 8) & 255, l = (cd >> 16) & 255;
-      const float w = c_feat<DK, NT>.w[a];
+      const float w = __ldg(&g_feat<DK, NT>.w[a]);
       fq = w * xq[i] * xq[j] * xq[l];
       fk = w * xk[i] * xk[j] * xk[l];
     }
@@ -70,11 +89,23 @@ decode_kernel(DecodeParams p) {
   }
   __syncthreads();
 
-  const int cg = tid % CG, r0 = tid / CG;
   const float4 v4 = *reinterpret_cast<const float4*>(vv + cg * 4);
   float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
-  float4* S4 = reinterpret_cast<float4*>(st);
-  for (int it0 = 0; it0 < NIT; it0 += UNR) {
+  // S += phi(k) [v]^T row by row, partial phi(q)^T S on the way
+  auto row = [&](int a, float4 x) {
+    const float fk = phk[a], fq = phq[a];
+    x.x = fmaf(fk, v4.x, x.x); x.y = fmaf(fk, v4.y, x.y);
+    x.z = fmaf(fk, v4.z, x.z); x.w = fmaf(fk, v4.w, x.w);
+    part.x = fmaf(fq, x.x, part.x); part.y = fmaf(fq, x.y, part.y);
+    part.z = fmaf(fq, x.z, part.z); part.w = fmaf(fq, x.w, part.w);
+    S4[(size_t)a * CG + cg] = x;
+  };
+#pragma unroll
+  for (int u = 0; u < U0; ++u) {
+    const int a = r0 + RP * u;
+    if (u < NIT && a < DPAD) row(a, s0[u]);
+  }
+  for (int it0 = U0; it0 < NIT; it0 += UNR) {
     float4 s[UNR];
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
@@ -84,15 +115,7 @@ decode_kernel(DecodeParams p) {
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
       const int a = r0 + RP * (it0 + u);
-      if (it0 + u < NIT && a < DPAD) {
-        const float fk = phk[a], fq = phq[a];
-        float4 x = s[u];
-        x.x = fmaf(fk, v4.x, x.x); x.y = fmaf(fk, v4.y, x.y);
-        x.z = fmaf(fk, v4.z, x.z); x.w = fmaf(fk, v4.w, x.w);
-        part.x = fmaf(fq, x.x, part.x); part.y = fmaf(fq, x.y, part.y);
-        part.z = fmaf(fq, x.z, part.z); part.w = fmaf(fq, x.w, part.w);
-        S4[(size_t)a * CG + cg] = x;
-      }
+      if (it0 + u < NIT && a < DPAD) row(a, s[u]);
     }
   }
   // normaliser column z (DPAD floats after the S part)
