@@ -69,12 +69,24 @@ def test_ragged_lengths(G, N):
 
 @pytest.mark.parametrize("d,dv,n,dtype", [
     (16, 64, 1, "f32"), (16, 64, 2, "f32"), (16, 64, 4, "f32"), (32, 128, 3, "f32"),
-    (32, 32, 3, "f32"), (16, 32, 4, "f32"), (16, 128, 3, "bf16"), (16, 64, 4, "bf16"),
+    (32, 32, 3, "f32"), (16, 32, 4, "f32"), (16, 32, 3, "f32"), (32, 32, 2, "f32"),
+    (32, 64, 2, "f32"), (16, 128, 3, "bf16"), (16, 64, 4, "bf16"),
     (32, 128, 3, "bf16"), (32, 64, 2, "bf16"), (16, 64, 3, "bf16"),
 ])
 def test_shapes(G, d, dv, n, dtype):
     cfg = G.T.Config(1, 2, d, dv, n, dtype)
     _all_heads(G, cfg, 333, seed=7 + d + dv + n)
+
+
+@pytest.mark.parametrize("d,dv,n", [(16, 32, 3), (32, 32, 2), (32, 64, 2), (16, 64, 2)])
+def test_fp32_tensor_core_shapes_multi_span(G, d, dv, n):
+    """fp32 shapes on the tensor cores (16-column output halves, a 48-row
+    last feature block, direct output stores) cut into several spans: the span
+    pass, the scan and the bulk-copied span prefixes at other state sizes."""
+    cfg = G.T.Config(1, 2, d, dv, n, "f32")
+    plan = G.T.prefill_plan(cfg, 3000)
+    assert plan["path"] == G.T.TSA_PATH_TC_F32 and plan["n_spans"] > 1, plan
+    _all_heads(G, cfg, 3000, seed=50 + d + dv + n)
 
 
 def test_n1_is_running_mean(G):
