@@ -95,71 +95,34 @@ __device__ __forceinline__ uint4 feat8(const float (&x)[DK + 1]) {
 }
 
 // Write the G groups of 8 features starting at A0 (a multiple of 8) for one
-// token into the feature tile of every CTA of the cluster: `local` points at
-// the token's row in this CTA's tile (8-feature groups 128 bytes apart), and
-// `remote[r]` is the shared::cluster address of the same row in CTA r (used for
-// r != R, this CTA's rank).
-template <int DK, int NT, int NS, int R, int A0, int G>
+// token into its row of the feature tile: `row` points at the token's row,
+// 8-feature groups 128 bytes apart.
+template <int DK, int NT, int A0, int G>
 struct PhiGroups {
-  static __device__ __forceinline__ void run(const float (&x)[DK + 1], uint8_t* local, const uint32_t* remote) {
-    PhiGroups<DK, NT, NS, R, A0, G - 1>::run(x, local, remote);
+  static __device__ __forceinline__ void run(const float (&x)[DK + 1], uint8_t* row) {
+    PhiGroups<DK, NT, A0, G - 1>::run(x, row);
     constexpr int a = A0 + 8 * (G - 1);
     constexpr int grp = (a % 128) / 8;
-    const uint4 v = feat8<DK, NT, a>(x);
-    *reinterpret_cast<uint4*>(local + grp * 128) = v;
-#pragma unroll
-    for (int r = 0; r < NS; ++r)
-      if (r != R) tc::st_cluster_v4(remote[r] + grp * 128, v);
+    *reinterpret_cast<uint4*>(row + grp * 128) = feat8<DK, NT, a>(x);
   }
 };
-template <int DK, int NT, int NS, int R, int A0>
-struct PhiGroups<DK, NT, NS, R, A0, 0> {
-  static __device__ __forceinline__ void run(const float (&)[DK + 1], uint8_t*, const uint32_t*) {}
+template <int DK, int NT, int A0>
+struct PhiGroups<DK, NT, A0, 0> {
+  static __device__ __forceinline__ void run(const float (&)[DK + 1], uint8_t*) {}
 };
 
-// Groups of 8 (of the 16 in a 128-wide tile) that CTA r of a cluster of NS
-// builds: [tc_group0(NS, r), tc_group0(NS, r + 1)); each half of the CTA's
-// workers takes one part of that range.
-__host__ __device__ constexpr int tc_group0(int ns, int r) { return (16 * r + ns - 1) / ns; }
-__host__ __device__ constexpr int tc_group_mid(int ns, int r) {
-  return tc_group0(ns, r) + (tc_group0(ns, r + 1) - tc_group0(ns, r) + 1) / 2;
-}
-
-// This CTA's share of feature block f for one token (runtime f and half pick a
-// compile-time instantiation).
-template <int DK, int NT, int NS, int R, int F = 0>
-__device__ __forceinline__ void build_phi_part(int f, int half, const float (&x)[DK + 1], uint8_t* local,
-                                               const uint32_t* remote) {
+// Half `half` (groups 8*half .. 8*half + 7) of feature block f for one token;
+// the runtime block index picks a compile-time instantiation (one call site
+// per kernel keeps one copy of the feature code).
+template <int DK, int NT, int F = 0>
+__device__ __forceinline__ void build_phi_half(int f, int half, const float (&x)[DK + 1], uint8_t* row) {
   if constexpr (F < FeatConst<DK, NT>::NB) {
     if (f == F) {
-      constexpr int g0 = tc_group0(NS, R), gm = tc_group_mid(NS, R), g1 = tc_group0(NS, R + 1);
-      if (half == 0) PhiGroups<DK, NT, NS, R, F * 128 + 8 * g0, gm - g0>::run(x, local, remote);
-      else PhiGroups<DK, NT, NS, R, F * 128 + 8 * gm, g1 - gm>::run(x, local, remote);
+      if (half == 0) PhiGroups<DK, NT, F * 128, 8>::run(x, row);
+      else PhiGroups<DK, NT, F * 128 + 64, 8>::run(x, row);
       return;
     }
-    build_phi_part<DK, NT, NS, R, F + 1>(f, half, x, local, remote);
-  }
-}
-
-// Runtime rank -> instantiation.
-template <int DK, int NT, int NS>
-__device__ __forceinline__ void build_phi_rank(int rank, int f, int half, const float (&x)[DK + 1],
-                                               uint8_t* local, const uint32_t* remote) {
-  if constexpr (NS == 1) {
-    build_phi_part<DK, NT, 1, 0>(f, half, x, local, remote);
-  } else if constexpr (NS == 2) {
-    if (rank == 0) build_phi_part<DK, NT, 2, 0>(f, half, x, local, remote);
-    else build_phi_part<DK, NT, 2, 1>(f, half, x, local, remote);
-  } else if constexpr (NS == 3) {
-    if (rank == 0) build_phi_part<DK, NT, 3, 0>(f, half, x, local, remote);
-    else if (rank == 1) build_phi_part<DK, NT, 3, 1>(f, half, x, local, remote);
-    else build_phi_part<DK, NT, 3, 2>(f, half, x, local, remote);
-  } else {
-    static_assert(NS >= 1 && NS <= 4, "cluster size");
-    if (rank == 0) build_phi_part<DK, NT, 4, 0>(f, half, x, local, remote);
-    else if (rank == 1) build_phi_part<DK, NT, 4, 1>(f, half, x, local, remote);
-    else if (rank == 2) build_phi_part<DK, NT, 4, 2>(f, half, x, local, remote);
-    else build_phi_part<DK, NT, 4, 3>(f, half, x, local, remote);
+    build_phi_half<DK, NT, F + 1>(f, half, x, row);
   }
 }
 

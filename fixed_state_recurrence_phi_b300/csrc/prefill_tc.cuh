@@ -371,7 +371,7 @@ span_state_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       bool ok = true;
       for (int f = 0; f < NB; ++f, pos.next()) {
         if (!(ok = ring.acquire(B, pos.s))) break;
-        build_phi_rank<DK, NT, 1>(0, f, half, xk, smem + L.slot(pos.s) + prow, nullptr);
+        build_phi_half<DK, NT>(f, half, xk, smem + L.slot(pos.s) + prow);
         ring.release(B, pos.s, lane);
       }
       if (!ok) break;
@@ -667,7 +667,7 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
         float x[DK + 1];
 #pragma unroll
         for (int e = 0; e <= DK; ++e) x[e] = upd ? xk[e] : xq[e];
-        build_phi_rank<DK, NT, 1>(0, f, half, x, smem + L.slot(pos.s) + prow, nullptr);
+        build_phi_half<DK, NT>(f, half, x, smem + L.slot(pos.s) + prow);
         ring.release(B, pos.s, lane);
         pos.next();
       }
