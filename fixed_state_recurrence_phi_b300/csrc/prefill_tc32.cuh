@@ -12,18 +12,27 @@
 // rounding of lo are ~2^-16 relative.
 //
 // Per CTA (one head, one span, all value columns plus the normaliser group):
-// fp32 q, k, v tiles of a chunk land by TMA in a staging area; the worker
-// warps turn them into hi/lo bf16 operand tiles (q, k for Q K^T; v for
-// P [V,1] and the update) and keep each thread's q and k inputs in registers
-// for the feature map. Feature and P tiles travel through a ring of 32 KB
-// slots, each holding the hi and lo halves of a 128 x 64 bf16 tile:
-//   P use     : 128 query rows x 64 keys           (K-major A)
-//   readout   : 128 tokens x 64 features of a block (K-major A), K = 64 (or
-//               the block's last rows)
-//   update    : 64 tokens x 128 features of a block (MN-major A), K = 64
-// The bf16 hi/lo copies of the state hold only the rows the readout reads
-// (the last feature block is cut to a multiple of 16 rows). Warp roles and
-// bounded waits as in prefill_tc.cuh.
+// fp32 q, k, v tiles of a chunk land by TMA in a staging area as
+// [col/4][token][4] tiles; they are split into hi/lo bf16 operand tiles (q, k
+// for Q K^T; v for P [V,1] and the update). The state lives in TMEM; its
+// hi/lo copies in shared memory (only the rows the readout reads: the last
+// feature block is cut to a multiple of 16 rows) are the readout's B operand.
+//
+// The output pass runs three warp roles (span_output_tc32_kernel):
+//   TMEM warps (0-7)     operand and state conversions; P = mask(T_n(A))
+//                        written into TMEM over the scores (the P [V,1] MMAs
+//                        read A from TMEM); the output, staged per warp and
+//                        stored by TMA
+//   builder warps (8-15) readout feature tiles (128 tokens x 64 features of
+//                        a block) into a two-buffer TMEM area (the readout
+//                        MMAs read A from TMEM); update feature tiles (64
+//                        tokens x 128 features of a block, or the last
+//                        block's few rows for all 128 tokens) through a ring
+//                        of 32 KB shared-memory slots (hi and lo halves)
+//   issuer warp (16)     TMA loads and MMAs
+// The span pass (span_state_tc32_kernel) has 8 workers (v conversion, update
+// tiles) and the issuer. All hand-offs are mbarriers with bounded waits, as
+// in prefill_tc.cuh.
 #pragma once
 #include <cuda.h>
 #include "common.cuh"
@@ -79,16 +88,21 @@ struct Tc32Smem {
   __host__ __device__ size_t slot(int r) const { return ring0 + (size_t)r * 32768; }
 };
 
-// mbarriers of the fp32 kernels (shared memory, in this order) and counts:
-//   sfull      staging tiles (fp32 q, k, v) of the chunk landed   (1 + tx)
-//   sfree      workers have consumed the staging                 (8)
-//   tiles      workers wrote the hi/lo operand tiles              (8)
-//   ostored    output stores have read their staging              (8)
-//   pready     P written into TMEM over the scores A              (8)
-//   stload, rofull[2] / roempty[2]  initial state copy, readout tiles in
-//              TMEM (after the TMEM allocation word and the abort flag)
-//   ring sfull[3] / sempty[3], qk, odone, ofree, conv, chunk, drain as in
-//   prefill_tc.cuh
+// mbarriers of the fp32 kernels (shared memory) and arrival counts. Slots
+// 0-15 are those of prefill_tc.cuh's TcBars (ring sfull[3] / sempty[3], qk,
+// odone, conv, chunk, drain keep their meaning); the slots of TcBars that
+// these kernels do not use carry their own barriers:
+//   0  stg_full   staging tiles (fp32 q, k, v) of the chunk landed   (1 + tx)
+//   1  stg_free   the staging is read (workers; output pass: TMEM and
+//                 builder warps)                                  (8 or 16)
+//   2  tiles      hi/lo q, k operand tiles written                     (8)
+//   3  ostored    output stores have read their staging               (8)
+//   12 pready     P written into TMEM over the scores A                (8)
+//   16 (the TMEM allocation word and the abort flag)
+//   17 stload     the span's initial state copied into the ring area (1 + tx)
+//   18-19 rofull  readout feature tile r of the TMEM buffers written    (8)
+//   20-21 roempty ... and read by its MMAs (the span pass: vfree, its v
+//                 tile buffer r free again)                            (1)
 struct Tc32Bars {
   uint64_t* b;
   __device__ uint64_t* stg_full() const { return b + 0; }
