@@ -63,6 +63,7 @@ struct TcParams {
   int* err;          // device error word (set on a timed-out wait)
   long long N;
   int heads, dv, n_spans, chunks_per_span, accumulate, n_slices, nmax, ring;
+  int span_layout;   // fp32 span pass: its own shared-memory layout (Tc32Smem)
   int slice_c0[TC_MAX_SLICES];
   int slice_w[TC_MAX_SLICES];
 };

@@ -22,6 +22,12 @@ size_t smem_tc32(int dv, int ring) {
   using S = Tc32Shape<DK, NT>;
   return Tc32Smem(DK, dv, dv + 16, S::ROWS, ring).total;
 }
+// the span pass's own layout (no q staging, q/k tiles or state copies)
+template <int DK, int NT>
+size_t smem_tc32_span(int dv, int ring) {
+  using S = Tc32Shape<DK, NT>;
+  return Tc32Smem(DK, dv, dv + 16, S::ROWS, ring, true).total;
+}
 
 size_t smem_for(int dk, int nt, int dv, int ring) {
 #define TSA_T32_CASE(DK, NT) \
@@ -90,9 +96,18 @@ tsa_status launch32(const tsa_plan& pl, const PrefillParams& pp, cudaStream_t s)
   const unsigned grid = (unsigned)((long long)pp.heads * pl.n_spans);
   cudaError_t e;
   if (pl.n_spans > 1) {
-    e = set_smem_once((const void*)span_state_tc32_kernel<DK, NT>, smem);
+    // the span pass: its own layout (three ring slots where that fits), or
+    // the output pass's where its own does not fit
+    TcParams ps = p;
+    int smem_s = smem;
+    if (smem_tc32_span<DK, NT>(pp.dv, 2) <= kSmemLimit) {
+      ps.span_layout = 1;
+      ps.ring = (smem_tc32_span<DK, NT>(pp.dv, 3) <= kSmemLimit) ? 3 : 2;
+      smem_s = (int)smem_tc32_span<DK, NT>(pp.dv, ps.ring);
+    }
+    e = set_smem_once((const void*)span_state_tc32_kernel<DK, NT>, smem_s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_state_tc32)");
-    span_state_tc32_kernel<DK, NT><<<grid, TC_THREADS, smem, s>>>(p, mk, mv);
+    span_state_tc32_kernel<DK, NT><<<grid, TC_THREADS, smem_s, s>>>(ps, mk, mv);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch span_state_tc32");
     const int elems4 = (int)(round_up(S::D, 4) * (pp.dv + 1) / 4);

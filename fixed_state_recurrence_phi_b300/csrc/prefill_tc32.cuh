@@ -66,10 +66,26 @@ struct Tc32Shape {
 struct Tc32Smem {
   size_t qs, ks, vs, qh, ql, kh, kl, vh, vl, ring0, sh, sl, bar, total;
   int ring, nm;
-  __host__ __device__ Tc32Smem(int dk, int dv, int nm_, int rows, int ring_slots) {
+  // span_pass: the span pass's own layout, without the q staging, the q/k
+  // operand tiles and the state copies; sh and sl then hold its second v
+  // tile buffer (hi, lo), and the space saved can take a third ring slot.
+  __host__ __device__ Tc32Smem(int dk, int dv, int nm_, int rows, int ring_slots, bool span_pass = false) {
     ring = ring_slots;
     nm = nm_;
     const size_t x32 = (size_t)128 * dk * 4, x16 = (size_t)128 * dk * 2, v16 = (size_t)128 * nm_ * 2;
+    if (span_pass) {
+      qs = ks = 0;
+      vs = ks + x32;
+      qh = ql = kh = kl = vs;   // unused
+      vh = vs + (size_t)128 * dv * 4;
+      vl = vh + v16;
+      sh = vl + v16;
+      sl = sh + v16;
+      ring0 = sl + v16;
+      bar = ring0 + (size_t)ring * 32768;
+      total = bar + 256;
+      return;
+    }
     qs = 0;
     ks = qs + x32;
     vs = ks + x32;
@@ -449,14 +465,15 @@ span_state_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_
   extern __shared__ __align__(1024) uint8_t smem[];
   const TcUnit u = tc_unit(p);
   const int W = u.W, nm = u.nm;
-  const Tc32Smem L(DK, W, nm, S::ROWS, p.ring);
+  const Tc32Smem L(DK, W, nm, S::ROWS, p.ring, p.span_layout != 0);
   const Tc32Bars X{reinterpret_cast<uint64_t*>(smem + L.bar)};
   const TcBars B = X.ring_bars();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wq = warp & 3, half = (warp >> 2) & 1;
-  // v tiles in two buffers when the (here unused) state-copy area holds the
-  // second, so that the workers convert the next chunk's v while this
-  // chunk's MMAs still read the other
-  const bool v2 = S::ROWS >= 128;
+  // v tiles in two buffers when sh/sl hold the second (the span-pass layout,
+  // or the shared layout's state-copy area when it is large enough), so that
+  // the workers convert the next chunk's v while this chunk's MMAs still
+  // read the other
+  const bool v2 = p.span_layout != 0 || S::ROWS >= 128;
   auto vh_b = [&](int vb) { return vb ? smem + L.sh : smem + L.vh; };
   auto vl_b = [&](int vb) { return vb ? smem + L.sh + (size_t)128 * nm * 2 : smem + L.vl; };
 
