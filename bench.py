@@ -60,6 +60,29 @@ def _dist():
     return ws, rank, local
 
 
+def rank_seed(seed: int, rank: int) -> int:
+    """Weak scaling: every rank runs its own batch of the workload, drawn from
+    its own seed."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    """The slowest rank's time (all_reduce MAX over the process group; the
+    tensor lives on `device`: the GPU under NCCL, the CPU under gloo)."""
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(ws: int, tokens_per_rank: int, ms_max: float) -> float:
+    """Whole-job tokens/s: all ranks' tokens over the slowest rank's time."""
+    return ws * tokens_per_rank / (ms_max / 1e3)
+
+
 def _algorithmic_prefill_bytes(w) -> int:
     """q, k, v read + out written (element size of the dtype) + final states
     written (fp32, D*(d_v+1) per head)."""
@@ -260,17 +283,13 @@ def _run_ours(args, clk):
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x: float) -> float:
-        if ws == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+    def slowest(x: float) -> float:
+        return max_over_ranks(x, ws, dev)
 
     # ---------------- prefill workload (weak scaling: one batch per rank) ----
     w = PREFILL
     cfg = T.Config(w["B"], w["H"], w["d_k"], w["d_v"], w["n_terms"], w["dtype"])
-    q, k, v = torch_qkv(w["B"], w["H"], w["N"], w["d_k"], w["d_v"], w["dtype"], w["seed"] + 1000 * rank,
+    q, k, v = torch_qkv(w["B"], w["H"], w["N"], w["d_k"], w["d_v"], w["dtype"], rank_seed(w["seed"], rank),
                         0, dev)
     out = torch.empty((w["B"], w["H"], w["N"], w["d_v"]), dtype=q.dtype, device=dev)
     st = T.new_states(cfg, dev)
@@ -302,7 +321,7 @@ def _run_ours(args, clk):
               evs[i][1].record(stream)
           barrier()
           step_ms = [a.elapsed_time(b) for a, b in evs]
-          ms = max_over_ranks(statistics.mean(step_ms))
+          ms = slowest(statistics.mean(step_ms))
           # host time of one call (argument checks, plan, tensor maps, launches)
           hs = []
           for _ in range(5):
@@ -337,7 +356,7 @@ def _run_ours(args, clk):
                   gevs[i][1].record(stream)
               barrier()
               T.sync_status(stream)
-              ms = max_over_ranks(statistics.mean([a.elapsed_time(b) for a, b in gevs]))
+              ms = slowest(statistics.mean([a.elapsed_time(b) for a, b in gevs]))
               timing = "CUDA graph of one tsa_prefill call, replayed per step"
               del g
           except Exception as e:  # capture unsupported here: keep the per-call timing
@@ -365,7 +384,7 @@ def _run_ours(args, clk):
               a.record(stream); e2e_step(); b.record(stream)
               e_ms.append((a, b))
           barrier()
-          e2e_ms = max_over_ranks(statistics.mean([a.elapsed_time(b) for a, b in e_ms]))
+          e2e_ms = slowest(statistics.mean([a.elapsed_time(b) for a, b in e_ms]))
           h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
           d2h = oh.numel() * oh.element_size() + sh.numel() * sh.element_size()
           del qh, kh, vh, oh, sh, qd, kd, vd
@@ -379,7 +398,7 @@ def _run_ours(args, clk):
               tw["N"] = args.tc_n
           tcfg = T.Config(tw["B"], tw["H"], tw["d_k"], tw["d_v"], tw["n_terms"], tw["dtype"])
           tq, tk, tv = torch_qkv(tw["B"], tw["H"], tw["N"], tw["d_k"], tw["d_v"], tw["dtype"],
-                                 tw["seed"] + 1000 * rank, 0, dev)
+                                 rank_seed(tw["seed"], rank), 0, dev)
           tout = torch.empty((tw["B"], tw["H"], tw["N"], tw["d_v"]), dtype=tq.dtype, device=dev)
           tst = T.new_states(tcfg, dev)
           tplan = T.prefill_plan(tcfg, tw["N"])
@@ -396,7 +415,7 @@ def _run_ours(args, clk):
               b.record(stream)
               tev.append((a, b))
           barrier()
-          tms = max_over_ranks(statistics.mean([a.elapsed_time(b) for a, b in tev]))
+          tms = slowest(statistics.mean([a.elapsed_time(b) for a, b in tev]))
           T.sync_status(stream)
           fl = _algorithmic_prefill_flops(tw)
           pk_burst, pk_sust, pk_src = _bf16_peaks()
@@ -418,7 +437,7 @@ def _run_ours(args, clk):
           # ---------------- decode workload ----------------------------------
           dstates = []
           dq, dk, dv = torch_qkv(dw["B"], dw["H"], args.decode_prefill_n, dw["d_k"], dw["d_v"], dw["dtype"],
-                                 dw["seed"] + 1000 * rank, 0, dev)
+                                 rank_seed(dw["seed"], rank), 0, dev)
           dout = torch.empty((dw["B"], dw["H"], args.decode_prefill_n, dw["d_v"]), dtype=dq.dtype, device=dev)
           s0 = T.new_states(dcfg, dev)
           pa, pb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -432,7 +451,7 @@ def _run_ours(args, clk):
           for _ in range(DECODE_ROTATE):
               dstates.append(s0.clone())
           tq, tk, tv = torch_qkv(dw["B"], dw["H"], steps, dw["d_k"], dw["d_v"], dw["dtype"],
-                                 dw["seed"] + 1000 * rank, 1, dev)
+                                 rank_seed(dw["seed"], rank), 1, dev)
           tq = tq.permute(2, 0, 1, 3).contiguous(); tk = tk.permute(2, 0, 1, 3).contiguous()
           tv = tv.permute(2, 0, 1, 3).contiguous()
           touts = torch.empty((steps, dw["B"], dw["H"], dw["d_v"]), dtype=tq.dtype, device=dev)
@@ -468,7 +487,7 @@ def _run_ours(args, clk):
               g.replay()
           b.record(stream)
           barrier()
-          dec_us = max_over_ranks(a.elapsed_time(b) * 1e3 / (reps * steps))
+          dec_us = slowest(a.elapsed_time(b) * 1e3 / (reps * steps))
 
           # ---------------- merge -------------------------------------------
           m_ms = []
@@ -483,7 +502,7 @@ def _run_ours(args, clk):
 
     # ---------------- report -------------------------------------------------
     tokens = w["B"] * w["N"]
-    value = ws * tokens / (ms / 1e3) if do_pre else None
+    value = weak_scaling_value(ws, tokens, ms) if do_pre else None
     pre_bytes = _algorithmic_prefill_bytes(w)
     dec_bytes = _algorithmic_decode_bytes(dw)
     state_bytes_step = dw["B"] * dw["H"] * T.state_elems(dcfg) * 4 * 2
@@ -507,7 +526,7 @@ def _run_ours(args, clk):
                      "peak_source": f"{peak_src} (copy bandwidth)",
                      "algorithmic_bytes": pre_bytes,
                      "traffic": traffic.get("prefill")},
-        "e2e": {"value": ws * tokens / (e2e_ms / 1e3) if do_pre else None, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": weak_scaling_value(ws, tokens, e2e_ms) if do_pre else None, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * plan["launches"] if do_pre else 0,
         "decode": {"workload": dw["workload"], "us_per_step": dec_us, "us_per_step_eager": eager_us,
