@@ -652,39 +652,6 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
   const bool out_tma = tc32_out_tma(S::ROWS, nm, W);
 
   TSA_TRACE_EVENT(31, 0);
-  // initial state -> TMEM, then its hi/lo copies
-  if (tid < TC_WORKERS) {
-    tc::grid_dep_wait();
-    const float* src = st_src;
-    if (st_bulk) {
-      // a failed wait leaves the abort flag set: every later wait gives up
-      tc_wait_warp(B, X.stload(), 0u);
-      src = reinterpret_cast<const float*>(smem + L.ring0);
-    }
-    for (int f = 0; f < NB; ++f) {
-      const int a = f * 128 + i;
-      for (int g = half; g < nm / 16; g += 2) {
-        uint32_t r[16];
-#pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) {
-          const int cc = g * 16 + 4 * e4;
-          float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-          if (src != nullptr && a < D) {
-            if (cc < W) x = *reinterpret_cast<const float4*>(src + (size_t)a * p.dv + u.c0 + cc);
-            else if (cc == W) x.x = src[(size_t)DPAD * p.dv + a];
-          }
-          r[4 * e4] = __float_as_uint(x.x);
-          r[4 * e4 + 1] = __float_as_uint(x.y);
-          r[4 * e4 + 2] = __float_as_uint(x.z);
-          r[4 * e4 + 3] = __float_as_uint(x.w);
-        }
-        tc::tmem_st16(tm + lane_off + f * nm + g * 16, r);
-      }
-    }
-    tc::tmem_wait_st();
-    TSA_TRACE_EVENT(32, 0);
-    for (int f = 0; f < NB; ++f) tc32_convert_state<DK, NT>(smem + L.sh, smem + L.sl, tm, lane_off, nm, f, i, half);
-  }
   tc::fence_proxy_async();
   tc::fence_before_sync();
   __syncthreads();
@@ -722,7 +689,8 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
         mma3(tm + col_A, dQh + (uint64_t)(k * 256), dQl + (uint64_t)(k * 256), dKh + (uint64_t)(k * 256),
              dKl + (uint64_t)(k * 256), id_qk, k > 0 ? 1u : 0u);
       tc::mma_commit_elect(B.qk());
-      if (c > 0 && !(ok = tc_wait_warp(B, B.conv(), (c - 1) & 1u))) break;
+      // the state copies for this chunk's readouts (one conversion per chunk)
+      if (!(ok = tc_wait_warp(B, B.conv(), c & 1u))) break;
       TSA_TRACE_EVENT(2, c);
       // O = phi(Q_f) [S_f, z_f] summed over blocks, 64 features at a time,
       // the feature tiles read from TMEM
@@ -800,7 +768,44 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
       tc::fence_proxy_async();
       tc_warp_arrive(X.tiles(), lane);
       TSA_TRACE_EVENT(12, c);
-      if (c > 0) {
+      if (c == 0) {
+        // the span's initial state -> TMEM, then its hi/lo copies (here, not
+        // before the chunk loop, so that the builders, the q K^T and P of the
+        // first chunk overlap its arrival)
+        tc::grid_dep_wait();
+        const float* src = st_src;
+        if (st_bulk) {
+          if (!tc_wait_warp(B, X.stload(), 0u)) break;
+          src = reinterpret_cast<const float*>(smem + L.ring0);
+        }
+        for (int f = 0; f < NB; ++f) {
+          const int a = f * 128 + i;
+          for (int g = half; g < nm / 16; g += 2) {
+            uint32_t r[16];
+#pragma unroll
+            for (int e4 = 0; e4 < 4; ++e4) {
+              const int cc = g * 16 + 4 * e4;
+              float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+              if (src != nullptr && a < D) {
+                if (cc < W) x = *reinterpret_cast<const float4*>(src + (size_t)a * p.dv + u.c0 + cc);
+                else if (cc == W) x.x = src[(size_t)DPAD * p.dv + a];
+              }
+              r[4 * e4] = __float_as_uint(x.x);
+              r[4 * e4 + 1] = __float_as_uint(x.y);
+              r[4 * e4 + 2] = __float_as_uint(x.z);
+              r[4 * e4 + 3] = __float_as_uint(x.w);
+            }
+            tc::tmem_st16(tm + lane_off + f * nm + g * 16, r);
+          }
+        }
+        tc::tmem_wait_st();
+        TSA_TRACE_EVENT(32, 0);
+        tc::fence_after_sync();
+        for (int fb = 0; fb < NB; ++fb)
+          tc32_convert_state<DK, NT>(smem + L.sh, smem + L.sl, tm, lane_off, nm, fb, i, half);
+        tc::fence_proxy_async();
+        tc_warp_arrive(B.conv(), lane);
+      } else {
         // the previous chunk's state -> hi/lo copies for this chunk's readouts
         if (!tc_wait_warp(B, B.chunk(), (c - 1) & 1u)) break;
         if (out_tma) {
@@ -933,6 +938,9 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
           tc_warp_arrive(X.stg_free(), lane);
           f = 0;
           h = 0;
+          // the first update tile goes where the initial state was copied:
+          // wait until the TMEM warps have converted it
+          if (c == 0 && !(ok = tc_wait_warp(B, B.conv(), 0u))) break;
         }
         const bool upd = (k >= n_ro);
         const int g = upd ? qq : 2 * h + half;
