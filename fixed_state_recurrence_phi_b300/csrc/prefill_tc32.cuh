@@ -119,6 +119,7 @@ struct Tc32Smem {
 //   18-19 rofull  readout feature tile r of the TMEM buffers written    (8)
 //   20-21 roempty ... and read by its MMAs (the span pass: vfree, its v
 //                 tile buffer r free again)                            (1)
+//   22 (a flag: the initial-state copy has been issued)
 struct Tc32Bars {
   uint64_t* b;
   __device__ uint64_t* stg_full() const { return b + 0; }
@@ -131,6 +132,8 @@ struct Tc32Bars {
   __device__ uint64_t* pready() const { return b + 12; }
   // the span's initial state copied into the ring area            (1 + tx)
   __device__ uint64_t* stload() const { return b + 17; }
+  // set once that copy has been issued (the drain waits for it then)
+  __device__ volatile int* copy_issued() const { return reinterpret_cast<volatile int*>(b + 22); }
   // span pass: v tile buffer r free again (its MMAs are done)         (1)
   __device__ uint64_t* vfree(int r) const { return b + 20 + r; }
   // readout feature tile r of the TMEM double buffer written           (8)
@@ -147,6 +150,7 @@ struct Tc32Bars {
       tc::mbar_init(roempty(r), 1);
     }
     tc::mbar_init(stload(), 1);
+    *copy_issued() = 0;
     *TcBars{b}.abort_flag() = 0;
     tc::mbar_fence_init();
   }
@@ -621,18 +625,11 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
   if (warp == 0) tc::tmem_alloc(B.tmem_slot(), 512);
   if (tid == 0) X.init(16);
   if (warp == 0) {
-    // first loads at once, overlapping the set-up below: the chunk's inputs
-    // (ready before this call's first launch), then, once the grid this one
-    // depends on (the scan) is done, the span's initial state
+    // the first chunk's inputs at once (ready before this call's first
+    // launch), overlapping the set-up below
     __syncwarp();
     if (u.n_chunks > 0)
       tc32_issue_staging(L, smem, X.stg_full(), &tm_q, &tm_k, &tm_v, u.t_begin, u.head, u.c0, W, DK);
-    __syncwarp();
-    tc::grid_dep_wait();
-    if (st_bulk && tc::elect_one()) {
-      tc::mbar_arrive_expect_tx(X.stload(), st_bytes);
-      tc::bulk_load(smem + L.ring0, st_src, st_bytes, X.stload());
-    }
   }
   if (tid < TC_WORKERS) {
     tc_write_ones(smem + L.vh, W, tid);
@@ -748,7 +745,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
     tc::mma_commit_elect(B.drain());
     tc::mbar_wait(B.drain(), 0, TC_WAIT_NS);
     for (; got < req; ++got) tc::mbar_wait(X.stg_full(), got & 1u, TC_WAIT_NS);
-    if (st_bulk) tc::mbar_wait(X.stload(), 0, TC_WAIT_NS);   // the initial-state copy, too
+    if (*X.copy_issued()) tc::mbar_wait(X.stload(), 0, TC_WAIT_NS);   // the initial-state copy, too
   } else if (tid < TC_WORKERS) {
     // ---------------------------- TMEM warps -------------------------------
     // q, k, v and the state -> hi/lo operands, P, the output; thread = TMEM
@@ -772,9 +769,16 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
         // the span's initial state -> TMEM, then its hi/lo copies (here, not
         // before the chunk loop, so that the builders, the q K^T and P of the
         // first chunk overlap its arrival)
+        // the grid this one depends on (the scan) is done: its prefixes, or
+        // the caller's state, may be read; one bulk copy into the ring area
         tc::grid_dep_wait();
         const float* src = st_src;
         if (st_bulk) {
+          if (warp == 0 && tc::elect_one()) {
+            *X.copy_issued() = 1;
+            tc::mbar_arrive_expect_tx(X.stload(), st_bytes);
+            tc::bulk_load(smem + L.ring0, st_src, st_bytes, X.stload());
+          }
           if (!tc_wait_warp(B, X.stload(), 0u)) break;
           src = reinterpret_cast<const float*>(smem + L.ring0);
         }
