@@ -42,6 +42,8 @@ ORDER4 = dict(workload="order4_B4_H16_N32768", B=4, H=16, N=32768, d_k=16, d_v=6
 WIDE = dict(workload="wide_B2_H32_N65536", B=2, H=32, N=65536, d_k=32, d_v=128, n_terms=3, dtype="bf16", seed=5)
 L2_FLUSH_BYTES = 256 << 20
 DECODE_ROTATE = 8
+APPEND_LENGTHS = (16, 32, 64, 256)
+APPEND_REPS = 20
 
 
 def _peaks():
@@ -119,6 +121,16 @@ def _algorithmic_decode_bytes(w) -> int:
     heads = w["B"] * w["H"]
     D = sum(__import__("math").comb(w["d_k"] + m - 1, m) for m in range(w["n_terms"]))
     return heads * (2 * D * (w["d_v"] + 1) * 4 + (2 * w["d_k"] + 2 * w["d_v"]) * es)
+
+
+def _algorithmic_append_bytes(w, L: int) -> int:
+    """A short append of L tokens to every head: the state read + written once
+    (D*(d_v+1) fp32 per head; padding not counted) plus the segment's q, k, v in
+    and out."""
+    es = 4 if w["dtype"] == "f32" else 2
+    heads = w["B"] * w["H"]
+    D = sum(__import__("math").comb(w["d_k"] + m - 1, m) for m in range(w["n_terms"]))
+    return heads * (2 * D * (w["d_v"] + 1) * 4 + L * (2 * w["d_k"] + 2 * w["d_v"]) * es)
 
 
 class ClockSampler:
@@ -303,6 +315,7 @@ def _run_ours(args, clk):
     ms = ms_eager = e2e_ms = host_us = float("nan"); h2d = d2h = 0
     timing = "n/a"
     dec_us = eager_us = long_prefill_ms = merge_ms = float("nan")
+    append_lines = []
     steps, reps = 1024, 3
     dw = DECODE
     dcfg = T.Config(dw["B"], dw["H"], dw["d_k"], dw["d_v"], dw["n_terms"], dw["dtype"])
@@ -489,6 +502,50 @@ def _run_ours(args, clk):
           barrier()
           dec_us = slowest(a.elapsed_time(b) * 1e3 / (reps * steps))
 
+          # ---------------- short appends (prefill with ACCUMULATE) ---------
+          # L new tokens per head folded into the decode states: one
+          # tsa_prefill call continuing every head; a CUDA graph of one call
+          # per state set (rotated, > L2), replayed.
+          for L in APPEND_LENGTHS:
+              aq, ak, av = torch_qkv(dw["B"], dw["H"], L, dw["d_k"], dw["d_v"], dw["dtype"],
+                                     rank_seed(dw["seed"], rank), 2, dev)
+              ao = torch.empty((dw["B"], dw["H"], L, dw["d_v"]), dtype=aq.dtype, device=dev)
+              aplan = T.prefill_plan(dcfg, L)
+
+              def append_all(s):
+                  for st_i in dstates:
+                      T.prefill(dcfg, L, aq, ak, av, ao, st_i, accumulate=True, stream=s)
+
+              append_all(stream)
+              barrier()
+              gs = torch.cuda.Stream()
+              gs.wait_stream(stream)
+              g = torch.cuda.CUDAGraph()
+              with torch.cuda.stream(gs):
+                  with torch.cuda.graph(g, stream=gs):
+                      append_all(gs)
+              stream.wait_stream(gs)
+              g.replay(); barrier()
+              a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+              a.record(stream)
+              for _ in range(APPEND_REPS):
+                  g.replay()
+              b.record(stream)
+              barrier()
+              T.sync_status(stream)
+              a_us = slowest(a.elapsed_time(b) * 1e3 / (APPEND_REPS * len(dstates)))
+              abytes = _algorithmic_append_bytes(dw, L)
+              append_lines.append({
+                  "workload": f"append_B{dw['B']}_H{dw['H']}_L{L}", "L": L, "us_per_call": a_us,
+                  "tokens_per_s": ws * dw["B"] * L / (a_us / 1e6),
+                  "path": ["simt", "tc", "tc_f32"][aplan["path"]],
+                  "roofline": {"bound": "hbm", "achieved": abytes / (a_us / 1e6) / 1e9, "peak": hbm_peak,
+                               "unit": "GB/s", "frac": abytes / (a_us / 1e6) / 1e9 / hbm_peak,
+                               "algorithmic_bytes": abytes},
+                  "timing": f"CUDA graph of {len(dstates)} calls (one per state set) x {APPEND_REPS}",
+              })
+              del g, aq, ak, av, ao
+
           # ---------------- merge -------------------------------------------
           m_ms = []
           for i in range(10):
@@ -542,6 +599,7 @@ def _run_ours(args, clk):
                    "states_prefilled_with_N": args.decode_prefill_n,
                    "prefill_ms": long_prefill_ms},
         "prefill_tensor_core": tc_lines,
+        "append": append_lines,
         "merge": {"workload": dw["workload"], "ms": merge_ms,
                   "GBps": 3 * T.state_bytes(dcfg) / (merge_ms / 1e3) / 1e9},
         "clocks": clocks,

@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <climits>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -180,8 +181,29 @@ static tsa_status make_plan_tc(const tsa_config* c, long long N, int num_sms, co
   return TSA_OK;
 }
 
+// Segments up to this length go to the short-segment prefill when the library
+// chooses (chunk = 0); chunk = 16 asks for it at any length.
+static constexpr long long kShortAutoMaxN = 32;
+
 tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl) {
   memset(pl, 0, sizeof(*pl));
+  // Short segments: each head's state stays in shared memory for the whole
+  // segment (read once, written once), 16-token blocks on the CUDA cores.
+  if (short_supported(c->d_k, c->n_terms, c->d_v) &&
+      (c->chunk == 16 || (c->chunk == 0 && N <= kShortAutoMaxN))) {
+    const size_t smem = short_smem(c->d_k, c->n_terms, c->d_v);
+    pl->chunk = 16;
+    pl->slice_width = c->d_v;
+    pl->n_slices = 1;
+    pl->n_spans = 1;
+    pl->chunks_per_span = (int)std::max<long long>(1, std::min<long long>((N + 15) / 16, INT_MAX));
+    pl->smem_bytes = smem;
+    pl->ctas_per_sm = std::max(1, std::min(2, (int)(kSmemPerSm / (smem + 1024))));   // 2: registers
+    pl->scratch_bytes = 0;
+    pl->launches = 1;
+    pl->path = TSA_PATH_SHORT;
+    return TSA_OK;
+  }
   if (c->dtype == TSA_BF16 && tc_supported(c->d_k, c->n_terms)) {
     TcSlicing ts;
     if (tc_slicing(c->d_k, c->n_terms, c->d_v, &ts)) {
@@ -285,6 +307,7 @@ static tsa_status dispatch_prefill(const tsa_config* c, const tsa_plan& pl, Pref
 // translation units of the library).
 tsa_status launch_prefill(const tsa_config* c, const tsa_plan& pl, PrefillParams p,
                           cudaStream_t s) {
+  if (pl.path == TSA_PATH_SHORT) return launch_prefill_short(c, p, s);
   if (pl.path == TSA_PATH_TC) return launch_prefill_tc(c, pl, p, s);
   if (pl.path == TSA_PATH_TC_F32) return launch_prefill_tc32(c, pl, p, s);
   return (c->dtype == TSA_F32) ? dispatch_prefill<float>(c, pl, p, s)

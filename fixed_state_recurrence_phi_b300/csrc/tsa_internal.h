@@ -31,4 +31,8 @@ bool tc32_fits(int dk, int nt, int dv);
 size_t tc32_smem(int dk, int nt, int dv);
 tsa_status launch_prefill_tc32(const tsa_config* c, const tsa_plan& pl, const PrefillParams& p, cudaStream_t s);
 tsa_status take_device_error();
+// Short-segment prefill, state resident in shared memory (prefill_short.cu).
+bool short_supported(int dk, int nt, int dv);
+size_t short_smem(int dk, int nt, int dv);
+tsa_status launch_prefill_short(const tsa_config* c, const PrefillParams& p, cudaStream_t s);
 }  // namespace tsa

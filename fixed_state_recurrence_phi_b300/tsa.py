@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libtsa.so")
 TSA_OK, TSA_ERR_INVALID, TSA_ERR_UNSUPPORTED, TSA_ERR_CUDA, TSA_ERR_TIMEOUT = range(5)
 TSA_F32, TSA_BF16 = 0, 1
 TSA_PREFILL_ACCUMULATE = 1
-TSA_PATH_SIMT, TSA_PATH_TC, TSA_PATH_TC_F32 = 0, 1, 2
+TSA_PATH_SIMT, TSA_PATH_TC, TSA_PATH_TC_F32, TSA_PATH_SHORT = 0, 1, 2, 3
 
 # Every symbol include/tsa.h declares (checked by the CPU test suite).
 EXPORTS = (

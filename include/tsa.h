@@ -61,7 +61,7 @@ typedef struct {
   int d_v;          /* value width: 32, 64 or 128                             */
   int n_terms;      /* n Taylor terms, orders 0..n-1: 1..4 (feature dim <= 1024) */
   tsa_dtype dtype;  /* element type of q, k, v and out (states are always fp32) */
-  int chunk;        /* prefill chunk length; 0 = library's choice             */
+  int chunk;        /* prefill chunk length; 0 = library's choice (see tsa_plan) */
 } tsa_config;
 
 /* tsa_prefill flag: continue from the states already in `states` instead of
@@ -103,10 +103,17 @@ tsa_status tsa_feature_index(int d_k, int n_terms, int* idx, float* weight);
  * path: TSA_PATH_SIMT (fp32 FFMA on the CUDA cores), TSA_PATH_TC (bf16
  * inputs on the tcgen05 tensor cores, fp32 TMEM accumulators) or
  * TSA_PATH_TC_F32 (fp32 inputs on the tensor cores: every operand split into
- * bf16 hi + lo parts and every product taken as three MMAs). */
+ * bf16 hi + lo parts and every product taken as three MMAs) or
+ * TSA_PATH_SHORT (short segments, e.g. a few tokens appended with
+ * TSA_PREFILL_ACCUMULATE: one CTA per head keeps the head's state in shared
+ * memory for the whole segment, so the state is read and written once; fp32
+ * on the CUDA cores in blocks of chunk = 16 tokens). The library takes
+ * TSA_PATH_SHORT for N <= 32 where the state fits (d_k = 16 with n <= 3, or
+ * d_k = 32 with n <= 2); cfg->chunk = 16 asks for it at any N. */
 #define TSA_PATH_SIMT 0
 #define TSA_PATH_TC 1
 #define TSA_PATH_TC_F32 2
+#define TSA_PATH_SHORT 3
 typedef struct {
   int chunk;
   int slice_width;

@@ -85,6 +85,28 @@ def test_plan_covers_all_chunks(T):
     assert T.prefill_plan(T.Config(1, 8, 16, 64, 3), 8192, num_sms=148)["n_spans"] >= 8
 
 
+def test_plan_short_segments(T):
+    """Short segments go to the shared-memory-resident path where the state
+    fits; chunk = 16 asks for it at any length; chunk = 128 keeps the chunked
+    tensor-core path."""
+    for dt in ("f32", "bf16"):
+        for N in (1, 16, 32):
+            p = T.prefill_plan(T.Config(64, 16, 16, 64, 3, dt), N, num_sms=148)
+            assert p["path"] == T.TSA_PATH_SHORT and p["chunk"] == 16, (dt, N, p)
+            assert p["chunks_per_span"] == -(-N // 16) and p["launches"] == 1 and p["scratch_bytes"] == 0
+            assert p["ctas_per_sm"] >= 2
+        assert T.prefill_plan(T.Config(64, 16, 16, 64, 3, dt), 33, num_sms=148)["path"] != T.TSA_PATH_SHORT
+        assert T.prefill_plan(T.Config(1, 1, 16, 64, 3, dt, chunk=16), 5000,
+                              num_sms=148)["path"] == T.TSA_PATH_SHORT
+        assert T.prefill_plan(T.Config(64, 16, 16, 64, 3, dt, chunk=128), 8,
+                              num_sms=148)["path"] != T.TSA_PATH_SHORT
+    # states too large for shared memory keep the chunked paths
+    for (d, dv, n) in [(16, 64, 4), (32, 64, 3), (16, 128, 3)]:
+        assert T.prefill_plan(T.Config(4, 4, d, dv, n, "bf16"), 8, num_sms=148)["path"] != T.TSA_PATH_SHORT
+        with pytest.raises(T.TsaError):
+            T.prefill_plan(T.Config(4, 4, d, dv, n, "bf16", chunk=16), 8, num_sms=148)
+
+
 def test_validation_codes(T):
     """Invalid arguments are rejected on the host before any CUDA call."""
     ok = T.Config(1, 1, 16, 64, 3)

@@ -67,6 +67,42 @@ def test_ragged_lengths(G, N):
     _all_heads(G, cfg, N, seed=100 + N)
 
 
+@pytest.mark.parametrize("N", [1, 2, 31, 32])
+def test_ragged_lengths_tensor_core_chunk(G, N):
+    """Short sequences forced onto the 128-token tensor-core chunk (the
+    library's own choice there is the short-segment prefill)."""
+    cfg = G.T.Config(2, 3, 16, 64, 3, "f32", chunk=128)
+    assert G.T.prefill_plan(cfg, N)["path"] == G.T.TSA_PATH_TC_F32
+    _all_heads(G, cfg, N, seed=150 + N)
+
+
+@pytest.mark.parametrize("d,dv,n,dtype,N", [
+    (16, 64, 3, "f32", 1), (16, 64, 3, "f32", 17), (16, 64, 3, "f32", 32), (16, 64, 3, "f32", 64),
+    (16, 64, 3, "f32", 300),     # chunk = 16 asked for: 19 blocks, ragged tail
+    (16, 64, 3, "bf16", 40), (16, 32, 3, "f32", 33), (16, 128, 2, "f32", 50),
+    (16, 64, 1, "bf16", 20), (32, 128, 2, "f32", 31), (32, 32, 1, "bf16", 5),
+])
+def test_short_segment_shapes(G, d, dv, n, dtype, N):
+    """The short-segment prefill (head state in shared memory, 16-token
+    blocks): from zero, and continuing a 100-token prefix with ACCUMULATE."""
+    T, O = G.T, G.O
+    cfg = T.Config(2, 3, d, dv, n, dtype, chunk=16)
+    assert T.prefill_plan(cfg, N)["path"] == T.TSA_PATH_SHORT
+    _all_heads(G, cfg, N, seed=400 + N + d + dv + n)
+    pre = T.Config(2, 3, d, dv, n, dtype)
+    q, k, v = G.make_inputs(cfg, 100 + N, seed=500 + N)
+    sl = lambda x, a, b: x[:, :, a:b].contiguous()
+    _, st = G.gpu_prefill(pre, sl(q, 0, 100), sl(k, 0, 100), sl(v, 0, 100))
+    out, st = G.gpu_prefill(cfg, sl(q, 100, 100 + N), sl(k, 100, 100 + N), sl(v, 100, 100 + N),
+                            states=st, accumulate=True)
+    Sg, og = G.canonical(cfg, st), G.host(out)
+    qh, kh, vh = G.host(q), G.host(k), G.host(v)
+    for b in range(2):
+        for h in range(3):
+            o_r, S_r = O.prefill_recurrent(qh[b, h], kh[b, h], vh[b, h], n)
+            G.check_head(cfg, og[b, h], Sg[b, h], o_r[100:], S_r, G.TOL[dtype], f"append b={b} h={h}")
+
+
 @pytest.mark.parametrize("d,dv,n,dtype", [
     (16, 64, 1, "f32"), (16, 64, 2, "f32"), (16, 64, 4, "f32"), (32, 128, 3, "f32"),
     (32, 32, 3, "f32"), (16, 32, 4, "f32"), (16, 32, 3, "f32"), (32, 32, 2, "f32"),
@@ -120,6 +156,34 @@ def test_accumulate_continues_the_sequence(G):
     for h in range(2):
         o_r, S_r = O.prefill_recurrent(qh[0, h], kh[0, h], vh[0, h], 3)
         G.check_head(cfg, G.host(out2)[0, h], Sg[0, h], o_r[700:], S_r, 1e-4, "accumulate")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_short_appends_B64_H16(G, dtype):
+    """B=64 H=16 d16 dv64 n=3 (the decode workload's heads): states from a
+    300-token prefill, then segments of 1, 16, 64 and 200 tokens appended in
+    turn with ACCUMULATE (the launch configuration of the benchmark's short
+    appends); sampled heads checked segment by segment against the oracle
+    continuing from its own state."""
+    T = G.T
+    cfg = T.Config(64, 16, 16, 64, 3, dtype)
+    tol = G.TOL[dtype]
+    q, k, v = G.make_inputs(cfg, 300, seed=21)
+    _, st = G.gpu_prefill(cfg, q, k, v)
+    heads = G.sample_heads(64, 16, k=2, seed=21)
+    S_refs = {}
+    for (b, h) in heads:
+        _, S_refs[(b, h)] = G.oracle_prefill(G.host(q[b, h]), G.host(k[b, h]), G.host(v[b, h]), 3)
+    for phase, L in enumerate((1, 16, 64, 200), start=1):
+        aq, ak, av = G.make_inputs(cfg, L, seed=21, phase=phase)
+        out, st = G.gpu_prefill(cfg, aq, ak, av, states=st, accumulate=True)
+        Sg = G.canonical(cfg, st)
+        og = G.host(out)
+        for (b, h) in heads:
+            o_r, S_r = G.oracle_prefill(G.host(aq[b, h]), G.host(ak[b, h]), G.host(av[b, h]), 3,
+                                        S0=S_refs[(b, h)])
+            G.check_head(cfg, og[b, h], Sg[b, h], o_r, S_r, tol, f"L={L} head {(b, h)}")
+            S_refs[(b, h)] = S_r
 
 
 def test_merge_of_segments_equals_whole(G):

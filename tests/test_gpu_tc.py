@@ -52,7 +52,7 @@ def test_bf16_uses_tensor_core_path(G):
 
 @pytest.mark.parametrize("N", [1, 2, 127, 128, 129, 255, 256, 257, 1000])
 def test_tc_ragged_lengths(G, N):
-    cfg = G.T.Config(2, 3, 16, 64, 3, "bf16")
+    cfg = G.T.Config(2, 3, 16, 64, 3, "bf16", chunk=128)
     _check_all_heads(G, cfg, N, seed=200 + N)
 
 
