@@ -43,6 +43,8 @@ WIDE = dict(workload="wide_B2_H32_N65536", B=2, H=32, N=65536, d_k=32, d_v=128, 
 L2_FLUSH_BYTES = 256 << 20
 DECODE_ROTATE = 8
 APPEND_LENGTHS = (16, 32, 64, 256)
+# tsa_plan.path values (include/tsa.h)
+PATH_NAMES = ("simt", "tc", "tc_f32", "short")
 APPEND_REPS = 20
 
 
@@ -538,7 +540,7 @@ def _run_ours(args, clk):
               append_lines.append({
                   "workload": f"append_B{dw['B']}_H{dw['H']}_L{L}", "L": L, "us_per_call": a_us,
                   "tokens_per_s": ws * dw["B"] * L / (a_us / 1e6),
-                  "path": ["simt", "tc", "tc_f32"][aplan["path"]],
+                  "path": PATH_NAMES[aplan["path"]],
                   "roofline": {"bound": "hbm", "achieved": abytes / (a_us / 1e6) / 1e9, "peak": hbm_peak,
                                "unit": "GB/s", "frac": abytes / (a_us / 1e6) / 1e9 / hbm_peak,
                                "algorithmic_bytes": abytes},
@@ -574,7 +576,7 @@ def _run_ours(args, clk):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w["workload"], "B": w["B"], "H": w["H"], "N": w["N"], "d_k": w["d_k"],
                    "d_v": w["d_v"], "n_terms": w["n_terms"], "chunk": plan["chunk"],
-                   "n_spans": plan["n_spans"], "path": ["simt", "tc", "tc_f32"][plan["path"]],
+                   "n_spans": plan["n_spans"], "path": PATH_NAMES[plan["path"]],
                    "l2": "flushed between timed steps (256 MB write)", "timing": timing},
         "ms_per_step_eager": ms_eager,
         "host_us_per_call": host_us,
