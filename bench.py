@@ -45,6 +45,7 @@ DECODE_ROTATE = 8
 APPEND_LENGTHS = (16, 32, 64, 256)
 # tsa_plan.path values (include/tsa.h)
 PATH_NAMES = ("simt", "tc", "tc_f32", "short")
+ORDER_SWEEP = (1, 2, 3, 4)
 APPEND_REPS = 20
 
 
@@ -448,6 +449,49 @@ def _run_ours(args, clk):
           del tq, tk, tv, tout, tst
           torch.cuda.empty_cache()
 
+      order_lines = []
+      if args.only in ("all", "orders"):
+          # ---------------- order sweep on the prefill workload's shape -------
+          # state size and throughput per number of Taylor terms (the accuracy
+          # side of the sweep is a parity test against exact softmax)
+          for n in ORDER_SWEEP:
+              ocfg = T.Config(w["B"], w["H"], w["d_k"], w["d_v"], n, w["dtype"])
+              oplan = T.prefill_plan(ocfg, w["N"])
+              ost = T.new_states(ocfg, dev)
+              T.prefill(ocfg, w["N"], q, k, v, out, ost, stream=stream)
+              barrier()
+              og = torch.cuda.CUDAGraph()
+              ogs = torch.cuda.Stream()
+              ogs.wait_stream(stream)
+              with torch.cuda.stream(ogs):
+                  with torch.cuda.graph(og, stream=ogs):
+                      T.prefill(ocfg, w["N"], q, k, v, out, ost, stream=ogs)
+              stream.wait_stream(ogs)
+              for _ in range(3):
+                  flush.fill_(1.0)
+                  og.replay()
+              barrier()
+              oev = []
+              for i in range(max(3, args.steps // 2)):
+                  flush.fill_(float(i))
+                  a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                  a.record(stream)
+                  og.replay()
+                  b.record(stream)
+                  oev.append((a, b))
+              barrier()
+              T.sync_status(stream)
+              oms = slowest(statistics.mean([a.elapsed_time(b) for a, b in oev]))
+              del og
+              order_lines.append({
+                  "workload": w["workload"], "n_terms": n, "ms": oms,
+                  "tokens_per_s": ws * w["B"] * w["N"] / (oms / 1e3),
+                  "state_bytes_per_head": T.state_elems(ocfg) * 4,
+                  "path": PATH_NAMES[oplan["path"]],
+                  "timing": "CUDA graph of one tsa_prefill call, replayed per step, L2 flushed between steps",
+              })
+              del ost
+
       if do_dec:
           # ---------------- decode workload ----------------------------------
           dstates = []
@@ -602,6 +646,7 @@ def _run_ours(args, clk):
                    "prefill_ms": long_prefill_ms},
         "prefill_tensor_core": tc_lines,
         "append": append_lines,
+        "orders": order_lines,
         "merge": {"workload": dw["workload"], "ms": merge_ms,
                   "GBps": 3 * T.state_bytes(dcfg) / (merge_ms / 1e3) / 1e9},
         "clocks": clocks,
@@ -628,7 +673,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "order4", "wide"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "order4", "wide", "orders"], default="all",
                     help="run one part (profiling captures on small cases)")
     ap.add_argument("--tc-n", type=int, default=0,
                     help="sequence length of the order4/wide workloads (default: theirs)")

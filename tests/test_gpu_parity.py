@@ -186,6 +186,35 @@ def test_short_appends_B64_H16(G, dtype):
             S_refs[(b, h)] = S_r
 
 
+@pytest.mark.parametrize("d,dtype", [(16, "f32"), (32, "f32"), (16, "bf16")])
+def test_order_sweep_against_softmax(G, d, dtype):
+    """Accuracy against exact causal softmax as the number of Taylor terms
+    grows, at the state size each order costs (abstract: accuracy improves
+    quickly with n while the state widens combinatorially). On the same
+    inputs the CUDA path's error against softmax equals the oracle's own
+    truncation error to within the parity tolerance, and it falls strictly
+    from one order to the next."""
+    T, O = G.T, G.O
+    orders = [1, 2, 3, 4] if d == 16 else [1, 2, 3]
+    B, H, N, dv = 1, 4, 512, 64
+    errs = []
+    for n in orders:
+        cfg = T.Config(B, H, d, dv, n, dtype)
+        q, k, v = G.make_inputs(cfg, N, seed=60 + d)
+        out, _ = G.gpu_prefill(cfg, q, k, v)
+        og, qh, kh, vh = G.host(out), G.host(q), G.host(k), G.host(v)
+        e_gpu = e_ref = 0.0
+        for h in range(H):
+            sm = O.softmax_attention(qh[0, h], kh[0, h], vh[0, h])
+            ref = O.attention_direct(qh[0, h], kh[0, h], vh[0, h], n)
+            e_gpu = max(e_gpu, G.rel_err(og[0, h], sm))
+            e_ref = max(e_ref, G.rel_err(ref, sm))
+        assert abs(e_gpu - e_ref) <= G.TOL[dtype], (n, e_gpu, e_ref)
+        errs.append((T.state_elems(cfg), e_gpu))
+    for (s0, e0), (s1, e1) in zip(errs, errs[1:]):
+        assert s1 > s0 and e1 < e0, errs
+
+
 def test_merge_of_segments_equals_whole(G):
     T, O = G.T, G.O
     cfg = T.Config(2, 2, 16, 64, 3, "f32")
