@@ -329,39 +329,45 @@ short_prefill_kernel(ShortParams p) {
         vp[jp][2] = make_float2(x0.z, x1.z);
         vp[jp][3] = make_float2(x0.w, x1.w);
       }
-      for (int a = r0; a < DPAD; a += RS) {
-        float4 s = *reinterpret_cast<const float4*>(st + a * DV + 4 * cg);
-        const float4* f4 = reinterpret_cast<const float4*>(fk + a * LB);
-        float2 acc[4];
+      // two copies of the row loop, so that each stores to a known address
+      // space (a store through a generic pointer could alias the next row's
+      // shared-memory loads and would be ordered before them)
+      auto rows = [&](float* dS, float* dz) {
+        for (int a = r0; a < DPAD; a += RS) {
+          float4 s = *reinterpret_cast<const float4*>(st + a * DV + 4 * cg);
+          const float4* f4 = reinterpret_cast<const float4*>(fk + a * LB);
+          float2 acc[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[c] = make_float2(0.f, 0.f);
+          for (int c = 0; c < 4; ++c) acc[c] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int jj = 0; jj < LB / 4; ++jj) {
-          const float4 f = f4[jj];
-          const float2 fa = make_float2(f.x, f.y), fb = make_float2(f.z, f.w);
+          for (int jj = 0; jj < LB / 4; ++jj) {
+            const float4 f = f4[jj];
+            const float2 fa = make_float2(f.x, f.y), fb = make_float2(f.z, f.w);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            ffma2(acc[c], fa, vp[2 * jj][c]);
-            ffma2(acc[c], fb, vp[2 * jj + 1][c]);
+            for (int c = 0; c < 4; ++c) {
+              ffma2(acc[c], fa, vp[2 * jj][c]);
+              ffma2(acc[c], fb, vp[2 * jj + 1][c]);
+            }
           }
+          s.x += acc[0].x + acc[0].y;
+          s.y += acc[1].x + acc[1].y;
+          s.z += acc[2].x + acc[2].y;
+          s.w += acc[3].x + acc[3].y;
+          *reinterpret_cast<float4*>(dS + a * DV + 4 * cg) = s;
         }
-        s.x += acc[0].x + acc[0].y;
-        s.y += acc[1].x + acc[1].y;
-        s.z += acc[2].x + acc[2].y;
-        s.w += acc[3].x + acc[3].y;
-        float4* dst = reinterpret_cast<float4*>((last ? gst : st) + a * DV + 4 * cg);
-        *dst = s;
-      }
-      for (int a = tid; a < DPAD; a += 256) {
-        const float4* f4 = reinterpret_cast<const float4*>(fk + a * LB);
-        float zz = z[a];
+        for (int a = tid; a < DPAD; a += 256) {
+          const float4* f4 = reinterpret_cast<const float4*>(fk + a * LB);
+          float zz = z[a];
 #pragma unroll
-        for (int jj = 0; jj < LB / 4; ++jj) {
-          const float4 f = f4[jj];
-          zz += (f.x + f.y) + (f.z + f.w);
+          for (int jj = 0; jj < LB / 4; ++jj) {
+            const float4 f = f4[jj];
+            zz += (f.x + f.y) + (f.z + f.w);
+          }
+          dz[a] = zz;
         }
-        (last ? gst + DPAD * DV : z)[a] = zz;
-      }
+      };
+      if (last) rows(gst, gst + DPAD * DV);
+      else rows(st, z);
     }
     __syncthreads();                       // block b's reads of x, v are done
     if (b + 1 < nblk) store_in();
