@@ -100,6 +100,18 @@ def test_plan_short_segments(T):
                               num_sms=148)["path"] == T.TSA_PATH_SHORT
         assert T.prefill_plan(T.Config(64, 16, 16, 64, 3, dt, chunk=128), 8,
                               num_sms=148)["path"] != T.TSA_PATH_SHORT
+    # shared memory of the layout: state, phi(q) and phi(k) of a block, the
+    # block's values and inputs, intra-block kernel values, the 8 warps'
+    # readout partials and normaliser partials, feature codes and weights, and
+    # the mbarrier, in fp32 words
+    def words(d, dv, n):
+        dpad = -(-T.feature_dim(d, n) // 4) * 4
+        x = -(-(16 * (d + 1)) // 4) * 4
+        return dpad * (dv + 1) + 2 * dpad * 16 + 16 * dv + 2 * x + 256 + 8 * 16 * dv + 8 * 16 + 2 * dpad + 4
+    for (d, dv, n) in [(16, 64, 3), (16, 32, 3), (16, 128, 2), (32, 128, 2), (32, 32, 1)]:
+        p = T.prefill_plan(T.Config(4, 4, d, dv, n, "f32", chunk=16), 40, num_sms=148)
+        assert p["path"] == T.TSA_PATH_SHORT and p["smem_bytes"] == 4 * words(d, dv, n), (d, dv, n, p)
+        assert p["smem_bytes"] <= 113 * 1024
     # states too large for shared memory keep the chunked paths
     for (d, dv, n) in [(16, 64, 4), (32, 64, 3), (16, 128, 3)]:
         assert T.prefill_plan(T.Config(4, 4, d, dv, n, "bf16"), 8, num_sms=148)["path"] != T.TSA_PATH_SHORT
