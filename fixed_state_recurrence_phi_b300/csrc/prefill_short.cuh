@@ -26,7 +26,7 @@
 //             partials in shared memory; den_t = phi(q_t).z per warp
 //   output    partial sums + intra-block terms, divided, stored
 //   update    S[a][4 columns] += sum_j phi(k_j)[a] v_j, with the thread's
-//             values held in registers as token pairs; z[a] += sum_j phi(k_j)[a]
+//             values held in registers; z[a] += sum_j phi(k_j)[a]
 // The kernel is bound by shared-memory bandwidth, so every element of S is
 // read once per block by the readout and once (read and written) by the
 // update, with the other operand held in registers.
@@ -322,41 +322,30 @@ short_prefill_kernel(ShortParams p) {
       const bool last = (b == nblk - 1);
       const int cg = tid % CG, r0 = tid / CG;
       constexpr int RS = 256 / CG;
-      // the thread's values as token pairs: vp[jp][c] = (v_2jp[c], v_2jp+1[c])
-      float2 vp[LB / 2][4];
+      // the thread's values of the block's tokens, held in registers
+      float4 vr[LB];
 #pragma unroll
-      for (int jp = 0; jp < LB / 2; ++jp) {
-        const float4 x0 = *reinterpret_cast<const float4*>(vv + (2 * jp) * DV + 4 * cg);
-        const float4 x1 = *reinterpret_cast<const float4*>(vv + (2 * jp + 1) * DV + 4 * cg);
-        vp[jp][0] = make_float2(x0.x, x1.x);
-        vp[jp][1] = make_float2(x0.y, x1.y);
-        vp[jp][2] = make_float2(x0.z, x1.z);
-        vp[jp][3] = make_float2(x0.w, x1.w);
-      }
+      for (int j = 0; j < LB; ++j) vr[j] = *reinterpret_cast<const float4*>(vv + j * DV + 4 * cg);
       // two copies of the row loop, so that each stores to a known address
       // space (a store through a generic pointer could alias the next row's
-      // shared-memory loads and would be ordered before them)
+      // shared-memory loads and would be ordered before them); two rows in
+      // flight per thread
       auto rows = [&](float* dS, float* dz) {
+#pragma unroll 2
         for (int a = r0; a < DPAD; a += RS) {
           float4 s = *reinterpret_cast<const float4*>(st + a * DV + 4 * cg);
           const float4* f4 = reinterpret_cast<const float4*>(fk + a * LB);
-          float2 acc[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) acc[c] = make_float2(0.f, 0.f);
 #pragma unroll
           for (int jj = 0; jj < LB / 4; ++jj) {
             const float4 f = f4[jj];
-            const float2 fa = make_float2(f.x, f.y), fb = make_float2(f.z, f.w);
+            const float fv[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              fma_pair(acc[c], fa, vp[2 * jj][c]);
-              fma_pair(acc[c], fb, vp[2 * jj + 1][c]);
+            for (int u = 0; u < 4; ++u) {
+              const float4 x = vr[4 * jj + u];
+              s.x = fmaf(fv[u], x.x, s.x); s.y = fmaf(fv[u], x.y, s.y);
+              s.z = fmaf(fv[u], x.z, s.z); s.w = fmaf(fv[u], x.w, s.w);
             }
           }
-          s.x += acc[0].x + acc[0].y;
-          s.y += acc[1].x + acc[1].y;
-          s.z += acc[2].x + acc[2].y;
-          s.w += acc[3].x + acc[3].y;
           *reinterpret_cast<float4*>(dS + a * DV + 4 * cg) = s;
         }
         for (int a = tid; a < DPAD; a += 256) {
