@@ -218,17 +218,22 @@ class ClockSampler:
                 "samples": len(sm), "every_ms": 100}
 
 
-def cpu_baseline_prefill(w, max_heads=None):
-    """The float64 oracle (recurrent form, as it stands) on host cores."""
+def _oracle_head_prefill(args):
+    """One head's recurrent float64 prefill (a worker of the multi-core leg);
+    returns its wall time in seconds."""
+    w, h = args
     from fixed_state_recurrence_phi_b300.inputs import np_qkv
     from oracle import tsa_oracle as O
+    q, k, v = np_qkv(w["N"], w["d_k"], w["d_v"], seed=[w["seed"], h])
+    t0 = time.perf_counter()
+    O.prefill_recurrent(q, k, v, w["n_terms"])
+    return time.perf_counter() - t0
+
+
+def cpu_baseline_prefill(w, max_heads=None):
+    """The float64 oracle (recurrent form, as it stands) on one host core."""
     heads = w["B"] * w["H"] if max_heads is None else max_heads
-    t = 0.0
-    for h in range(heads):
-        q, k, v = np_qkv(w["N"], w["d_k"], w["d_v"], seed=[w["seed"], h])
-        t0 = time.perf_counter()
-        O.prefill_recurrent(q, k, v, w["n_terms"])
-        t += time.perf_counter() - t0
+    t = sum(_oracle_head_prefill((w, h)) for h in range(heads))
     per_head = t / heads
     all_heads = w["B"] * w["H"]
     return {"value": w["B"] * w["N"] / (per_head * all_heads), "unit": "tokens/s", "cores": 1,
@@ -237,16 +242,55 @@ def cpu_baseline_prefill(w, max_heads=None):
                       f"core; tokens/s = B*N / (mean head time x {all_heads} heads)"}
 
 
+def cpu_baseline_prefill_cores(w):
+    """The same oracle with the heads spread over the host cores (one process
+    per head, started with spawn: this process has initialised CUDA)."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    heads = w["B"] * w["H"]
+    cores = max(1, min(heads, len(os.sched_getaffinity(0))))
+    with cf.ProcessPoolExecutor(max_workers=cores, mp_context=mp.get_context("spawn")) as ex:
+        list(ex.map(_oracle_head_prefill, [(w, 0)] * cores))   # warm the workers (imports)
+        t0 = time.perf_counter()
+        list(ex.map(_oracle_head_prefill, [(w, h) for h in range(heads)]))
+        t = time.perf_counter() - t0
+    return {"value": w["B"] * w["N"] / t, "unit": "tokens/s", "cores": cores,
+            "sample": f"recurrent float64 prefill of all {heads} heads x {w['N']} tokens, "
+                      f"one process per head on {cores} cores (wall time of the batch)"}
+
+
+def cpu_baseline_decode(w, steps=2):
+    """The oracle's float64 decode step (as it stands: one call per head) over
+    every head of the decode workload, on one core, for a few steps."""
+    from oracle import tsa_oracle as O
+    heads = w["B"] * w["H"]
+    D = sum(__import__("math").comb(w["d_k"] + m - 1, m) for m in range(w["n_terms"]))
+    rng = np.random.default_rng(w["seed"])
+    S = [np.zeros((D, w["d_v"] + 1)) for _ in range(heads)]
+    x = rng.standard_normal((steps, heads, 2, w["d_k"]))
+    x /= np.linalg.norm(x, axis=-1, keepdims=True)
+    vv = rng.standard_normal((steps, heads, w["d_v"]))
+    t0 = time.perf_counter()
+    for s in range(steps):
+        for h in range(heads):
+            _, S[h] = O.decode_step(x[s, h, 0], x[s, h, 1], vv[s, h], S[h], w["n_terms"])
+    t = (time.perf_counter() - t0) / steps
+    return {"us_per_step": t * 1e6, "state_GBps": heads * D * (w["d_v"] + 1) * 8 * 2 / t / 1e9,
+            "cores": 1, "sample": f"{steps} steps over all {heads} heads, float64, one decode_step call per "
+                                  f"head (state bytes counted in float64)"}
+
+
 def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
         return
     w = PREFILL
+    heads = w["B"] * w["H"]
     times = []
     for i in range(args.warmup + args.steps):
-        r = cpu_baseline_prefill(w, max_heads=1)
+        t_step = sum(_oracle_head_prefill((w, h)) for h in range(heads))
         if i >= args.warmup:
-            times.append(w["B"] * w["N"] / r["value"])
+            times.append(t_step)
     t = statistics.mean(times)
     value = w["B"] * w["N"] / t
     line = {
@@ -254,10 +298,10 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w["workload"], "B": w["B"], "H": w["H"], "N": w["N"], "d_k": w["d_k"],
-                   "d_v": w["d_v"], "n_terms": w["n_terms"], "l2": "n/a (CPU)"},
+                   "d_v": w["d_v"], "n_terms": w["n_terms"]},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": "each step: recurrent float64 prefill of 1 of 8 heads x 8192 tokens "
-                                   "on 1 host core; tokens/s scaled by the 8 heads"},
+                         "sample": f"each step: recurrent float64 prefill of all {heads} heads x {w['N']} "
+                                   "tokens on 1 host core (inputs drawn outside the timing)"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -612,8 +656,14 @@ def _run_ours(args, clk):
     ach = pre_bytes / (ms / 1e3) / 1e9 if do_pre else float("nan")
     if rank != 0:
         return
-    cpu = cpu_baseline_prefill(w) if (ws == 1 and do_pre and not args.no_cpu_baseline) else None
+    cpu = None
+    if ws == 1 and do_pre and not args.no_cpu_baseline:
+        cpu = cpu_baseline_prefill(w)
+        cpu["legs"] = [dict(cpu_baseline_prefill_cores(w), what="prefill, heads over cores")]
+        if do_dec:
+            cpu["legs"].append(dict(cpu_baseline_decode(dw), what=f"decode step, {dw['workload']}"))
     traffic = _profile_traffic()
+    r3 = lambda x: None if x is None else float(f"{x:.4g}")
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -622,35 +672,39 @@ def _run_ours(args, clk):
                    "d_v": w["d_v"], "n_terms": w["n_terms"], "chunk": plan["chunk"],
                    "n_spans": plan["n_spans"], "path": PATH_NAMES[plan["path"]],
                    "l2": "flushed between timed steps (256 MB write)", "timing": timing},
-        "ms_per_step_eager": ms_eager,
-        "host_us_per_call": host_us,
         "roofline": {"bound": "hbm", "kernel": "tsa_prefill (all launches of the call)",
                      "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
                      "peak_source": f"{peak_src} (copy bandwidth)",
                      "algorithmic_bytes": pre_bytes,
                      "traffic": traffic.get("prefill")},
-        "e2e": {"value": weak_scaling_value(ws, tokens, e2e_ms) if do_pre else None, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "e2e": {"value": weak_scaling_value(ws, tokens, e2e_ms) if do_pre else None, "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * plan["launches"] if do_pre else 0,
-        "decode": {"workload": dw["workload"], "us_per_step": dec_us, "us_per_step_eager": eager_us,
-                   "us_per_token_per_sequence": dec_us / dw["B"],
-                   "state_GBps": state_bytes_step / (dec_us / 1e6) / 1e9,
-                   "roofline": {"bound": "hbm", "kernel": "decode_kernel",
-                                "achieved": dec_bytes / (dec_us / 1e6) / 1e9, "peak": hbm_peak,
-                                "unit": "GB/s", "frac": dec_bytes / (dec_us / 1e6) / 1e9 / hbm_peak,
-                                "algorithmic_bytes": dec_bytes, "traffic": traffic.get("decode")},
-                   "timing": f"CUDA graph of {steps} steps x {reps}, states rotated over "
-                             f"{DECODE_ROTATE} sets (> L2)",
-                   "gpu_launches": reps * steps,
-                   "states_prefilled_with_N": args.decode_prefill_n,
-                   "prefill_ms": long_prefill_ms},
-        "prefill_tensor_core": tc_lines,
-        "append": append_lines,
-        "orders": order_lines,
-        "merge": {"workload": dw["workload"], "ms": merge_ms,
-                  "GBps": 3 * T.state_bytes(dcfg) / (merge_ms / 1e3) / 1e9},
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "ms_per_step_eager": ms_eager,
+        "host_us_per_call": host_us,
+        # compact sections; the tensor-core prefill and the decode come last
+        "append": [{"L": a["L"], "us": r3(a["us_per_call"]), "frac_hbm": r3(a["roofline"]["frac"]),
+                    "path": a["path"]} for a in append_lines],
+        "orders": [{"n": o["n_terms"], "ms": r3(o["ms"]), "state_B_per_head": o["state_bytes_per_head"],
+                    "path": o["path"]} for o in order_lines],
+        "merge": {"ms": r3(merge_ms), "GBps": r3(3 * T.state_bytes(dcfg) / (merge_ms / 1e3) / 1e9)},
+        "prefill_tensor_core": [
+            {"workload": t["workload"], "ms": r3(t["ms"]), "tokens_per_s": r3(t["tokens_per_s"]),
+             "plan": t["plan"],
+             "roofline": {"bound": "tensor", "achieved": r3(t["roofline"]["achieved"]),
+                          "peak": t["roofline"]["peak"], "unit": "TFLOP/s", "frac": r3(t["roofline"]["frac"]),
+                          "frac_of_sustained": r3(t["roofline"]["frac_of_sustained"]),
+                          "traffic": traffic.get(t["workload"])}} for t in tc_lines],
+        "decode": {"workload": dw["workload"], "us_per_step": r3(dec_us), "us_per_step_eager": r3(eager_us),
+                   "state_GBps": r3(state_bytes_step / (dec_us / 1e6) / 1e9),
+                   "roofline": {"bound": "hbm", "kernel": "decode_kernel",
+                                "achieved": r3(dec_bytes / (dec_us / 1e6) / 1e9), "peak": hbm_peak,
+                                "unit": "GB/s", "frac": r3(dec_bytes / (dec_us / 1e6) / 1e9 / hbm_peak),
+                                "algorithmic_bytes": dec_bytes, "traffic": traffic.get("decode")},
+                   "timing": f"graph of {steps} steps x {reps}, {DECODE_ROTATE} state sets (> L2)",
+                   "gpu_launches": reps * steps, "states_prefill_ms": r3(long_prefill_ms)},
     }
     print(json.dumps(line), flush=True)
 

@@ -278,15 +278,11 @@ span_scan_kernel(float* __restrict__ states, float* __restrict__ scratch, int he
 // Launch the span scan. Its carveout is pinned to the shared-memory maximum,
 // like the prefill kernels around it, so that the SMs do not repartition
 // L1/shared memory between the three launches of a multi-span prefill.
+cudaError_t set_carveout_once(const void* kernel, int carveout);   // tsa_abi.cu: once per device
 static inline cudaError_t launch_span_scan(float* states, float* scratch, int heads, int n_spans, int elems4,
                                            int accumulate, cudaStream_t s) {
-  static bool carveout_set = false;
-  if (!carveout_set) {
-    cudaError_t e = cudaFuncSetAttribute(span_scan_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    carveout_set = true;
-  }
+  cudaError_t ce = set_carveout_once((const void*)span_scan_kernel, (int)cudaSharedmemCarveoutMaxShared);
+  if (ce != cudaSuccess) return ce;
   // launched with a programmatic dependency on the span pass before it
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));

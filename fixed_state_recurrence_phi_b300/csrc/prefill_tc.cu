@@ -8,6 +8,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "tsa_internal.h"
@@ -28,7 +29,16 @@ bool g_err_ready[64];
 constexpr size_t kSmemLimit = 227 * 1024;
 constexpr int kTmemCols = 512;
 
+// Testing hooks (tsa_debug_set_wait_limit, tsa_debug_withhold_publication).
+std::atomic<unsigned long long> g_wait_ns{TC_WAIT_NS};
+std::atomic<int> g_withhold{0};
+
 }  // namespace
+
+void tc_debug_params(unsigned long long* wait_ns, int* withhold) {
+  *wait_ns = g_wait_ns.load();
+  *withhold = g_withhold.load();
+}
 
 tsa_status device_error_word(int** out) {
   int dev = 0;
@@ -155,6 +165,7 @@ tsa_status launch_tc(const tsa_plan& pl, const TcSlicing& ts, const PrefillParam
   p.chunks_per_span = pl.chunks_per_span; p.accumulate = pp.accumulate;
   p.n_slices = ts.n_slices; p.nmax = ts.nmax; p.ring = ts.ring;
   for (int k = 0; k < ts.n_slices; ++k) { p.slice_c0[k] = ts.c0[k]; p.slice_w[k] = ts.w[k]; }
+  tc_debug_params(&p.wait_ns, &p.dbg_withhold);
   tsa_status st = device_error_word(&p.err);
   if (st != TSA_OK) return st;
   CUtensorMap mq, mk, mv;
@@ -197,3 +208,14 @@ tsa_status launch_prefill_tc(const tsa_config* c, const tsa_plan& pl, const Pref
 }
 
 }  // namespace tsa
+
+extern "C" tsa_status tsa_debug_set_wait_limit(uint64_t ns) {
+  tsa::g_wait_ns.store(ns == 0 ? tsa::TC_WAIT_NS : (unsigned long long)ns);
+  return TSA_OK;
+}
+
+extern "C" tsa_status tsa_debug_withhold_publication(int what) {
+  if (what != 0 && what != 1) return tsa::fail(TSA_ERR_INVALID, "withhold must be 0 or 1 (got %d)", what);
+  tsa::g_withhold.store(what);
+  return TSA_OK;
+}

@@ -54,7 +54,7 @@ constexpr int TC_THREADS = 288;   // 8 worker warps + 1 issuer warp
 constexpr int TC_WORKERS = 256;
 constexpr int TC_MAX_SLICES = 4;
 constexpr int TC_MAX_RING = 3;
-constexpr uint64_t TC_WAIT_NS = 1000000000ull;   // 1 s per wait
+constexpr uint64_t TC_WAIT_NS = 1000000000ull;   // 1 s: the default bound of every wait
 
 struct TcParams {
   void* out;
@@ -64,6 +64,8 @@ struct TcParams {
   long long N;
   int heads, dv, n_spans, chunks_per_span, accumulate, n_slices, nmax, ring;
   int span_layout;   // fp32 span pass: its own shared-memory layout (Tc32Smem)
+  unsigned long long wait_ns;   // bound of each wait between the warp roles
+  int dbg_withhold;  // testing only: 1 = the issuer never publishes the first chunk's O
   int slice_c0[TC_MAX_SLICES];
   int slice_w[TC_MAX_SLICES];
 };
@@ -196,16 +198,19 @@ struct TcBars {
   __device__ uint64_t* drain() const { return b + 15; }
   __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(b + 16); }
   __device__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(b + 16) + 1; }
-  __device__ void init() const {
+  // the bound of each wait (the kernel's wait_ns), set by init
+  __device__ uint64_t* wait_limit() const { return b + 24; }
+  __device__ void init(uint64_t wait_ns) const {
     const uint32_t cnt[16] = {1, 8, 1, 1, 8, 8, 8, 1, 1, 1, 1, 1, 8, 8, 1, 1};
     for (int k = 0; k < 16; ++k) tc::mbar_init(b + k, cnt[k]);
     *abort_flag() = 0;
+    *wait_limit() = wait_ns;
     tc::mbar_fence_init();
   }
 };
 
 __device__ __forceinline__ bool tc_wait(const TcBars& B, uint64_t* bar, uint32_t parity) {
-  return tc::mbar_wait_or_abort(bar, parity, TC_WAIT_NS, B.abort_flag());
+  return tc::mbar_wait_or_abort(bar, parity, *B.wait_limit(), B.abort_flag());
 }
 // A worker warp waits as one: if any lane gives up, the whole warp does.
 __device__ __forceinline__ bool tc_wait_warp(const TcBars& B, uint64_t* bar, uint32_t parity) {
@@ -300,7 +305,7 @@ span_state_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   const int nm = u.nm;
 
   if (warp == 0) tc::tmem_alloc(B.tmem_slot(), 512);
-  if (tid == 0) B.init();
+  if (tid == 0) B.init(p.wait_ns);
   if (tid < TC_WORKERS) {
     tc_write_ones(smem + L.v(0), u.W, tid);
     tc_write_ones(smem + L.v(1), u.W, tid);
@@ -415,7 +420,7 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
   const size_t st_elems = (size_t)DPAD * (p.dv + 1);
 
   if (warp == 0) tc::tmem_alloc(B.tmem_slot(), 512);
-  if (tid == 0) B.init();
+  if (tid == 0) B.init(p.wait_ns);
   if (tid < TC_WORKERS) {
     tc_write_ones(smem + L.v(0), W, tid);
     tc_write_ones(smem + L.v(1), W, tid);

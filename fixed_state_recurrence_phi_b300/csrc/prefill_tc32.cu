@@ -82,6 +82,7 @@ tsa_status launch32(const tsa_plan& pl, const PrefillParams& pp, cudaStream_t s)
   p.slice_c0[0] = 0; p.slice_w[0] = pp.dv;
   p.ring = (smem_tc32<DK, NT>(pp.dv, 3) <= kSmemLimit) ? 3 : 2;
   const int smem = (int)smem_tc32<DK, NT>(pp.dv, p.ring);
+  tc_debug_params(&p.wait_ns, &p.dbg_withhold);
   tsa_status st = device_error_word(&p.err);
   if (st != TSA_OK) return st;
   CUtensorMap mq, mk, mv, mo;

@@ -142,7 +142,7 @@ struct Tc32Bars {
   __device__ uint64_t* roempty(int r) const { return b + 20 + r; }
   __device__ TcBars ring_bars() const { return TcBars{b}; }
   // stg_users: warps that read the staging (8, or 16 in the output kernel)
-  __device__ void init(uint32_t stg_users = 8) const {
+  __device__ void init(uint64_t wait_ns, uint32_t stg_users = 8) const {
     const uint32_t cnt[16] = {1, stg_users, 8, 8, 8, 8, 8, 1, 1, 1, 1, 1, 8, 8, 1, 1};
     for (int k = 0; k < 16; ++k) tc::mbar_init(b + k, cnt[k]);
     for (int r = 0; r < 2; ++r) {
@@ -152,6 +152,7 @@ struct Tc32Bars {
     tc::mbar_init(stload(), 1);
     *copy_issued() = 0;
     *TcBars{b}.abort_flag() = 0;
+    *TcBars{b}.wait_limit() = wait_ns;
     tc::mbar_fence_init();
   }
 };
@@ -483,7 +484,7 @@ span_state_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_
 
   tc::grid_dep_launch();   // the scan after this pass may be launched now
   if (warp == 0) tc::tmem_alloc(B.tmem_slot(), 512);
-  if (tid == 0) X.init();
+  if (tid == 0) X.init(p.wait_ns);
   if (warp == 0) {
     __syncwarp();   // the first inputs at once, overlapping the set-up
     if (u.n_chunks > 0)
@@ -623,7 +624,7 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
   const bool st_bulk = st_src != nullptr && st_bytes % 16 == 0 && st_bytes <= (uint32_t)p.ring * 32768u;
 
   if (warp == 0) tc::tmem_alloc(B.tmem_slot(), 512);
-  if (tid == 0) X.init(16);
+  if (tid == 0) X.init(p.wait_ns, 16);
   if (warp == 0) {
     // the first chunk's inputs at once (ready before this call's first
     // launch), overlapping the set-up below
@@ -726,7 +727,9 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
         const uint32_t ph = tm + col_A + (uint32_t)tc32_p_col(k);
         mma3_ts(tm + col_O, ph, ph + 16u, dVh + (uint64_t)(16 * k), dVl + (uint64_t)(16 * k), id_pv, 1u);
       }
-      tc::mma_commit_elect(B.odone());
+      // (testing only: with dbg_withhold the first chunk's O is never
+      // published, so the TMEM warps' bounded wait for it runs out)
+      if (!(p.dbg_withhold && c == 0)) tc::mma_commit_elect(B.odone());
       TSA_TRACE_EVENT(3, c);
       // S_f += phi(K_f)^T [V, 1], 64 tokens at a time
       if (need_update) {

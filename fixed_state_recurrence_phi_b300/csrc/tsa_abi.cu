@@ -117,6 +117,23 @@ cudaError_t set_smem_once(const void* kernel, int smem) {
   return e;
 }
 
+// The preferred shared-memory carveout of a kernel, set once per device (the
+// attribute is per device: a second GPU needs its own call).
+cudaError_t set_carveout_once(const void* kernel, int carveout) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, int> done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = done[dev].find(kernel);
+  if (it != done[dev].end() && it->second == carveout) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
+  if (e == cudaSuccess) done[dev][kernel] = carveout;
+  return e;
+}
+
 int device_sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -404,6 +421,7 @@ tsa_status tsa_prefill_plan(const tsa_config* c, int64_t N, int num_sms, tsa_pla
 
 tsa_status tsa_prefill(const tsa_config* c, int64_t N, const void* q, const void* k, const void* v,
                        void* out, float* states, unsigned flags, void* stream) {
+  NvtxRange nvtx_range("tsa_prefill");
   tsa_status st = check_config(c);
   if (st != TSA_OK) return st;
   if (N < 0) return fail(TSA_ERR_INVALID, "N must be >= 0 (got %lld)", (long long)N);
@@ -448,6 +466,7 @@ tsa_status tsa_prefill(const tsa_config* c, int64_t N, const void* q, const void
 
 tsa_status tsa_decode_step(const tsa_config* c, const void* q, const void* k, const void* v,
                            void* out, float* states, void* stream) {
+  NvtxRange nvtx_range("tsa_decode_step");
   tsa_status st = check_config(c);
   if (st != TSA_OK) return st;
   if (!q || !k || !v || !out || !states) return fail(TSA_ERR_INVALID, "NULL pointer");
@@ -461,6 +480,7 @@ tsa_status tsa_decode_step(const tsa_config* c, const void* q, const void* k, co
 }
 
 tsa_status tsa_state_merge(const tsa_config* c, float* a, const float* b, void* stream) {
+  NvtxRange nvtx_range("tsa_state_merge");
   tsa_status st = check_config(c);
   if (st != TSA_OK) return st;
   if (!a || !b) return fail(TSA_ERR_INVALID, "NULL state pointer");
@@ -479,6 +499,7 @@ tsa_status tsa_state_merge(const tsa_config* c, float* a, const float* b, void* 
 }
 
 tsa_status tsa_state_to_canonical(const tsa_config* c, const float* states, float* dst, void* stream) {
+  NvtxRange nvtx_range("tsa_state_to_canonical");
   tsa_status st = check_config(c);
   if (st != TSA_OK) return st;
   if (!states || !dst) return fail(TSA_ERR_INVALID, "NULL pointer");
@@ -493,6 +514,7 @@ tsa_status tsa_state_to_canonical(const tsa_config* c, const float* states, floa
 }
 
 tsa_status tsa_sync_status(void* stream) {
+  NvtxRange nvtx_range("tsa_sync_status");
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   return take_device_error();

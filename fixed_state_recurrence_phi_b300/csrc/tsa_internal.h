@@ -1,10 +1,20 @@
 // tsa_internal.h -- host helpers shared by the translation units of libtsa.so.
 #pragma once
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include "../../include/tsa.h"
 #include "prefill_params.h"
 
 namespace tsa {
+// An NVTX range over one ABI call (named after the call), so that a profiler
+// timeline shows which launches each call made. Header-only NVTX: without an
+// attached tool the push and pop are no-ops.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 tsa_status fail(tsa_status s, const char* fmt, ...);
 tsa_status cuda_fail(cudaError_t e, const char* what);
 tsa_status check_config(const tsa_config* c);
@@ -26,6 +36,9 @@ bool tc_supported(int dk, int nt);
 bool tc_slicing(int dk, int nt, int dv, TcSlicing* ts);
 tsa_status launch_prefill_tc(const tsa_config* c, const tsa_plan& pl, const PrefillParams& p, cudaStream_t s);
 tsa_status device_error_word(int** out);
+// The testing hooks' current settings: the bound of each wait and whether
+// the fp32 output pass withholds its first publication.
+void tc_debug_params(unsigned long long* wait_ns, int* withhold);
 // fp32 tensor-core prefill with split-bf16 operands (prefill_tc32.cu).
 bool tc32_fits(int dk, int nt, int dv);
 size_t tc32_smem(int dk, int nt, int dv);

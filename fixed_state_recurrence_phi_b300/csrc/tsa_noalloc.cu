@@ -31,7 +31,9 @@ bool g_ready[64];
 
 // Device address of g_noalloc_scratch on the current device. In host code the
 // array's name is only a host-side stand-in, so the address is looked up once
-// per device, with that device current, and cached.
+// per device, with that device current, and cached for the life of the
+// process (a cudaDeviceReset reloads the module and leaves the cached address
+// stale; the header tells callers not to reset a device they use this on).
 tsa_status scratch_address(float** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -59,6 +61,7 @@ using namespace tsa;
 extern "C" tsa_status tsa_prefill_noalloc(const tsa_config* c, int64_t N, const void* q, const void* k,
                                           const void* v, void* out, float* states, unsigned flags,
                                           void* stream) {
+  NvtxRange nvtx_range("tsa_prefill_noalloc");
   tsa_status st = check_config(c);
   if (st != TSA_OK) return st;
   if (N < 0) return fail(TSA_ERR_INVALID, "N must be >= 0 (got %lld)", (long long)N);

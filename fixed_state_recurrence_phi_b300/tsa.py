@@ -28,6 +28,7 @@ EXPORTS = (
     "tsa_decode_step",
     "tsa_state_merge", "tsa_state_to_canonical", "tsa_sync_status",
     "tsa_status_string", "tsa_last_error",
+    "tsa_debug_set_wait_limit", "tsa_debug_withhold_publication",
 )
 
 
@@ -72,6 +73,8 @@ def _load():
         "tsa_sync_status": (I, [P]),
         "tsa_status_string": (ctypes.c_char_p, [I]),
         "tsa_last_error": (ctypes.c_char_p, []),
+        "tsa_debug_set_wait_limit": (I, [ctypes.c_uint64]),
+        "tsa_debug_withhold_publication": (I, [I]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -193,6 +196,16 @@ def state_to_canonical(cfg, states, dst, stream=None):
 
 def sync_status(stream=None):
     _check("tsa_sync_status", _lib.tsa_sync_status(_stream(stream)))
+
+
+def debug_set_wait_limit(ns: int):
+    """Testing hook: the bound of every wait between warp roles (0 = default)."""
+    _check("tsa_debug_set_wait_limit", _lib.tsa_debug_set_wait_limit(int(ns)))
+
+
+def debug_withhold_publication(what: int):
+    """Testing hook: 1 = the fp32 output pass withholds its first publication."""
+    _check("tsa_debug_withhold_publication", _lib.tsa_debug_withhold_publication(int(what)))
 
 
 # ---- small torch conveniences (allocation only) ----------------------------

@@ -158,7 +158,9 @@ tsa_status tsa_prefill(const tsa_config* cfg, int64_t N, const void* q, const vo
  * single span per head need none.
  *  - The first call on each device looks up the array's device address (once,
  *    with that device current); make that first call before any stream
- *    capture.
+ *    capture. The address is kept for the life of the process: after a
+ *    cudaDeviceReset of that device it is stale, so do not call this entry
+ *    point on a device that has been reset.
  *  - All calls on a device share the one array, and a call leaves its own
  *    contents there. Calls that can overlap on the GPU (different streams with
  *    no ordering between them) race on it: order them on one stream, or use
@@ -192,6 +194,21 @@ tsa_status tsa_state_to_canonical(const tsa_config* cfg, const float* states, fl
  * leaving its outputs incomplete). The flag is per device and is cleared by
  * this call. */
 tsa_status tsa_sync_status(void* cuda_stream);
+
+/* Testing hooks for the failure path of the bounded waits; not for use in
+ * production. Both settings are process-wide and apply to calls made after
+ * them.
+ *  - tsa_debug_set_wait_limit: the bound, in nanoseconds, of every wait
+ *    between the warp roles of the tensor-core kernels (default 1 s; 0
+ *    restores the default).
+ *  - tsa_debug_withhold_publication(1): the fp32 tensor-core output pass
+ *    (TSA_PATH_TC_F32) never publishes the first chunk's completed output
+ *    accumulator, so the waits for it run out: each CTA gives up, releases
+ *    its tensor memory and exits with its outputs incomplete, and the next
+ *    tsa_sync_status returns TSA_ERR_TIMEOUT. 0 turns it off; other values
+ *    are TSA_ERR_INVALID. */
+tsa_status tsa_debug_set_wait_limit(uint64_t ns);
+tsa_status tsa_debug_withhold_publication(int what);
 
 const char* tsa_status_string(tsa_status s);
 const char* tsa_last_error(void);

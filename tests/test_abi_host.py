@@ -163,3 +163,12 @@ def test_validation_codes(T):
         T.prefill_plan(ok, -5, num_sms=148)
     assert e.value.status == T.TSA_ERR_INVALID
     assert T.status_string(T.TSA_ERR_TIMEOUT) == "TSA_ERR_TIMEOUT"
+
+
+def test_debug_hooks_validate(T):
+    """The testing hooks take only their documented values (host only)."""
+    with pytest.raises(T.TsaError) as e:
+        T.debug_withhold_publication(7)
+    assert e.value.status == T.TSA_ERR_INVALID
+    T.debug_withhold_publication(0)
+    T.debug_set_wait_limit(0)

@@ -1,0 +1,60 @@
+"""Failure detection on the GPU without a fault: a bounded device-side wait
+that runs out is reported as TSA_ERR_TIMEOUT, and the context stays usable.
+
+The testing hooks of the library shorten the bound of every wait between the
+warp roles of the tensor-core kernels to a few milliseconds and make the fp32
+output pass withhold one publication (the first chunk's completed output
+accumulator), so the warps waiting for it give up: each CTA sets its abort
+flag, stops issuing work, waits (bounded) for what it has in flight, releases
+its tensor memory and exits, and records the failure in the library's device
+error word. tsa_sync_status must then report TSA_ERR_TIMEOUT once; a normal
+prefill in the same process must afterwards match the oracle (its CTAs
+allocate the tensor memory the aborted ones released).
+"""
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def T():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from fixed_state_recurrence_phi_b300 import build
+    build.build()
+    from fixed_state_recurrence_phi_b300 import tsa
+    return tsa
+
+
+def test_withheld_publication_times_out_then_prefill_is_correct(T):
+    from gpu_helpers import check_head, host, make_inputs, oracle_prefill, canonical, TOL
+    cfg = T.Config(1, 2, 16, 64, 3, "f32")
+    N = 700
+    assert T.prefill_plan(cfg, N)["path"] == T.TSA_PATH_TC_F32
+    q, k, v = make_inputs(cfg, N, seed=31)
+    out = torch.zeros((1, 2, N, 64), device="cuda")
+    st = T.new_states(cfg)
+    T.sync_status()
+    T.debug_set_wait_limit(2_000_000)          # 2 ms per wait
+    T.debug_withhold_publication(1)
+    try:
+        T.prefill(cfg, N, q, k, v, out, st)
+        with pytest.raises(T.TsaError) as e:
+            T.sync_status()
+        assert e.value.status == T.TSA_ERR_TIMEOUT, T.last_error()
+    finally:
+        T.debug_withhold_publication(0)
+        T.debug_set_wait_limit(0)
+    T.sync_status()                              # reported once, then cleared
+    # the same call again, hooks off: complete and correct
+    out.zero_()
+    st.zero_()
+    T.prefill(cfg, N, q, k, v, out, st)
+    T.sync_status()
+    S = canonical(cfg, st)
+    qh, kh, vh = host(q), host(k), host(v)
+    for h in range(2):
+        o_r, S_r = oracle_prefill(qh[0, h], kh[0, h], vh[0, h], 3)
+        check_head(cfg, host(out[0, h]), S[0, h], o_r, S_r, TOL["f32"], f"head {h}")
+
