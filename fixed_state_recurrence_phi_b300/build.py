@@ -12,7 +12,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libtsa.so")
-SOURCES = ["tsa_abi.cu", "prefill_tc.cu", "prefill_tc32.cu", "prefill_short.cu", "tsa_noalloc.cu"]
+SOURCES = ["tsa_abi.cu", "prefill_tc.cu", "prefill_tc32.cu", "prefill_pair.cu", "prefill_short.cu", "tsa_noalloc.cu"]
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-std=c++17", "-O3", "-lineinfo",

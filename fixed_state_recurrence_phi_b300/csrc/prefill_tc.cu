@@ -157,35 +157,55 @@ cudaError_t set_smem(Kern kernel, int smem) {
 }
 
 template <int DK, int NT>
-tsa_status launch_tc(const tsa_plan& pl, const TcSlicing& ts, const PrefillParams& pp, cudaStream_t s) {
+void fill_tc_params(TcParams* p, const tsa_plan& pl, const TcSlicing& ts, const PrefillParams& pp) {
+  memset(p, 0, sizeof(*p));
+  p->out = pp.out; p->states = pp.states; p->scratch = pp.scratch;
+  p->N = pp.N; p->heads = pp.heads; p->dv = pp.dv; p->n_spans = pl.n_spans;
+  p->chunks_per_span = pl.chunks_per_span; p->accumulate = pp.accumulate;
+  p->n_slices = ts.n_slices; p->nmax = ts.nmax; p->ring = ts.ring;
+  for (int k = 0; k < ts.n_slices; ++k) { p->slice_c0[k] = ts.c0[k]; p->slice_w[k] = ts.w[k]; }
+  tc_debug_params(&p->wait_ns, &p->dbg_withhold);
+}
+
+// The span-state pass of a multi-span plan (each span's state sum into the
+// scratch, value slices as the TMEM budget allows) and the exclusive scan
+// over spans.
+template <int DK, int NT>
+tsa_status launch_span_tc(const tsa_plan& pl, const TcSlicing& ts, const PrefillParams& pp, cudaStream_t s) {
   TcParams p;
-  memset(&p, 0, sizeof(p));
-  p.out = pp.out; p.states = pp.states; p.scratch = pp.scratch;
-  p.N = pp.N; p.heads = pp.heads; p.dv = pp.dv; p.n_spans = pl.n_spans;
-  p.chunks_per_span = pl.chunks_per_span; p.accumulate = pp.accumulate;
-  p.n_slices = ts.n_slices; p.nmax = ts.nmax; p.ring = ts.ring;
-  for (int k = 0; k < ts.n_slices; ++k) { p.slice_c0[k] = ts.c0[k]; p.slice_w[k] = ts.w[k]; }
-  tc_debug_params(&p.wait_ns, &p.dbg_withhold);
+  fill_tc_params<DK, NT>(&p, pl, ts, pp);
   tsa_status st = device_error_word(&p.err);
   if (st != TSA_OK) return st;
+  CUtensorMap mk, mv;
+  if ((st = make_tmap(&mk, pp.k, DK, pp.N, pp.heads, DK / 8)) != TSA_OK) return st;
+  if ((st = make_tmap(&mv, pp.v, pp.dv, pp.N, pp.heads, 2)) != TSA_OK) return st;
+  const unsigned grid = (unsigned)((long long)pp.heads * ts.n_slices * pl.n_spans);
+  const int smem = (int)ts.smem;
+  cudaError_t e = set_smem(span_state_tc_kernel<DK, NT>, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_state_tc)");
+  span_state_tc_kernel<DK, NT><<<grid, TC_THREADS, smem, s>>>(p, mk, mv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch span_state_tc");
+  const int elems4 = (int)(round_up(feat_dim(DK, NT), 4) * (pp.dv + 1) / 4);
+  e = launch_span_scan(pp.states, pp.scratch, pp.heads, pl.n_spans, elems4, pp.accumulate, s);
+  if (e != cudaSuccess) return cuda_fail(e, "launch span_scan");
+  return TSA_OK;
+}
+
+template <int DK, int NT>
+tsa_status launch_tc(const tsa_plan& pl, const TcSlicing& ts, const PrefillParams& pp, cudaStream_t s) {
+  tsa_status st;
+  if (pl.n_spans > 1 && (st = launch_span_tc<DK, NT>(pl, ts, pp, s)) != TSA_OK) return st;
+  TcParams p;
+  fill_tc_params<DK, NT>(&p, pl, ts, pp);
+  if ((st = device_error_word(&p.err)) != TSA_OK) return st;
   CUtensorMap mq, mk, mv;
   if ((st = make_tmap(&mq, pp.q, DK, pp.N, pp.heads, DK / 8)) != TSA_OK) return st;
   if ((st = make_tmap(&mk, pp.k, DK, pp.N, pp.heads, DK / 8)) != TSA_OK) return st;
   if ((st = make_tmap(&mv, pp.v, pp.dv, pp.N, pp.heads, 2)) != TSA_OK) return st;
   const unsigned grid = (unsigned)((long long)pp.heads * ts.n_slices * pl.n_spans);
   const int smem = (int)ts.smem;
-  cudaError_t e;
-  if (pl.n_spans > 1) {
-    e = set_smem(span_state_tc_kernel<DK, NT>, smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_state_tc)");
-    span_state_tc_kernel<DK, NT><<<grid, TC_THREADS, smem, s>>>(p, mk, mv);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "launch span_state_tc");
-    const int elems4 = (int)(round_up(feat_dim(DK, NT), 4) * (pp.dv + 1) / 4);
-    e = launch_span_scan(pp.states, pp.scratch, pp.heads, pl.n_spans, elems4, pp.accumulate, s);
-    if (e != cudaSuccess) return cuda_fail(e, "launch span_scan");
-  }
-  e = set_smem(span_output_tc_kernel<__nv_bfloat16, DK, NT>, smem);
+  cudaError_t e = set_smem(span_output_tc_kernel<__nv_bfloat16, DK, NT>, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_output_tc)");
   span_output_tc_kernel<__nv_bfloat16, DK, NT><<<grid, TC_THREADS, smem, s>>>(p, mq, mk, mv);
   e = cudaGetLastError();
@@ -194,6 +214,18 @@ tsa_status launch_tc(const tsa_plan& pl, const TcSlicing& ts, const PrefillParam
 }
 
 }  // namespace
+
+tsa_status launch_span_states_tc(int dk, int nt, const tsa_plan& pl, const PrefillParams& p, cudaStream_t s) {
+  TcSlicing ts;
+  if (!tc_slicing(dk, nt, p.dv, &ts))
+    return fail(TSA_ERR_UNSUPPORTED, "no tensor-core slicing for d_k=%d d_v=%d n=%d", dk, p.dv, nt);
+#define TSA_TCS_CASE(DK, NT) \
+  if (dk == DK && nt == NT) return launch_span_tc<DK, NT>(pl, ts, p, s);
+  TSA_TCS_CASE(16, 1) TSA_TCS_CASE(16, 2) TSA_TCS_CASE(16, 3) TSA_TCS_CASE(16, 4)
+  TSA_TCS_CASE(32, 1) TSA_TCS_CASE(32, 2) TSA_TCS_CASE(32, 3)
+#undef TSA_TCS_CASE
+  return fail(TSA_ERR_UNSUPPORTED, "no tensor-core span pass for d_k=%d n=%d", dk, nt);
+}
 
 tsa_status launch_prefill_tc(const tsa_config* c, const tsa_plan& pl, const PrefillParams& p, cudaStream_t s) {
   TcSlicing ts;

@@ -195,6 +195,7 @@ static tsa_status make_plan_tc(const tsa_config* c, long long N, int num_sms, co
   pl->scratch_bytes = best_s > 1 ? (size_t)heads * best_s * state_floats_per_head(c) * 4 : 0;
   pl->launches = best_s > 1 ? 3 : 1;
   pl->path = path;
+  pl->cluster = 1;
   return TSA_OK;
 }
 
@@ -219,6 +220,7 @@ tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl
     pl->scratch_bytes = 0;
     pl->launches = 1;
     pl->path = TSA_PATH_SHORT;
+    pl->cluster = 1;
     return TSA_OK;
   }
   if (c->dtype == TSA_BF16 && tc_supported(c->d_k, c->n_terms)) {
@@ -226,6 +228,21 @@ tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl
     if (tc_slicing(c->d_k, c->n_terms, c->d_v, &ts)) {
       if (c->chunk != 0 && c->chunk != 128)
         return fail(TSA_ERR_UNSUPPORTED, "chunk=%d not built for bf16 (0 or 128)", c->chunk);
+      // a state that one CTA holds only in value slices: a CTA pair holds it
+      // whole, each CTA half of its feature blocks (prefill_pair.cuh)
+      int cs = 1;
+      size_t psmem = 0;
+      if (ts.n_slices > 1 && pair_fits(c->d_k, c->n_terms, c->d_v, &cs, &psmem) && cs == 2) {
+        TcSlicing tp = ts;
+        tp.n_slices = cs;   // CTAs per (head, span), for the cost of the plan
+        tp.w[0] = c->d_v;
+        tp.smem = psmem;
+        tsa_status st = make_plan_tc(c, N, num_sms, tp, pl, TSA_PATH_TC);
+        pl->n_slices = 1;
+        pl->slice_width = c->d_v;
+        pl->cluster = cs;
+        return st;
+      }
       return make_plan_tc(c, N, num_sms, ts, pl, TSA_PATH_TC);
     }
   }
@@ -274,6 +291,7 @@ tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl
   pl->scratch_bytes = best_s > 1 ? (size_t)heads * best_s * state_floats_per_head(c) * 4 : 0;
   pl->launches = best_s > 1 ? 3 : 1;
   pl->path = TSA_PATH_SIMT;
+  pl->cluster = 1;
   return TSA_OK;
 }
 
@@ -325,7 +343,8 @@ static tsa_status dispatch_prefill(const tsa_config* c, const tsa_plan& pl, Pref
 tsa_status launch_prefill(const tsa_config* c, const tsa_plan& pl, PrefillParams p,
                           cudaStream_t s) {
   if (pl.path == TSA_PATH_SHORT) return launch_prefill_short(c, p, s);
-  if (pl.path == TSA_PATH_TC) return launch_prefill_tc(c, pl, p, s);
+  if (pl.path == TSA_PATH_TC)
+    return pl.cluster == 2 ? launch_prefill_pair(c, pl, p, s) : launch_prefill_tc(c, pl, p, s);
   if (pl.path == TSA_PATH_TC_F32) return launch_prefill_tc32(c, pl, p, s);
   return (c->dtype == TSA_F32) ? dispatch_prefill<float>(c, pl, p, s)
                                : dispatch_prefill<__nv_bfloat16>(c, pl, p, s);

@@ -35,6 +35,13 @@ struct TcSlicing {
 bool tc_supported(int dk, int nt);
 bool tc_slicing(int dk, int nt, int dv, TcSlicing* ts);
 tsa_status launch_prefill_tc(const tsa_config* c, const tsa_plan& pl, const PrefillParams& p, cudaStream_t s);
+// The span-state pass and scan of a multi-span bf16 plan (value-sliced).
+tsa_status launch_span_states_tc(int dk, int nt, const tsa_plan& pl, const PrefillParams& p, cudaStream_t s);
+// bf16 prefill with the head state shared by a cluster of CTAs
+// (prefill_pair.cu): whether a layout exists, its CTAs per (head, span) and
+// its shared memory.
+bool pair_fits(int dk, int nt, int dv, int* cs, size_t* smem);
+tsa_status launch_prefill_pair(const tsa_config* c, const tsa_plan& pl, const PrefillParams& p, cudaStream_t s);
 tsa_status device_error_word(int** out);
 // The testing hooks' current settings: the bound of each wait and whether
 // the fp32 output pass withholds its first publication.

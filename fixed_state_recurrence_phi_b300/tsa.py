@@ -43,7 +43,7 @@ class TsaPlan(ctypes.Structure):
                 ("n_spans", ctypes.c_int), ("chunks_per_span", ctypes.c_int),
                 ("ctas_per_sm", ctypes.c_int), ("launches", ctypes.c_int),
                 ("smem_bytes", ctypes.c_size_t), ("scratch_bytes", ctypes.c_size_t),
-                ("path", ctypes.c_int)]
+                ("path", ctypes.c_int), ("cluster", ctypes.c_int)]
 
 
 class TsaError(RuntimeError):

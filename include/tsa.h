@@ -125,6 +125,9 @@ typedef struct {
   size_t smem_bytes;
   size_t scratch_bytes;
   int path;
+  int cluster;      /* CTAs that share one (head, span): 1, or 2 when the bf16
+                       head state is too large for one SM's tensor memory and
+                       its feature blocks are divided between a CTA pair */
 } tsa_plan;
 
 tsa_status tsa_prefill_plan(const tsa_config* cfg, int64_t N, int num_sms, tsa_plan* out);

@@ -57,8 +57,9 @@ def test_tc_ragged_lengths(G, N):
 
 
 @pytest.mark.parametrize("d,dv,n,N", [
-    (16, 64, 4, 700),     # 8 feature blocks, two value slices of 32
-    (32, 128, 3, 600),    # 5 feature blocks, three value slices
+    (16, 64, 4, 700),     # 8 feature blocks: a CTA pair, 4 blocks each
+    (32, 128, 3, 600),    # 5 feature blocks: a CTA pair, the last block split by columns
+    (32, 64, 3, 450),     # the same split at d_v 64
     (16, 128, 3, 500),    # one slice of 128 (+ the normaliser group: N = 144)
     (32, 32, 2, 400),     # one feature block
     (16, 32, 1, 300),     # n = 1: a running mean
@@ -78,10 +79,49 @@ def test_tc_multi_span(G):
 
 
 def test_tc_multi_span_multi_slice_order4(G):
+    """Order 4 with few heads: the value-sliced span pass and the scan, then
+    the CTA-pair output pass starting each span from its prefix."""
     cfg = G.T.Config(1, 1, 16, 64, 4, "bf16")
     plan = G.T.prefill_plan(cfg, 5000)
-    assert plan["n_spans"] > 1 and plan["n_slices"] == 2
+    assert plan["n_spans"] > 1 and plan["cluster"] == 2
     _check_all_heads(G, cfg, 5000, seed=32, chunked=256)
+
+
+def test_pair_plans(G):
+    """The heads whose state one SM's tensor memory holds only in value slices
+    are shared by a CTA pair: order 4 at d_k 16 (8 feature blocks, 4 each),
+    d_k 32 (5 blocks: 2 each and the last split by columns)."""
+    T = G.T
+    for d, dv, n in [(16, 64, 4), (32, 128, 3), (32, 64, 3)]:
+        p = T.prefill_plan(T.Config(4, 16, d, dv, n, "bf16"), 32768)
+        assert p["path"] == T.TSA_PATH_TC and p["cluster"] == 2 and p["n_slices"] == 1, (d, dv, n, p)
+    for d, dv, n in [(16, 64, 3), (16, 128, 3), (32, 32, 3)]:
+        assert T.prefill_plan(T.Config(4, 16, d, dv, n, "bf16"), 32768)["cluster"] == 1
+
+
+@pytest.mark.parametrize("d,dv,n,N", [
+    (16, 64, 4, 1), (16, 64, 4, 127), (16, 64, 4, 129), (16, 64, 4, 385),
+    (32, 128, 3, 1), (32, 128, 3, 200), (32, 64, 3, 500), (32, 64, 3, 129),
+])
+def test_pair_ragged(G, d, dv, n, N):
+    cfg = G.T.Config(1, 3, d, dv, n, "bf16")
+    _check_all_heads(G, cfg, N, seed=400 + d + dv + n + N)
+
+
+@pytest.mark.parametrize("d,dv,n", [(16, 64, 4), (32, 128, 3)])
+def test_pair_accumulate_continues_the_sequence(G, d, dv, n):
+    T, O = G.T, G.O
+    cfg = T.Config(1, 2, d, dv, n, "bf16")
+    q, k, v = G.make_inputs(cfg, 900, seed=35 + d)
+    sl = lambda x, a, b: x[:, :, a:b].contiguous()
+    _, st = G.gpu_prefill(cfg, sl(q, 0, 333), sl(k, 0, 333), sl(v, 0, 333))
+    out2, st = G.gpu_prefill(cfg, sl(q, 333, 900), sl(k, 333, 900), sl(v, 333, 900), states=st,
+                             accumulate=True)
+    Sg = G.canonical(cfg, st)
+    qh, kh, vh = G.host(q), G.host(k), G.host(v)
+    for h in range(2):
+        o_r, S_r = O.prefill_recurrent(qh[0, h], kh[0, h], vh[0, h], n)
+        G.check_head(cfg, G.host(out2)[0, h], Sg[0, h], o_r[333:], S_r, G.TOL["bf16"], "accumulate")
 
 
 def test_tc_accumulate_continues_the_sequence(G):
