@@ -94,6 +94,94 @@ __device__ __forceinline__ uint4 feat8(const float (&x)[DK + 1]) {
   return r;
 }
 
+// ---- the same features from the packed bf16 inputs ---------------------------
+// A token's inputs as they arrive, two bf16 per 32-bit word: xp[e] holds
+// x[2e] (low half) and x[2e + 1] (high half); x0 is the value of the order-0
+// feature (1, or 0 for a masked token). Only these words live in registers:
+// an input's fp32 value is one shift or mask of its word, and the bf16 pair of
+// two inputs one byte permutation of their words, so a feature pair costs the
+// multiplier pair's conversion (shared along a run of monomials that differ
+// only in their last index), at most one permutation and one bf16x2
+// multiply. Results are bitwise equal to feat2: the multiplier is still
+// formed in fp32 and rounded once, and the pair holds the same bf16 inputs.
+
+template <int I>
+__device__ __forceinline__ float in_f32(const uint32_t* xp) {
+  return __uint_as_float((I % 2) ? (xp[I / 2] & 0xFFFF0000u) : (xp[I / 2] << 16));
+}
+
+// Index of the last input factor of feature A (-1: the order-0 feature, or
+// past the end) and whether its multiplier is exactly 1 (order 1).
+template <int DK, int NT, int A>
+struct FeatY {
+  using FC = FeatConst<DK, NT>;
+  static constexpr bool live = A < FC::D;
+  static constexpr uint32_t cd = live ? FC::tab.code[A] : 0u;
+  static constexpr int i = cd & 255, j = (cd >> 8) & 255, l = (cd >> 16) & 255;
+  static constexpr int y = (!live || i == DK) ? -1 : (j == DK ? i : (l == DK ? j : l));
+  static constexpr bool unit_m = live && i != DK && j == DK;
+};
+
+// Multiplier m of feature A (the monomial without its last input factor, with
+// the weight), in fp32.
+template <int DK, int NT, int A>
+__device__ __forceinline__ float feat_m(const uint32_t* xp, float x0) {
+  using Y = FeatY<DK, NT, A>;
+  if constexpr (!Y::live) {
+    return 0.0f;
+  } else {
+    constexpr float w = FeatConst<DK, NT>::tab.w[A];
+    if constexpr (Y::i == DK) return x0;
+    else if constexpr (Y::j == DK) return 1.0f;
+    else if constexpr (Y::l == DK) return (w == 1.0f) ? in_f32<Y::i>(xp) : in_f32<Y::i>(xp) * w;
+    else if constexpr (w == 1.0f) return in_f32<Y::i>(xp) * in_f32<Y::j>(xp);
+    else return (in_f32<Y::i>(xp) * in_f32<Y::j>(xp)) * w;
+  }
+}
+
+// The bf16 pair (y_a, y_b) of the last input factors (y = -1: the value 1).
+template <int YA, int YB>
+__device__ __forceinline__ uint32_t in_pair(const uint32_t* xp) {
+  if constexpr (YA >= 0 && YB == YA + 1 && YA % 2 == 0) {
+    return xp[YA / 2];
+  } else if constexpr (YA >= 0 && YB >= 0) {
+    constexpr uint32_t sel = ((YB % 2) ? 0x7600u : 0x5400u) | ((YA % 2) ? 0x32u : 0x10u);
+    return __byte_perm(xp[YA / 2], xp[YB / 2], sel);
+  } else {
+    const uint32_t lo = (YA >= 0) ? (((YA % 2) ? (xp[YA / 2] >> 16) : xp[YA / 2]) & 0xFFFFu) : 0x3F80u;
+    const uint32_t hi = (YB >= 0) ? (((YB % 2) ? (xp[YB / 2] >> 16) : xp[YB / 2]) & 0xFFFFu) : 0x3F80u;
+    return lo | (hi << 16);
+  }
+}
+
+template <int DK, int NT, int A>
+__device__ __forceinline__ uint32_t feat2p(const uint32_t* xp, float x0) {
+  using Ya = FeatY<DK, NT, A>;
+  using Yb = FeatY<DK, NT, A + 1>;
+  if constexpr (!Ya::live) {
+    return 0u;
+  } else if constexpr (Ya::unit_m && (Yb::unit_m || !Yb::live)) {
+    // order 1: the inputs themselves
+    return Yb::live ? in_pair<Ya::y, Yb::y>(xp) : (in_pair<Ya::y, Ya::y>(xp) & 0xFFFFu);
+  } else {
+    const uint32_t m = tc::pack_bf16x2(feat_m<DK, NT, A>(xp, x0), feat_m<DK, NT, A + 1>(xp, x0));
+    const uint32_t y = in_pair<Ya::y, (Yb::live ? Yb::y : -1)>(xp);
+    const __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&m),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&y));
+    return *reinterpret_cast<const uint32_t*>(&r);
+  }
+}
+
+template <int DK, int NT, int A>
+__device__ __forceinline__ uint4 feat8p(const uint32_t* xp, float x0) {
+  uint4 r;
+  r.x = feat2p<DK, NT, A + 0>(xp, x0);
+  r.y = feat2p<DK, NT, A + 2>(xp, x0);
+  r.z = feat2p<DK, NT, A + 4>(xp, x0);
+  r.w = feat2p<DK, NT, A + 6>(xp, x0);
+  return r;
+}
+
 // Write the G groups of 8 features starting at A0 (a multiple of 8) for one
 // token into its row of the feature tile: `row` points at the token's row,
 // 8-feature groups 128 bytes apart.

@@ -170,27 +170,37 @@ __device__ __forceinline__ bool pr_wait_warp(const PairBars& B, uint64_t* bar, u
 // 32 features (block F, features 32G .. 32G + 31) of one token as 4 groups of
 // 8 bf16, stored 128 bytes apart from `dst`.
 template <int DK, int NT, int F, int G>
-__device__ __forceinline__ void pr_phi32(const float (&x)[DK + 1], uint8_t* dst) {
+__device__ __forceinline__ void pr_phi32(const uint32_t* xp, float x0, uint8_t* dst) {
   constexpr int A = F * 128 + 32 * G;
-  *reinterpret_cast<uint4*>(dst + 0) = feat8<DK, NT, A + 0>(x);
-  *reinterpret_cast<uint4*>(dst + 128) = feat8<DK, NT, A + 8>(x);
-  *reinterpret_cast<uint4*>(dst + 256) = feat8<DK, NT, A + 16>(x);
-  *reinterpret_cast<uint4*>(dst + 384) = feat8<DK, NT, A + 24>(x);
+  *reinterpret_cast<uint4*>(dst + 0) = feat8p<DK, NT, A + 0>(xp, x0);
+  *reinterpret_cast<uint4*>(dst + 128) = feat8p<DK, NT, A + 8>(xp, x0);
+  *reinterpret_cast<uint4*>(dst + 256) = feat8p<DK, NT, A + 16>(xp, x0);
+  *reinterpret_cast<uint4*>(dst + 384) = feat8p<DK, NT, A + 24>(xp, x0);
 }
 // Runtime (block f, quarter g) -> instantiation; one call site per kernel.
 template <int DK, int NT, int F = 0>
-__device__ __forceinline__ void pr_build32(int f, int g, const float (&x)[DK + 1], uint8_t* dst) {
+__device__ __forceinline__ void pr_build32(int f, int g, const uint32_t* xp, float x0, uint8_t* dst) {
   if constexpr (F < FeatConst<DK, NT>::NB) {
     if (f == F) {
       switch (g) {
-        case 0: pr_phi32<DK, NT, F, 0>(x, dst); break;
-        case 1: pr_phi32<DK, NT, F, 1>(x, dst); break;
-        case 2: pr_phi32<DK, NT, F, 2>(x, dst); break;
-        default: pr_phi32<DK, NT, F, 3>(x, dst); break;
+        case 0: pr_phi32<DK, NT, F, 0>(xp, x0, dst); break;
+        case 1: pr_phi32<DK, NT, F, 1>(xp, x0, dst); break;
+        case 2: pr_phi32<DK, NT, F, 2>(xp, x0, dst); break;
+        default: pr_phi32<DK, NT, F, 3>(xp, x0, dst); break;
       }
       return;
     }
-    pr_build32<DK, NT, F + 1>(f, g, x, dst);
+    pr_build32<DK, NT, F + 1>(f, g, xp, x0, dst);
+  }
+}
+
+// A token's d inputs from a [e/8][t][8] bf16 tile, as packed bf16 pairs.
+template <int DK>
+__device__ __forceinline__ void pr_load_xp(const uint8_t* tile, int t, uint32_t (&xp)[DK / 2]) {
+#pragma unroll
+  for (int g = 0; g < DK / 8; ++g) {
+    const uint4 u = *reinterpret_cast<const uint4*>(tile + g * 2048 + t * 16);
+    xp[4 * g] = u.x; xp[4 * g + 1] = u.y; xp[4 * g + 2] = u.z; xp[4 * g + 3] = u.w;
   }
 }
 
@@ -227,6 +237,7 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
   const int ntile = p.ntile[r];
   const int zc = p.zc, nm = p.nm, dv = p.dv;
   const size_t st_elems = (size_t)DPAD * (dv + 1);
+  TSA_TRACE_DECL
 
   if (warp == 0) tc::tmem_alloc(B.tmem_slot(), 512);
   if (tid == 0) {
@@ -307,16 +318,14 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
       const bool need_update = single || has_next;
       const int vb = c % p.nvbuf;
       // P of this chunk is written (so Q K^T of this chunk is done)
+      TSA_TRACE_EVENT(100, c);
       if (!(ok = pr_wait_warp(B, B.pready(), c & 1u))) break;
+      TSA_TRACE_EVENT(101, c);
       tc::fence_after_sync();
-      // the next chunk's q, k: their buffer's previous users are done
-      if (has_next) {
-        const int nb = (c + 1) % p.nqk;
-        if (p.nqk == 1) {
-          if (!(ok = pr_wait_warp(B, B.qkempty(0), c & 1u))) break;
-        } else if (c >= 1) {
-          if (!(ok = pr_wait_warp(B, B.qkempty(nb), ((c - 1) >> 1) & 1u))) break;
-        }
+      // the next chunk's q, k into the other buffer (two buffers): the builders
+      // have finished chunk c - 1, the buffer's previous user
+      if (has_next && p.nqk == 2) {
+        if (c >= 1 && !(ok = pr_wait_warp(B, B.qkempty((c + 1) & 1), ((c - 1) >> 1) & 1u))) break;
         load_qk(c + 1);
       }
       // the next chunk's v into the other buffer (two buffers): chunk c-1 is done
@@ -331,6 +340,7 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
       for (int t = 0; t < ntile && ok; ++t) {
         const PairTile& T = p.tile[r][t];
         if (!(ok = pr_wait_warp(B, B.conv(t), c & 1u))) break;
+        TSA_TRACE_EVENT(103, t);
         tc::fence_after_sync();
         const uint32_t id_ro = tc::idesc_bf16(128, T.w, false, true);
         const uint64_t dS = tc::sdesc(aS + (uint32_t)T.s_off, 128, (uint32_t)T.ro_rows * 16);
@@ -363,8 +373,10 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
         tc::mma_commit_elect(B.pvdone());
       }
       if (!(p.dbg_withhold && c == 0)) tc::mma_commit_elect(B.odone());
-      // separate score columns: the next chunk's Q K^T now
-      if (has_next && !p.shared_o) {
+      TSA_TRACE_EVENT(106, c);
+      // separate score columns and the next chunk's q, k already loaded (two
+      // buffers): its Q K^T now
+      if (has_next && !p.shared_o && p.nqk == 2) {
         if (!(ok = pr_wait_warp(B, B.qkfull((c + 1) % p.nqk), ((c + 1) / p.nqk) & 1u))) break;
         ++qk_got;
         tc::fence_after_sync();
@@ -394,9 +406,15 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
         if (!ok) break;
       }
       tc::mma_commit_elect(B.chunk());
-      if (has_next && p.shared_o) {
-        // the scores go where O is: after O has been read out
-        if (!(ok = pr_wait_warp(B, B.ofree(), c & 1u))) break;
+      TSA_TRACE_EVENT(109, c);
+      // one q, k buffer: the next chunk's once the builders are done with this one
+      if (has_next && p.nqk == 1) {
+        if (!(ok = pr_wait_warp(B, B.qkempty(0), c & 1u))) break;
+        load_qk(c + 1);
+      }
+      if (has_next && (p.shared_o || p.nqk == 1)) {
+        // shared columns: the scores go where O is, after O has been read out
+        if (p.shared_o && !(ok = pr_wait_warp(B, B.ofree(), c & 1u))) break;
         if (!(ok = pr_wait_warp(B, B.qkfull((c + 1) % p.nqk), ((c + 1) / p.nqk) & 1u))) break;
         ++qk_got;
         tc::fence_after_sync();
@@ -524,11 +542,13 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
         tc::fence_proxy_async();
         for (int t = 0; t < ntile; ++t) tc_warp_arrive(B.conv(t), lane);
         if (!(ok = compute_p(0, valid))) break;
-      } else if (p.shared_o) {
+      } else if (p.shared_o || p.nqk == 1) {
         if (!(ok = compute_p(c, valid))) break;
       }
       // ---- the output of chunk c
+      TSA_TRACE_EVENT(201, c);
       if (!(ok = pr_wait_warp(B, B.odone(), c & 1u))) break;
+      TSA_TRACE_EVENT(202, c);
       tc::fence_after_sync();
       if (p.cs == 1 || own_rows) {
         float inv;
@@ -591,8 +611,9 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
       }
       tc::fence_before_sync();
       tc_warp_arrive(B.ofree(), lane);
-      // ---- separate score columns: the next chunk's P now
-      if (has_next && !p.shared_o) {
+      TSA_TRACE_EVENT(204, c);
+      // ---- separate score columns, Q K^T issued early: the next chunk's P now
+      if (has_next && !p.shared_o && p.nqk == 2) {
         const int valid1 = (int)min((long long)TC_C, t_end - (t0 + TC_C));
         if (!(ok = compute_p(c + 1, valid1))) break;
       }
@@ -609,11 +630,19 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
     }
   } else if (warp < PR_ISSUER_WARP) {
     // --------------------------- builder warps ------------------------------
+    // One pass over the chunk's ring uses: the readout tiles of each tile's
+    // block (64-feature halves; token t, quarter 2h + qr), then its two update
+    // tiles (64 tokens each; token 64h + tq, quarter qq). The token's inputs are
+    // read from the q / k tile for each use (nothing is kept across uses, which
+    // keeps the builders clear of register spills), and the q, k buffer is
+    // released after the chunk's last use.
     const int bt = tid - PR_BUILDER0;
-    const int t = bt & 127, qr = bt >> 7;         // readout: token t, quarter 2h + qr of the block
-    const int tq = bt & 63, qq = bt >> 6;         // update: token 64h + tq, quarter qq
-    const int ro_row = (t / 8) * 1024 + (t % 8) * 16;
-    const int up_row = (tq / 8) * 2048 + (tq % 8) * 16;
+    const int t = bt & 127, qr = bt >> 7;
+    const int tq = bt & 63, qq = bt >> 6;
+    const int ro_row = (t / 8) * 1024 + (t % 8) * 16 + (4 * qr) * 128;
+    const int up_row = (tq / 8) * 2048 + (tq % 8) * 16 + (4 * qq) * 128;
+    int n_ro = 0;
+    for (int tt = 0; tt < ntile; ++tt) n_ro += pr_ro_halves(p.tile[r][tt].ro_rows);
     PrRing ring;
     ring.n = p.ring;
     for (int c = 0; c < n_chunks; ++c) {
@@ -621,53 +650,40 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
       const int valid = (int)min((long long)TC_C, t_end - t0);
       const bool need_update = single || (c + 1 < n_chunks);
       const int qb = c % p.nqk;
+      TSA_TRACE_EVENT(300, c);
       if (!pr_wait_warp(B, B.qkfull(qb), (c / p.nqk) & 1u)) break;
-      float xq[DK + 1], xk[2][DK + 1];
-      tc_load_x<DK>(smem + p.off_q + qb * p.qsz, t, xq);
-      tc_load_x<DK>(smem + p.off_k + qb * p.qsz, tq, xk[0]);
-      tc_load_x<DK>(smem + p.off_k + qb * p.qsz, 64 + tq, xk[1]);
-      xq[DK] = 1.0f;
-      xk[0][DK] = (tq < valid) ? 1.0f : 0.0f;
-      xk[1][DK] = (64 + tq < valid) ? 1.0f : 0.0f;
-      tc_warp_arrive(B.qkempty(qb), lane);
+      TSA_TRACE_EVENT(301, c);
+      const uint8_t* qtile = smem + p.off_q + qb * p.qsz;
+      const uint8_t* ktile = smem + p.off_k + qb * p.qsz;
+      const int nuse = n_ro + (need_update ? 2 * ntile : 0);
       bool ok = true;
-      auto acquire = [&]() -> bool {
+      int tt = 0, h = 0;
+      for (int u = 0; u < nuse; ++u) {
+        const bool upd = u >= n_ro;
+        if (u == n_ro) { tt = 0; h = 0; }
+        const PairTile& T = p.tile[r][tt];
         if ((ring.used >> ring.s) & 1u) {
-          if (!pr_wait_warp(B, B.rempty(ring.s), (ring.ph >> ring.s) & 1u)) return false;
+          if (!(ok = pr_wait_warp(B, B.rempty(ring.s), (ring.ph >> ring.s) & 1u))) break;
           ring.ph ^= 1u << ring.s;
         }
-        return true;
-      };
-      auto release = [&]() {
+        TSA_TRACE_EVENT(302, ring.s);
+        const int tok = upd ? 64 * h + tq : t;
+        if (upd || 64 * h + 32 * qr < T.ro_rows) {
+          uint32_t xp[DK / 2];
+          pr_load_xp<DK>(upd ? ktile : qtile, tok, xp);
+          const float x0 = (!upd || tok < valid) ? 1.0f : 0.0f;
+          pr_build32<DK, NT>(T.blk, upd ? qq : 2 * h + qr, xp, x0,
+                             smem + p.off_ring + ring.s * 16384 + (upd ? up_row : ro_row));
+        }
         tc::fence_proxy_async();
         tc_warp_arrive(B.rfull(ring.s), lane);
+        TSA_TRACE_EVENT(303, ring.s);
         ring.used |= 1u << ring.s;
         ring.s = (ring.s + 1 == ring.n) ? 0 : ring.s + 1;
-      };
-      for (int tt = 0; tt < p.ntile[r] && ok; ++tt) {
-        const PairTile& T = p.tile[r][tt];
-        for (int h = 0; h < pr_ro_halves(T.ro_rows); ++h) {
-          if (!(ok = acquire())) break;
-          if (64 * h + 32 * qr < T.ro_rows)
-            pr_build32<DK, NT>(T.blk, 2 * h + qr, xq, smem + p.off_ring + ring.s * 16384 + ro_row + (4 * qr) * 128);
-          release();
-        }
+        if (++h == (upd ? 2 : pr_ro_halves(T.ro_rows))) { h = 0; ++tt; }
       }
       if (!ok) break;
-      if (need_update) {
-        for (int tt = 0; tt < p.ntile[r] && ok; ++tt) {
-          const PairTile& T = p.tile[r][tt];
-          for (int h = 0; h < 2; ++h) {
-            if (!(ok = acquire())) break;
-            float x[DK + 1];
-#pragma unroll
-            for (int e = 0; e <= DK; ++e) x[e] = h ? xk[1][e] : xk[0][e];
-            pr_build32<DK, NT>(T.blk, qq, x, smem + p.off_ring + ring.s * 16384 + up_row + (4 * qq) * 128);
-            release();
-          }
-        }
-        if (!ok) break;
-      }
+      tc_warp_arrive(B.qkempty(qb), lane);
     }
   }
   tc::fence_before_sync();
