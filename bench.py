@@ -483,8 +483,9 @@ def _run_ours(args, clk):
           tc_lines.append({
               "workload": tw["workload"], "N": tw["N"], "ms": tms,
               "tokens_per_s": ws * tw["B"] * tw["N"] / (tms / 1e3),
-              "path": "tensor cores (tcgen05, bf16 in, fp32 TMEM accumulators)" if tplan["path"] == 1 else "simt",
-              "plan": {k2: tplan[k2] for k2 in ("chunk", "n_slices", "slice_width", "n_spans", "launches")},
+              "path": ("tensor cores (tcgen05, bf16 in, fp32 TMEM accumulators"
+                       + (", CTA pairs" if tplan["cluster"] == 2 else "") + ")") if tplan["path"] == 1 else "simt",
+              "plan": {k2: tplan[k2] for k2 in ("chunk", "n_slices", "slice_width", "n_spans", "launches", "cluster")},
               "roofline": {"bound": "tensor", "achieved": ach, "peak": pk_burst, "unit": "TFLOP/s",
                            "frac": ach / pk_burst, "frac_of_sustained": ach / pk_sust,
                            "peak_source": f"{pk_src} cuBLAS bf16 (burst; sustained {pk_sust})",
