@@ -70,6 +70,55 @@ tsa_status make_tmap32(CUtensorMap* m, const void* base, int inner, long long N,
   return TSA_OK;
 }
 
+// The span pass (each span's state sum into the scratch) and the exclusive
+// scan over spans, which also writes the final state. The pass takes its own
+// layout (three ring slots where that fits), or the output pass's (`smem`)
+// where its own does not fit.
+template <int DK, int NT>
+tsa_status span_pass32(const tsa_plan& pl, const PrefillParams& pp, const TcParams& p, int smem,
+                       const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t s) {
+  using S = Tc32Shape<DK, NT>;
+  const unsigned grid = (unsigned)((long long)pp.heads * pl.n_spans);
+  TcParams ps = p;
+  int smem_s = smem;
+  if (smem_tc32_span<DK, NT>(pp.dv, 2) <= kSmemLimit) {
+    ps.span_layout = 1;
+    ps.ring = (smem_tc32_span<DK, NT>(pp.dv, 3) <= kSmemLimit) ? 3 : 2;
+    smem_s = (int)smem_tc32_span<DK, NT>(pp.dv, ps.ring);
+  }
+  cudaError_t e = set_smem_once((const void*)span_state_tc32_kernel<DK, NT>, smem_s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_state_tc32)");
+  span_state_tc32_kernel<DK, NT><<<grid, TC_THREADS, smem_s, s>>>(ps, mk, mv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch span_state_tc32");
+  const int elems4 = (int)(round_up(S::D, 4) * (pp.dv + 1) / 4);
+  e = launch_span_scan(pp.states, pp.scratch, pp.heads, pl.n_spans, elems4, pp.accumulate, s);
+  if (e != cudaSuccess) return cuda_fail(e, "launch span_scan");
+  return TSA_OK;
+}
+
+// The final state only (tsa_prefill_states): span pass and scan, any number
+// of spans.
+template <int DK, int NT>
+tsa_status states32(const tsa_plan& pl, const PrefillParams& pp, cudaStream_t s) {
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  p.states = pp.states; p.scratch = pp.scratch;
+  p.N = pp.N; p.heads = pp.heads; p.dv = pp.dv; p.n_spans = pl.n_spans;
+  p.chunks_per_span = pl.chunks_per_span; p.accumulate = pp.accumulate;
+  p.n_slices = 1; p.nmax = pp.dv + 16;
+  p.slice_c0[0] = 0; p.slice_w[0] = pp.dv;
+  p.ring = (smem_tc32<DK, NT>(pp.dv, 3) <= kSmemLimit) ? 3 : 2;
+  const int smem = (int)smem_tc32<DK, NT>(pp.dv, p.ring);
+  tc_debug_params(&p.wait_ns, &p.dbg_withhold);
+  tsa_status st = device_error_word(&p.err);
+  if (st != TSA_OK) return st;
+  CUtensorMap mk, mv;
+  if ((st = make_tmap32(&mk, pp.k, DK, pp.N, pp.heads, DK)) != TSA_OK) return st;
+  if ((st = make_tmap32(&mv, pp.v, pp.dv, pp.N, pp.heads, pp.dv)) != TSA_OK) return st;
+  return span_pass32<DK, NT>(pl, pp, p, smem, mk, mv, s);
+}
+
 template <int DK, int NT>
 tsa_status launch32(const tsa_plan& pl, const PrefillParams& pp, cudaStream_t s) {
   using S = Tc32Shape<DK, NT>;
@@ -96,25 +145,7 @@ tsa_status launch32(const tsa_plan& pl, const PrefillParams& pp, cudaStream_t s)
     return st;
   const unsigned grid = (unsigned)((long long)pp.heads * pl.n_spans);
   cudaError_t e;
-  if (pl.n_spans > 1) {
-    // the span pass: its own layout (three ring slots where that fits), or
-    // the output pass's where its own does not fit
-    TcParams ps = p;
-    int smem_s = smem;
-    if (smem_tc32_span<DK, NT>(pp.dv, 2) <= kSmemLimit) {
-      ps.span_layout = 1;
-      ps.ring = (smem_tc32_span<DK, NT>(pp.dv, 3) <= kSmemLimit) ? 3 : 2;
-      smem_s = (int)smem_tc32_span<DK, NT>(pp.dv, ps.ring);
-    }
-    e = set_smem_once((const void*)span_state_tc32_kernel<DK, NT>, smem_s);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_state_tc32)");
-    span_state_tc32_kernel<DK, NT><<<grid, TC_THREADS, smem_s, s>>>(ps, mk, mv);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "launch span_state_tc32");
-    const int elems4 = (int)(round_up(S::D, 4) * (pp.dv + 1) / 4);
-    e = launch_span_scan(pp.states, pp.scratch, pp.heads, pl.n_spans, elems4, pp.accumulate, s);
-    if (e != cudaSuccess) return cuda_fail(e, "launch span_scan");
-  }
+  if (pl.n_spans > 1 && (st = span_pass32<DK, NT>(pl, pp, p, smem, mk, mv, s)) != TSA_OK) return st;
   e = set_smem_once((const void*)span_output_tc32_kernel<DK, NT>, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_output_tc32)");
   // after the scan: launched with a programmatic dependency, so that its
@@ -155,6 +186,15 @@ bool tc32_fits(int dk, int nt, int dv) {
 size_t tc32_smem(int dk, int nt, int dv) {
   const size_t s3 = smem_for(dk, nt, dv, 3);
   return (s3 > 0 && s3 <= kSmemLimit) ? s3 : smem_for(dk, nt, dv, 2);
+}
+
+tsa_status launch_states_tc32(const tsa_config* c, const tsa_plan& pl, const PrefillParams& p, cudaStream_t s) {
+#define TSA_S32_CASE(DK, NT) \
+  if (c->d_k == DK && c->n_terms == NT) return states32<DK, NT>(pl, p, s);
+  TSA_S32_CASE(16, 1) TSA_S32_CASE(16, 2) TSA_S32_CASE(16, 3) TSA_S32_CASE(16, 4)
+  TSA_S32_CASE(32, 1) TSA_S32_CASE(32, 2) TSA_S32_CASE(32, 3)
+#undef TSA_S32_CASE
+  return fail(TSA_ERR_UNSUPPORTED, "no fp32 tensor-core span pass for d_k=%d n=%d", c->d_k, c->n_terms);
 }
 
 tsa_status launch_prefill_tc32(const tsa_config* c, const tsa_plan& pl, const PrefillParams& p, cudaStream_t s) {

@@ -338,6 +338,85 @@ static tsa_status dispatch_prefill(const tsa_config* c, const tsa_plan& pl, Pref
   return fail(TSA_ERR_UNSUPPORTED, "no prefill kernel for d_k=%d n=%d", c->d_k, c->n_terms);
 }
 
+// ---------------------------------------------------------------------------
+// The final state only (tsa_prefill_states): the span pass of the prefill
+// path and the scan over spans, no outputs.
+// ---------------------------------------------------------------------------
+template <typename T, int DK, int NT, int W>
+static tsa_status launch_states_simt(const tsa_plan& pl, PrefillParams p, cudaStream_t s) {
+  using L = SimtLayout<DK, NT, W>;
+  const unsigned grid = (unsigned)((long long)p.heads * pl.n_slices * pl.n_spans);
+  cudaError_t e = set_smem_once((const void*)span_state_kernel<T, DK, NT, W>, (int)L::bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_state)");
+  span_state_kernel<T, DK, NT, W><<<grid, 256, L::bytes, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch span_state");
+  const int elems4 = (int)(L::DPAD * (p.dv + 1) / 4);
+  e = launch_span_scan(p.states, p.scratch, p.heads, pl.n_spans, elems4, p.accumulate, s);
+  if (e != cudaSuccess) return cuda_fail(e, "launch span_scan");
+  return TSA_OK;
+}
+
+template <typename T>
+static tsa_status dispatch_states_simt(const tsa_config* c, const tsa_plan& pl, PrefillParams p, cudaStream_t s) {
+#define TSA_ST_CASE(DK, NT)                                                  \
+  if (c->d_k == DK && c->n_terms == NT)                                      \
+    return pl.slice_width == 64 ? launch_states_simt<T, DK, NT, 64>(pl, p, s) \
+                                : launch_states_simt<T, DK, NT, 32>(pl, p, s);
+  TSA_ST_CASE(16, 1) TSA_ST_CASE(16, 2) TSA_ST_CASE(16, 3) TSA_ST_CASE(16, 4)
+  TSA_ST_CASE(32, 1) TSA_ST_CASE(32, 2) TSA_ST_CASE(32, 3)
+#undef TSA_ST_CASE
+  return fail(TSA_ERR_UNSUPPORTED, "no span pass for d_k=%d n=%d", c->d_k, c->n_terms);
+}
+
+// The plan of a states-only call: the span pass of the tensor-core path for
+// the dtype where it applies (bf16: value-sliced; fp32: split operands), else
+// the CUDA-core span pass; spans enough to give every SM a CTA (the pass has
+// no output part, so more spans cost only the scan's share).
+tsa_status make_states_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl) {
+  memset(pl, 0, sizeof(*pl));
+  const long long heads = (long long)c->B * c->H;
+  int chunk = 64, n_slices = 1, slice_w = c->d_v, path = TSA_PATH_SIMT;
+  size_t smem = 0;
+  TcSlicing ts;
+  if (c->dtype == TSA_BF16 && tc_supported(c->d_k, c->n_terms) && tc_slicing(c->d_k, c->n_terms, c->d_v, &ts)) {
+    chunk = 128; n_slices = ts.n_slices; slice_w = ts.nmax - 16; path = TSA_PATH_TC; smem = ts.smem;
+  } else if (c->dtype == TSA_F32 && tc32_fits(c->d_k, c->n_terms, c->d_v)) {
+    chunk = 128; path = TSA_PATH_TC_F32; smem = tc32_smem(c->d_k, c->n_terms, c->d_v);
+  } else {
+    const int W = (c->d_v % 64 == 0 && simt_smem_bytes(c->d_k, c->n_terms, 64) <= kSmemLimit) ? 64 : 32;
+    smem = simt_smem_bytes(c->d_k, c->n_terms, W);
+    if (smem == 0 || smem > kSmemLimit) return fail(TSA_ERR_UNSUPPORTED, "no kernel fits shared memory");
+    slice_w = W;
+    n_slices = c->d_v / W;
+  }
+  const long long n_chunks = (N + chunk - 1) / chunk;
+  const long long units = heads * n_slices;
+  long long spans = std::max<long long>(1, std::min<long long>(n_chunks, (std::max(1, num_sms) + units - 1) / units));
+  while (spans > 1 && (double)heads * spans * state_floats_per_head(c) * 4.0 > (double)(1ull << 30)) --spans;
+  const long long cps = n_chunks > 0 ? (n_chunks + spans - 1) / spans : 0;
+  spans = cps > 0 ? (n_chunks + cps - 1) / cps : 1;
+  pl->chunk = chunk;
+  pl->slice_width = slice_w;
+  pl->n_slices = n_slices;
+  pl->n_spans = (int)spans;
+  pl->chunks_per_span = (int)cps;
+  pl->ctas_per_sm = 1;
+  pl->launches = 2;
+  pl->smem_bytes = smem;
+  pl->scratch_bytes = (size_t)heads * spans * state_floats_per_head(c) * 4;
+  pl->path = path;
+  pl->cluster = 1;
+  return TSA_OK;
+}
+
+tsa_status launch_states(const tsa_config* c, const tsa_plan& pl, PrefillParams p, cudaStream_t s) {
+  if (pl.path == TSA_PATH_TC) return launch_span_states_tc(c->d_k, c->n_terms, pl, p, s);
+  if (pl.path == TSA_PATH_TC_F32) return launch_states_tc32(c, pl, p, s);
+  return (c->dtype == TSA_F32) ? dispatch_states_simt<float>(c, pl, p, s)
+                               : dispatch_states_simt<__nv_bfloat16>(c, pl, p, s);
+}
+
 // Launch the prefill kernels of `pl` for either dtype (shared with the other
 // translation units of the library).
 tsa_status launch_prefill(const tsa_config* c, const tsa_plan& pl, PrefillParams p,
@@ -481,6 +560,45 @@ tsa_status tsa_prefill(const tsa_config* c, int64_t N, const void* q, const void
     if (st == TSA_OK) st = st2;
   }
   return st;
+}
+
+tsa_status tsa_prefill_states(const tsa_config* c, int64_t N, const void* k, const void* v, float* states,
+                              unsigned flags, void* stream) {
+  NvtxRange nvtx_range("tsa_prefill_states");
+  tsa_status st = check_config(c);
+  if (st != TSA_OK) return st;
+  if (N < 0) return fail(TSA_ERR_INVALID, "N must be >= 0 (got %lld)", (long long)N);
+  if (flags & ~TSA_PREFILL_ACCUMULATE) return fail(TSA_ERR_INVALID, "unknown flags 0x%x", flags);
+  if (!states) return fail(TSA_ERR_INVALID, "states is NULL");
+  if (!aligned16(states)) return fail(TSA_ERR_INVALID, "states not 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool acc = (flags & TSA_PREFILL_ACCUMULATE) != 0;
+  if (N == 0) {
+    if (!acc) {
+      cudaError_t e = cudaMemsetAsync(states, 0, tsa_state_bytes(c), s);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(states)");
+    }
+    return TSA_OK;
+  }
+  if (!k || !v) return fail(TSA_ERR_INVALID, "k and v must be non-NULL");
+  if (!aligned16(k) || !aligned16(v)) return fail(TSA_ERR_INVALID, "k and v must be 16-byte aligned");
+  const int sms = device_sm_count();
+  if (sms <= 0) return fail(TSA_ERR_CUDA, "no CUDA device");
+  tsa_plan pl;
+  st = make_states_plan(c, (long long)N, sms, &pl);
+  if (st != TSA_OK) return st;
+  PrefillParams p;
+  memset(&p, 0, sizeof(p));
+  p.k = k; p.v = v; p.states = states;
+  p.N = N; p.heads = c->B * c->H; p.dv = c->d_v; p.n_slices = pl.n_slices;
+  p.n_spans = pl.n_spans; p.chunks_per_span = pl.chunks_per_span; p.accumulate = acc ? 1 : 0;
+  void* scratch = nullptr;
+  st = scratch_alloc(&scratch, pl.scratch_bytes, s);
+  if (st != TSA_OK) return st;
+  p.scratch = static_cast<float*>(scratch);
+  st = launch_states(c, pl, p, s);
+  tsa_status st2 = scratch_free(scratch, s);
+  return st != TSA_OK ? st : st2;
 }
 
 tsa_status tsa_decode_step(const tsa_config* c, const void* q, const void* k, const void* v,

@@ -50,6 +50,11 @@ void tc_debug_params(unsigned long long* wait_ns, int* withhold);
 bool tc32_fits(int dk, int nt, int dv);
 size_t tc32_smem(int dk, int nt, int dv);
 tsa_status launch_prefill_tc32(const tsa_config* c, const tsa_plan& pl, const PrefillParams& p, cudaStream_t s);
+// The final state only: the fp32 span pass and the scan.
+tsa_status launch_states_tc32(const tsa_config* c, const tsa_plan& pl, const PrefillParams& p, cudaStream_t s);
+// Plan and launches of tsa_prefill_states (tsa_abi.cu).
+tsa_status make_states_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl);
+tsa_status launch_states(const tsa_config* c, const tsa_plan& pl, PrefillParams p, cudaStream_t s);
 tsa_status take_device_error();
 // Short-segment prefill, state resident in shared memory (prefill_short.cu).
 bool short_supported(int dk, int nt, int dv);

@@ -24,7 +24,7 @@ TSA_PATH_SIMT, TSA_PATH_TC, TSA_PATH_TC_F32, TSA_PATH_SHORT = 0, 1, 2, 3
 # Every symbol include/tsa.h declares (checked by the CPU test suite).
 EXPORTS = (
     "tsa_feature_dim", "tsa_state_pad_dim", "tsa_state_elems", "tsa_state_bytes",
-    "tsa_feature_index", "tsa_prefill_plan", "tsa_prefill", "tsa_prefill_noalloc",
+    "tsa_feature_index", "tsa_prefill_plan", "tsa_prefill", "tsa_prefill_noalloc", "tsa_prefill_states",
     "tsa_decode_step",
     "tsa_state_merge", "tsa_state_to_canonical", "tsa_sync_status",
     "tsa_status_string", "tsa_last_error",
@@ -67,6 +67,7 @@ def _load():
         "tsa_prefill_plan": (I, [C, I64, I, ctypes.POINTER(TsaPlan)]),
         "tsa_prefill": (I, [C, I64, P, P, P, P, P, U, P]),
         "tsa_prefill_noalloc": (I, [C, I64, P, P, P, P, P, U, P]),
+        "tsa_prefill_states": (I, [C, I64, P, P, P, U, P]),
         "tsa_decode_step": (I, [C, P, P, P, P, P, P]),
         "tsa_state_merge": (I, [C, P, P, P]),
         "tsa_state_to_canonical": (I, [C, P, P, P]),
@@ -178,6 +179,13 @@ def prefill_noalloc(cfg, N: int, q, k, v, out, states, accumulate: bool = False,
     _check("tsa_prefill_noalloc",
            _lib.tsa_prefill_noalloc(_cfg(cfg), int(N), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
                                     _ptr(states), flags, _stream(stream)))
+
+
+def prefill_states(cfg, N: int, k, v, states, accumulate: bool = False, stream=None):
+    """The state sum of N tokens (no outputs); see include/tsa.h."""
+    flags = TSA_PREFILL_ACCUMULATE if accumulate else 0
+    _check("tsa_prefill_states", _lib.tsa_prefill_states(_cfg(cfg), int(N), _ptr(k), _ptr(v), _ptr(states), flags,
+                                                         _stream(stream)))
 
 
 def decode_step(cfg, q, k, v, out, states, stream=None):

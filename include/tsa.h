@@ -172,6 +172,22 @@ tsa_status tsa_prefill_noalloc(const tsa_config* cfg, int64_t N, const void* q, 
                                const void* v, void* out, float* states, unsigned flags,
                                void* cuda_stream);
 
+/* The state after N tokens without the outputs: S (+)= sum_j phi(k_j) [v_j; 1]^T
+ * for every head (the state sum of a segment; states are additive across
+ * segments, abstract: "the states are additive across chunks, so prefill
+ * admits a parallel scan"). It is the first step of a prefill whose sequence
+ * is split over several devices: each device sums its own segment, the
+ * segment sums are exchanged, and each device then runs tsa_prefill on its
+ * segment with TSA_PREFILL_ACCUMULATE from the sum of the segments before it.
+ *  k : [B, H, N, d_k] dtype;  v : [B, H, N, d_v] dtype  (q is not needed)
+ *  states: as for tsa_prefill. Without TSA_PREFILL_ACCUMULATE it receives the
+ *          segment's sum; with it, the sum is added to what it holds.
+ * Runs the span-state pass of the prefill path and the scan over spans (two
+ * launches) with stream-ordered scratch from the library's pool. N = 0, errors
+ * and alignment as for tsa_prefill. */
+tsa_status tsa_prefill_states(const tsa_config* cfg, int64_t N, const void* k, const void* v,
+                              float* states, unsigned flags, void* cuda_stream);
+
 /* One decode token for every head, constant cost in the context length:
  *   S <- S + phi(k)[v; 1]^T;  out = (phi(q)^T S)[:d_v] / (phi(q)^T S)[d_v]
  *  q, k : [B, H, d_k] dtype;  v, out : [B, H, d_v] dtype;
