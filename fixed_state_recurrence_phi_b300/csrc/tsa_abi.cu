@@ -453,6 +453,27 @@ static tsa_status dispatch_decode(const tsa_config* c, DecodeParams p, cudaStrea
   return fail(TSA_ERR_UNSUPPORTED, "no decode kernel for d_k=%d n=%d", c->d_k, c->n_terms);
 }
 
+// phi(x) of `rows` fp32 input rows: out[r][a] = w_a * x_i * x_j * x_l from the
+// feature table (index d_k = the constant 1), one thread per (row, feature).
+template <int DK, int NT>
+__global__ void feature_map_kernel(const float* __restrict__ x, float* __restrict__ out, long long rows) {
+  constexpr int D = feat_dim(DK, NT);
+  const long long total = rows * D;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const long long r = e / D;
+    const int a = (int)(e - r * D);
+    const uint32_t code = g_feat<DK, NT>.code[a];
+    float v = g_feat<DK, NT>.w[a];
+#pragma unroll
+    for (int f = 0; f < 3; ++f) {
+      const int i = (int)((code >> (8 * f)) & 255u);
+      if (i != DK) v *= x[r * DK + i];
+    }
+    out[e] = v;
+  }
+}
+
 static unsigned grid_for(size_t n, unsigned per_block = 256) {
   const size_t b = (n + per_block - 1) / per_block;
   return (unsigned)std::max<size_t>(1, std::min<size_t>(b, 148u * 16u));
@@ -502,6 +523,26 @@ tsa_status tsa_feature_index(int d_k, int n_terms, int* idx, float* weight) {
   TSA_FI_CASE(16, 1) TSA_FI_CASE(16, 2) TSA_FI_CASE(16, 3) TSA_FI_CASE(16, 4)
   TSA_FI_CASE(32, 1) TSA_FI_CASE(32, 2) TSA_FI_CASE(32, 3)
 #undef TSA_FI_CASE
+  return fail(TSA_ERR_UNSUPPORTED, "no feature table for d_k=%d n=%d", d_k, n_terms);
+}
+
+tsa_status tsa_feature_map(int d_k, int n_terms, int64_t rows, const float* x, float* out, void* stream) {
+  NvtxRange nvtx_range("tsa_feature_map");
+  if (d_k < 1 || n_terms < 1) return fail(TSA_ERR_INVALID, "d_k and n_terms must be >= 1");
+  if (rows < 0) return fail(TSA_ERR_INVALID, "rows must be >= 0");
+  if (rows == 0) return TSA_OK;
+  if (!x || !out) return fail(TSA_ERR_INVALID, "x and out must be non-NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t total = (size_t)rows * tsa_feature_dim(d_k, n_terms);
+#define TSA_FM_CASE(DK, NT)                                                                    \
+  if (d_k == DK && n_terms == NT) {                                                            \
+    feature_map_kernel<DK, NT><<<grid_for(total), 256, 0, s>>>(x, out, (long long)rows);      \
+    cudaError_t e = cudaGetLastError();                                                        \
+    return e == cudaSuccess ? TSA_OK : cuda_fail(e, "launch feature_map");                     \
+  }
+  TSA_FM_CASE(16, 1) TSA_FM_CASE(16, 2) TSA_FM_CASE(16, 3) TSA_FM_CASE(16, 4)
+  TSA_FM_CASE(32, 1) TSA_FM_CASE(32, 2) TSA_FM_CASE(32, 3)
+#undef TSA_FM_CASE
   return fail(TSA_ERR_UNSUPPORTED, "no feature table for d_k=%d n=%d", d_k, n_terms);
 }
 

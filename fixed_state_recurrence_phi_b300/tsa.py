@@ -24,7 +24,7 @@ TSA_PATH_SIMT, TSA_PATH_TC, TSA_PATH_TC_F32, TSA_PATH_SHORT = 0, 1, 2, 3
 # Every symbol include/tsa.h declares (checked by the CPU test suite).
 EXPORTS = (
     "tsa_feature_dim", "tsa_state_pad_dim", "tsa_state_elems", "tsa_state_bytes",
-    "tsa_feature_index", "tsa_prefill_plan", "tsa_prefill", "tsa_prefill_noalloc", "tsa_prefill_states",
+    "tsa_feature_index", "tsa_feature_map", "tsa_prefill_plan", "tsa_prefill", "tsa_prefill_noalloc", "tsa_prefill_states",
     "tsa_decode_step",
     "tsa_state_merge", "tsa_state_to_canonical", "tsa_sync_status",
     "tsa_status_string", "tsa_last_error",
@@ -64,6 +64,7 @@ def _load():
         "tsa_state_elems": (SZ, [C]),
         "tsa_state_bytes": (SZ, [C]),
         "tsa_feature_index": (I, [I, I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_float)]),
+        "tsa_feature_map": (I, [I, I, I64, P, P, P]),
         "tsa_prefill_plan": (I, [C, I64, I, ctypes.POINTER(TsaPlan)]),
         "tsa_prefill": (I, [C, I64, P, P, P, P, P, U, P]),
         "tsa_prefill_noalloc": (I, [C, I64, P, P, P, P, P, U, P]),
@@ -158,6 +159,12 @@ def feature_index(d_k: int, n_terms: int):
     w = (ctypes.c_float * max(D, 1))()
     _check("tsa_feature_index", _lib.tsa_feature_index(d_k, n_terms, idx, w))
     return np.array(idx[:3 * D], dtype=np.int32).reshape(D, 3), np.array(w[:D], dtype=np.float32)
+
+
+def feature_map(d_k: int, n_terms: int, x, out, stream=None):
+    """phi(x) of the rows of x ([rows, d_k] fp32) into out ([rows, D] fp32)."""
+    _check("tsa_feature_map", _lib.tsa_feature_map(int(d_k), int(n_terms), int(x.shape[0]), _ptr(x), _ptr(out),
+                                                   _stream(stream)))
 
 
 def prefill_plan(cfg, N: int, num_sms: int = 0) -> dict:

@@ -94,6 +94,16 @@ size_t tsa_state_bytes(const tsa_config* cfg);
  * holds 3*D ints, weight D floats. */
 tsa_status tsa_feature_index(int d_k, int n_terms, int* idx, float* weight);
 
+/* The feature map phi(x) = [phi_0(x) | ... | phi_{n-1}(x)] of `rows` inputs, in
+ * fp32, in the order of tsa_feature_index (so <phi_m(q), phi_m(k)> =
+ * (q.k)^m / m!; the m-th block is C(d+m-1, m) wide, abstract). The kernels
+ * build these features on chip and never store them; this call exports them,
+ * e.g. to check the width of the state by the rank of stacked features.
+ *  x   : [rows, d_k] fp32, device;  out : [rows, D] fp32, device (D =
+ *        tsa_feature_dim). Asynchronous on the stream. */
+tsa_status tsa_feature_map(int d_k, int n_terms, int64_t rows, const float* x, float* out,
+                           void* cuda_stream);
+
 /* How tsa_prefill splits the work (host only; num_sms <= 0 asks the current
  * device). The sequence of each head is cut into n_spans spans of
  * chunks_per_span chunks of `chunk` tokens; d_v into n_slices slices of at most
