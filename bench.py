@@ -46,6 +46,9 @@ APPEND_LENGTHS = (16, 32, 64, 256)
 # tsa_plan.path values (include/tsa.h)
 PATH_NAMES = ("simt", "tc", "tc_f32", "short")
 ORDER_SWEEP = (1, 2, 3, 4)
+# chunk lengths the library builds for the fp32 prefill (64: CUDA cores; 128:
+# tensor cores, the default)
+CHUNK_SWEEP = (64, 128)
 APPEND_REPS = 20
 
 
@@ -537,6 +540,41 @@ def _run_ours(args, clk):
               })
               del ost
 
+      chunk_lines = []
+      if args.only in ("all", "orders"):
+          # ---------------- chunk lengths on the prefill workload -----------
+          for ch in CHUNK_SWEEP:
+              ccfg = T.Config(w["B"], w["H"], w["d_k"], w["d_v"], w["n_terms"], w["dtype"], ch)
+              cplan = T.prefill_plan(ccfg, w["N"])
+              cst = T.new_states(ccfg, dev)
+              T.prefill(ccfg, w["N"], q, k, v, out, cst, stream=stream)
+              barrier()
+              cg = torch.cuda.CUDAGraph()
+              cgs = torch.cuda.Stream()
+              cgs.wait_stream(stream)
+              with torch.cuda.stream(cgs):
+                  with torch.cuda.graph(cg, stream=cgs):
+                      T.prefill(ccfg, w["N"], q, k, v, out, cst, stream=cgs)
+              stream.wait_stream(cgs)
+              for _ in range(3):
+                  flush.fill_(1.0)
+                  cg.replay()
+              barrier()
+              cev = []
+              for i in range(max(3, args.steps // 2)):
+                  flush.fill_(float(i))
+                  a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                  a.record(stream)
+                  cg.replay()
+                  b.record(stream)
+                  cev.append((a, b))
+              barrier()
+              T.sync_status(stream)
+              cms = slowest(statistics.mean([a.elapsed_time(b) for a, b in cev]))
+              del cg, cst
+              chunk_lines.append({"chunk": ch, "ms": cms, "path": PATH_NAMES[cplan["path"]],
+                                  "n_spans": cplan["n_spans"]})
+
       if do_dec:
           # ---------------- decode workload ----------------------------------
           dstates = []
@@ -691,6 +729,8 @@ def _run_ours(args, clk):
         "orders": [{"n": o["n_terms"], "ms": r3(o["ms"]), "state_B_per_head": o["state_bytes_per_head"],
                     "path": o["path"]} for o in order_lines],
         "merge": {"ms": r3(merge_ms), "GBps": r3(3 * T.state_bytes(dcfg) / (merge_ms / 1e3) / 1e9)},
+        "chunks": [{"chunk": c_["chunk"], "ms": r3(c_["ms"]), "path": c_["path"], "n_spans": c_["n_spans"]}
+                   for c_ in chunk_lines],
         "prefill_tensor_core": [
             {"workload": t["workload"], "ms": r3(t["ms"]), "tokens_per_s": r3(t["tokens_per_s"]),
              "plan": t["plan"],

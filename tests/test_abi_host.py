@@ -172,3 +172,14 @@ def test_debug_hooks_validate(T):
     assert e.value.status == T.TSA_ERR_INVALID
     T.debug_withhold_publication(0)
     T.debug_set_wait_limit(0)
+
+
+def test_chunk_lengths_built(T):
+    """fp32 prefill chunk lengths: 64 (CUDA cores), 128 (tensor cores) and
+    16 (short segments); 256 is not built (refused on the host)."""
+    for chunk, path in [(64, T.TSA_PATH_SIMT), (128, T.TSA_PATH_TC_F32), (16, T.TSA_PATH_SHORT)]:
+        p = T.prefill_plan(T.Config(1, 8, 16, 64, 3, "f32", chunk), 8192, num_sms=148)
+        assert p["chunk"] == chunk and p["path"] == path, (chunk, p)
+    with pytest.raises(T.TsaError) as e:
+        T.prefill_plan(T.Config(1, 8, 16, 64, 3, "f32", 256), 8192, num_sms=148)
+    assert e.value.status == T.TSA_ERR_UNSUPPORTED

@@ -143,6 +143,17 @@ def test_multi_span_8192(G):
     _all_heads(G, cfg, 8192, seed=2)
 
 
+@pytest.mark.parametrize("chunk,path", [(64, 0), (128, 2)])
+def test_prefill_8192_chunk_sizes(G, chunk, path):
+    """The 8192-token prefill workload at the chunk lengths the library
+    builds for fp32: 64 (CUDA cores) and 128 (tensor cores, the default);
+    every head."""
+    cfg = G.T.Config(1, 8, 16, 64, 3, "f32", chunk)
+    plan = G.T.prefill_plan(cfg, 8192)
+    assert plan["chunk"] == chunk and plan["path"] == path, plan
+    _all_heads(G, cfg, 8192, seed=12 + chunk)
+
+
 def test_accumulate_continues_the_sequence(G):
     T, O = G.T, G.O
     cfg = T.Config(1, 2, 16, 64, 3, "f32")
