@@ -24,7 +24,8 @@ constexpr int kTmemCols = 512;
 int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 // Shared-memory layout for (ring slots, v buffers, q/k buffers); false if it
-// does not fit.
+// does not fit. The layouts are tried with the deepest ring first: the
+// builders hold their inputs in registers, so one q/k buffer costs little.
 bool place_smem(PairParams* p, int dk, int s_bytes, int ring, int nvbuf, int nqk) {
   p->qsz = 128 * dk * 2;
   p->vsz = 128 * p->nm * 2;
@@ -79,7 +80,8 @@ bool pair_layout(int dk, int nt, int dv, PairParams* p) {
     p->col_O = col;
     p->col_A = p->shared_o ? col : col + nm;
     const int s_bytes = so;
-    const int pref[8][3] = {{3, 2, 2}, {2, 2, 2}, {3, 2, 1}, {2, 2, 1}, {3, 1, 2}, {3, 1, 1}, {2, 1, 2}, {2, 1, 1}};
+    const int pref[10][3] = {{4, 2, 2}, {4, 2, 1}, {3, 2, 2}, {3, 2, 1}, {2, 2, 2}, {2, 2, 1},
+                           {3, 1, 2}, {3, 1, 1}, {2, 1, 2}, {2, 1, 1}};
     for (auto& c : pref)
       if (place_smem(p, dk, s_bytes, c[0], c[1], c[2])) return true;
     return false;
@@ -123,7 +125,8 @@ bool pair_layout(int dk, int nt, int dv, PairParams* p) {
     return false;
   }
   const int s_bytes = std::max(sb[0], sb[1]);
-  const int pref[8][3] = {{3, 2, 2}, {2, 2, 2}, {3, 2, 1}, {2, 2, 1}, {3, 1, 2}, {3, 1, 1}, {2, 1, 2}, {2, 1, 1}};
+  const int pref[10][3] = {{4, 2, 2}, {4, 2, 1}, {3, 2, 2}, {3, 2, 1}, {2, 2, 2}, {2, 2, 1},
+                           {3, 1, 2}, {3, 1, 1}, {2, 1, 2}, {2, 1, 1}};
   for (auto& c : pref)
     if (place_smem(p, dk, s_bytes, c[0], c[1], c[2])) return true;
   return false;

@@ -322,10 +322,15 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
       if (!(ok = pr_wait_warp(B, B.pready(), c & 1u))) break;
       TSA_TRACE_EVENT(101, c);
       tc::fence_after_sync();
-      // the next chunk's q, k into the other buffer (two buffers): the builders
-      // have finished chunk c - 1, the buffer's previous user
-      if (has_next && p.nqk == 2) {
-        if (c >= 1 && !(ok = pr_wait_warp(B, B.qkempty((c + 1) & 1), ((c - 1) >> 1) & 1u))) break;
+      // the next chunk's q, k: its buffer's readers hold their inputs in
+      // registers (one buffer: this chunk's builders; two: the previous
+      // chunk's), and this chunk's Q K^T is done (P is written)
+      if (has_next) {
+        if (p.nqk == 1) {
+          if (!(ok = pr_wait_warp(B, B.qkempty(0), c & 1u))) break;
+        } else if (c >= 1) {
+          if (!(ok = pr_wait_warp(B, B.qkempty((c + 1) & 1), ((c - 1) >> 1) & 1u))) break;
+        }
         load_qk(c + 1);
       }
       // the next chunk's v into the other buffer (two buffers): chunk c-1 is done
@@ -374,9 +379,8 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
       }
       if (!(p.dbg_withhold && c == 0)) tc::mma_commit_elect(B.odone());
       TSA_TRACE_EVENT(106, c);
-      // separate score columns and the next chunk's q, k already loaded (two
-      // buffers): its Q K^T now
-      if (has_next && !p.shared_o && p.nqk == 2) {
+      // separate score columns: the next chunk's Q K^T now
+      if (has_next && !p.shared_o) {
         if (!(ok = pr_wait_warp(B, B.qkfull((c + 1) % p.nqk), ((c + 1) / p.nqk) & 1u))) break;
         ++qk_got;
         tc::fence_after_sync();
@@ -407,12 +411,7 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
       }
       tc::mma_commit_elect(B.chunk());
       TSA_TRACE_EVENT(109, c);
-      // one q, k buffer: the next chunk's once the builders are done with this one
-      if (has_next && p.nqk == 1) {
-        if (!(ok = pr_wait_warp(B, B.qkempty(0), c & 1u))) break;
-        load_qk(c + 1);
-      }
-      if (has_next && (p.shared_o || p.nqk == 1)) {
+      if (has_next && p.shared_o) {
         // shared columns: the scores go where O is, after O has been read out
         if (p.shared_o && !(ok = pr_wait_warp(B, B.ofree(), c & 1u))) break;
         if (!(ok = pr_wait_warp(B, B.qkfull((c + 1) % p.nqk), ((c + 1) / p.nqk) & 1u))) break;
@@ -542,7 +541,7 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
         tc::fence_proxy_async();
         for (int t = 0; t < ntile; ++t) tc_warp_arrive(B.conv(t), lane);
         if (!(ok = compute_p(0, valid))) break;
-      } else if (p.shared_o || p.nqk == 1) {
+      } else if (p.shared_o) {
         if (!(ok = compute_p(c, valid))) break;
       }
       // ---- the output of chunk c
@@ -613,7 +612,7 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
       tc_warp_arrive(B.ofree(), lane);
       TSA_TRACE_EVENT(204, c);
       // ---- separate score columns, Q K^T issued early: the next chunk's P now
-      if (has_next && !p.shared_o && p.nqk == 2) {
+      if (has_next && !p.shared_o) {
         const int valid1 = (int)min((long long)TC_C, t_end - (t0 + TC_C));
         if (!(ok = compute_p(c + 1, valid1))) break;
       }
@@ -632,10 +631,9 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
     // --------------------------- builder warps ------------------------------
     // One pass over the chunk's ring uses: the readout tiles of each tile's
     // block (64-feature halves; token t, quarter 2h + qr), then its two update
-    // tiles (64 tokens each; token 64h + tq, quarter qq). The token's inputs are
-    // read from the q / k tile for each use (nothing is kept across uses, which
-    // keeps the builders clear of register spills), and the q, k buffer is
-    // released after the chunk's last use.
+    // tiles (64 tokens each; token 64h + tq, quarter qq). The three tokens'
+    // inputs (packed bf16 pairs) are read once per chunk into registers and the
+    // q, k buffer is released at once.
     const int bt = tid - PR_BUILDER0;
     const int t = bt & 127, qr = bt >> 7;
     const int tq = bt & 63, qq = bt >> 6;
@@ -653,8 +651,11 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
       TSA_TRACE_EVENT(300, c);
       if (!pr_wait_warp(B, B.qkfull(qb), (c / p.nqk) & 1u)) break;
       TSA_TRACE_EVENT(301, c);
-      const uint8_t* qtile = smem + p.off_q + qb * p.qsz;
-      const uint8_t* ktile = smem + p.off_k + qb * p.qsz;
+      uint32_t xq[DK / 2], xk0[DK / 2], xk1[DK / 2];
+      pr_load_xp<DK>(smem + p.off_q + qb * p.qsz, t, xq);
+      pr_load_xp<DK>(smem + p.off_k + qb * p.qsz, tq, xk0);
+      pr_load_xp<DK>(smem + p.off_k + qb * p.qsz, 64 + tq, xk1);
+      tc_warp_arrive(B.qkempty(qb), lane);
       const int nuse = n_ro + (need_update ? 2 * ntile : 0);
       bool ok = true;
       int tt = 0, h = 0;
@@ -670,12 +671,16 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
         const int tok = upd ? 64 * h + tq : t;
         if (upd || 64 * h + 32 * qr < T.ro_rows) {
           uint32_t xp[DK / 2];
-          pr_load_xp<DK>(upd ? ktile : qtile, tok, xp);
+#pragma unroll
+          for (int e = 0; e < DK / 2; ++e) xp[e] = upd ? (h ? xk1[e] : xk0[e]) : xq[e];
+          TSA_TRACE_EVENT(304, 0);
           const float x0 = (!upd || tok < valid) ? 1.0f : 0.0f;
           pr_build32<DK, NT>(T.blk, upd ? qq : 2 * h + qr, xp, x0,
                              smem + p.off_ring + ring.s * 16384 + (upd ? up_row : ro_row));
+          TSA_TRACE_EVENT(305, 0);
         }
         tc::fence_proxy_async();
+        TSA_TRACE_EVENT(306, 0);
         tc_warp_arrive(B.rfull(ring.s), lane);
         TSA_TRACE_EVENT(303, ring.s);
         ring.used |= 1u << ring.s;
@@ -683,7 +688,6 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
         if (++h == (upd ? 2 : pr_ro_halves(T.ro_rows))) { h = 0; ++tt; }
       }
       if (!ok) break;
-      tc_warp_arrive(B.qkempty(qb), lane);
     }
   }
   tc::fence_before_sync();
