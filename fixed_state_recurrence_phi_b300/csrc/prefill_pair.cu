@@ -181,7 +181,7 @@ tsa_status launch_pair(const tsa_plan& pl, const PrefillParams& pp, cudaStream_t
   p.N = pp.N; p.heads = pp.heads; p.n_spans = pl.n_spans;
   p.chunks_per_span = pl.chunks_per_span; p.accumulate = pp.accumulate;
   tc_debug_params(&p.wait_ns, &p.dbg_withhold);
-  p.dbg_withhold = 0;   // the withheld-publication hook is the fp32 pass's
+  p.dbg_withhold = (p.dbg_withhold == 2);   // hook 2: rank 0's first partial rows
   tsa_status st = device_error_word(&p.err);
   if (st != TSA_OK) return st;
   // the span pass and scan of a multi-span plan: the value-sliced kernels

@@ -165,6 +165,7 @@ void fill_tc_params(TcParams* p, const tsa_plan& pl, const TcSlicing& ts, const 
   p->n_slices = ts.n_slices; p->nmax = ts.nmax; p->ring = ts.ring;
   for (int k = 0; k < ts.n_slices; ++k) { p->slice_c0[k] = ts.c0[k]; p->slice_w[k] = ts.w[k]; }
   tc_debug_params(&p->wait_ns, &p->dbg_withhold);
+  p->dbg_withhold = 0;   // no withheld publication in these kernels
 }
 
 // The span-state pass of a multi-span plan (each span's state sum into the
@@ -247,7 +248,7 @@ extern "C" tsa_status tsa_debug_set_wait_limit(uint64_t ns) {
 }
 
 extern "C" tsa_status tsa_debug_withhold_publication(int what) {
-  if (what != 0 && what != 1) return tsa::fail(TSA_ERR_INVALID, "withhold must be 0 or 1 (got %d)", what);
+  if (what < 0 || what > 2) return tsa::fail(TSA_ERR_INVALID, "withhold must be 0, 1 or 2 (got %d)", what);
   tsa::g_withhold.store(what);
   return TSA_OK;
 }

@@ -111,6 +111,7 @@ tsa_status states32(const tsa_plan& pl, const PrefillParams& pp, cudaStream_t s)
   p.ring = (smem_tc32<DK, NT>(pp.dv, 3) <= kSmemLimit) ? 3 : 2;
   const int smem = (int)smem_tc32<DK, NT>(pp.dv, p.ring);
   tc_debug_params(&p.wait_ns, &p.dbg_withhold);
+  p.dbg_withhold = (p.dbg_withhold == 1);   // hook 1: this pass's first O
   tsa_status st = device_error_word(&p.err);
   if (st != TSA_OK) return st;
   CUtensorMap mk, mv;
@@ -132,6 +133,7 @@ tsa_status launch32(const tsa_plan& pl, const PrefillParams& pp, cudaStream_t s)
   p.ring = (smem_tc32<DK, NT>(pp.dv, 3) <= kSmemLimit) ? 3 : 2;
   const int smem = (int)smem_tc32<DK, NT>(pp.dv, p.ring);
   tc_debug_params(&p.wait_ns, &p.dbg_withhold);
+  p.dbg_withhold = (p.dbg_withhold == 1);   // hook 1: this pass's first O
   tsa_status st = device_error_word(&p.err);
   if (st != TSA_OK) return st;
   CUtensorMap mq, mk, mv, mo;

@@ -234,8 +234,14 @@ tsa_status tsa_sync_status(void* cuda_stream);
  *    (TSA_PATH_TC_F32) never publishes the first chunk's completed output
  *    accumulator, so the waits for it run out: each CTA gives up, releases
  *    its tensor memory and exits with its outputs incomplete, and the next
- *    tsa_sync_status returns TSA_ERR_TIMEOUT. 0 turns it off; other values
- *    are TSA_ERR_INVALID. */
+ *    tsa_sync_status returns TSA_ERR_TIMEOUT.
+ *    tsa_debug_withhold_publication(2): in the bf16 prefill whose head state
+ *    a CTA pair shares (tsa_plan.cluster = 2), rank 0 of each pair never
+ *    tells its peer that its first chunk's partial output rows have arrived
+ *    in the peer's shared memory; the peer's wait runs out, the peer gives up
+ *    and makes rank 0 give up too, both release their tensor memory and
+ *    exit, and tsa_sync_status returns TSA_ERR_TIMEOUT.
+ *    0 turns it off; other values are TSA_ERR_INVALID. */
 tsa_status tsa_debug_set_wait_limit(uint64_t ns);
 tsa_status tsa_debug_withhold_publication(int what);
 

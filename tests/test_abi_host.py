@@ -168,7 +168,7 @@ def test_validation_codes(T):
 def test_debug_hooks_validate(T):
     """The testing hooks take only their documented values (host only)."""
     with pytest.raises(T.TsaError) as e:
-        T.debug_withhold_publication(7)
+        T.debug_withhold_publication(3)
     assert e.value.status == T.TSA_ERR_INVALID
     T.debug_withhold_publication(0)
     T.debug_set_wait_limit(0)

@@ -58,3 +58,38 @@ def test_withheld_publication_times_out_then_prefill_is_correct(T):
         o_r, S_r = oracle_prefill(qh[0, h], kh[0, h], vh[0, h], 3)
         check_head(cfg, host(out[0, h]), S[0, h], o_r, S_r, TOL["f32"], f"head {h}")
 
+
+def test_pair_exchange_withheld_times_out_then_prefill_is_correct(T):
+    """The CTA-pair prefill (bf16, order 4): rank 0 of each pair withholds its
+    first partial-output publication to its peer. The peer's bounded wait runs
+    out, it passes the abort to rank 0, both release their tensor memory and
+    leave through the cluster barrier, and TSA_ERR_TIMEOUT is reported; the
+    same prefill afterwards matches the oracle."""
+    from gpu_helpers import check_head, host, make_inputs, oracle_prefill, canonical, TOL
+    cfg = T.Config(1, 2, 16, 64, 4, "bf16")
+    N = 700
+    assert T.prefill_plan(cfg, N)["cluster"] == 2
+    q, k, v = make_inputs(cfg, N, seed=32)
+    out = torch.zeros((1, 2, N, 64), dtype=torch.bfloat16, device="cuda")
+    st = T.new_states(cfg)
+    T.sync_status()
+    T.debug_set_wait_limit(2_000_000)
+    T.debug_withhold_publication(2)
+    try:
+        T.prefill(cfg, N, q, k, v, out, st)
+        with pytest.raises(T.TsaError) as e:
+            T.sync_status()
+        assert e.value.status == T.TSA_ERR_TIMEOUT, T.last_error()
+    finally:
+        T.debug_withhold_publication(0)
+        T.debug_set_wait_limit(0)
+    T.sync_status()
+    out.zero_()
+    st.zero_()
+    T.prefill(cfg, N, q, k, v, out, st)
+    T.sync_status()
+    S = canonical(cfg, st)
+    qh, kh, vh = host(q), host(k), host(v)
+    for h in range(2):
+        o_r, S_r = oracle_prefill(qh[0, h], kh[0, h], vh[0, h], 4)
+        check_head(cfg, host(out[0, h]), S[0, h], o_r, S_r, TOL["bf16"], f"head {h}")
