@@ -234,6 +234,7 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
   const long long t_end = min(p.N, t_begin + (long long)p.chunks_per_span * TC_C);
   const int n_chunks = (int)((t_end - t_begin + TC_C - 1) / TC_C);
   const bool single = (p.n_spans == 1);
+  TSA_DCHECK(head < p.heads, dbg::kWorkUnit, head, p.heads);
   const int ntile = p.ntile[r];
   const int zc = p.zc, nm = p.nm, dv = p.dv;
   const size_t st_elems = (size_t)DPAD * (dv + 1);
@@ -523,9 +524,13 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
               float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
               const int cc = cc0 + 4 * e4;
               if (st_src != nullptr && a < D) {
-                if (cc < zc) x = *reinterpret_cast<const float4*>(st_src + (size_t)a * dv + cc);
-                else if (cc >= zc + 16) x = *reinterpret_cast<const float4*>(st_src + (size_t)a * dv + cc - 16);
-                else if (cc == zc) x.x = st_src[(size_t)DPAD * dv + a];
+                if (cc < zc || cc >= zc + 16) {
+                  const int vcol = cc < zc ? cc : cc - 16;   // the value column
+                  if (TSA_DCHECK_STATE((size_t)a * dv + vcol, 4, (size_t)DPAD * dv))
+                    x = *reinterpret_cast<const float4*>(st_src + (size_t)a * dv + vcol);
+                } else if (cc == zc) {
+                  x.x = st_src[(size_t)DPAD * dv + a];
+                }
               }
               rr[4 * e4] = __float_as_uint(x.x);
               rr[4 * e4 + 1] = __float_as_uint(x.y);
@@ -715,6 +720,7 @@ span_output_pair_kernel(const __grid_constant__ PairParams p, const __grid_const
           dst[(size_t)DPAD * dv + a] = (a < D) ? __uint_as_float(rr[0]) : 0.0f;
         } else {
           const int v0 = cc0 < zc ? cc0 : cc0 - 16;
+          if (!TSA_DCHECK_STATE((size_t)a * dv + v0, 16, (size_t)DPAD * dv)) continue;
           float4* o = reinterpret_cast<float4*>(dst + (size_t)a * dv + v0);
 #pragma unroll
           for (int e = 0; e < 4; ++e)

@@ -6,6 +6,9 @@
 #include "prefill_short.cuh"
 
 namespace tsa {
+
+// This translation unit's device-check report (debug build; debug_check.cuh).
+TSA_DEBUG_REPORT_READER(debug_report_short)
 namespace {
 
 template <typename T, int DK, int NT, int DV>

@@ -26,6 +26,7 @@
 #pragma once
 #include <cstring>
 #include "common.cuh"
+#include "debug_check.cuh"
 #include "prefill_params.h"
 
 namespace tsa {
@@ -212,6 +213,7 @@ span_state_kernel(PrefillParams p) {
   const int span = blockIdx.x % p.n_spans;
   const int slice = (blockIdx.x / p.n_spans) % p.n_slices;
   const int head = blockIdx.x / (p.n_spans * p.n_slices);
+  TSA_DCHECK(head < p.heads, dbg::kWorkUnit, head, p.heads);
   const int c0 = slice * W;
   const long long t_begin = (long long)span * p.chunks_per_span * L::C;
   const long long t_end = min(p.N, t_begin + (long long)p.chunks_per_span * L::C);
@@ -322,6 +324,7 @@ span_output_kernel(PrefillParams p) {
   const int span = blockIdx.x % p.n_spans;
   const int slice = (blockIdx.x / p.n_spans) % p.n_slices;
   const int head = blockIdx.x / (p.n_spans * p.n_slices);
+  TSA_DCHECK(head < p.heads, dbg::kWorkUnit, head, p.heads);
   const int c0 = slice * W;
   const long long t_begin = (long long)span * p.chunks_per_span * C;
   const long long t_end = min(p.N, t_begin + (long long)p.chunks_per_span * C);

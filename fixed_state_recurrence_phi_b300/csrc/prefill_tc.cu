@@ -16,6 +16,9 @@
 #include "prefill_simt.cuh"
 
 namespace tsa {
+
+// This translation unit's device-check report (debug build; debug_check.cuh).
+TSA_DEBUG_REPORT_READER(debug_report_tc)
 namespace {
 
 // Set by a kernel whose bounded wait gave up; read and cleared by

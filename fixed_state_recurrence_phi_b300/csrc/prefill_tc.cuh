@@ -134,6 +134,7 @@ __device__ __forceinline__ void tc_store_state(float* dst, uint32_t tm, uint32_t
       tc::tmem_wait_ld();
       if (a < DPAD) {
         if (g * 16 < W) {
+          if (!TSA_DCHECK_STATE((size_t)a * dv + c0 + g * 16, 16, (size_t)DPAD * dv)) continue;
           float4* o = reinterpret_cast<float4*>(dst + (size_t)a * dv + c0 + g * 16);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
@@ -165,6 +166,7 @@ __device__ __forceinline__ TcUnit tc_unit(const TcParams& p) {
   for (int k = 0; k < TC_MAX_SLICES; ++k)
     if (k == u.slice) { u.W = p.slice_w[k]; u.c0 = p.slice_c0[k]; }
   u.nm = u.W + 16;
+  TSA_DCHECK(u.head < p.heads, dbg::kWorkUnit, u.head, p.heads);
   u.t_begin = (long long)u.span * p.chunks_per_span * TC_C;
   u.t_end = min(p.N, u.t_begin + (long long)p.chunks_per_span * TC_C);
   u.n_chunks = (int)((u.t_end - u.t_begin + TC_C - 1) / TC_C);
@@ -447,7 +449,8 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
           const int c = g * 16 + e;
           float x = 0.0f;
           if (src != nullptr && a < D) {
-            if (c < W) x = src[(size_t)a * p.dv + u.c0 + c];
+            if (c < W && TSA_DCHECK_STATE((size_t)a * p.dv + u.c0 + c, 1, (size_t)DPAD * p.dv))
+              x = src[(size_t)a * p.dv + u.c0 + c];
             else if (c == W) x = src[(size_t)DPAD * p.dv + a];
           }
           v[e] = x;

@@ -13,6 +13,9 @@
 #include "prefill_simt.cuh"
 
 namespace tsa {
+
+// This translation unit's device-check report (debug build; debug_check.cuh).
+TSA_DEBUG_REPORT_READER(debug_report_tc32)
 namespace {
 
 constexpr size_t kSmemLimit = 227 * 1024;

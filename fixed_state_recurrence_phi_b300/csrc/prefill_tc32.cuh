@@ -794,7 +794,8 @@ span_output_tc32_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm
               const int cc = g * 16 + 4 * e4;
               float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
               if (src != nullptr && a < D) {
-                if (cc < W) x = *reinterpret_cast<const float4*>(src + (size_t)a * p.dv + u.c0 + cc);
+                if (cc < W && TSA_DCHECK_STATE((size_t)a * p.dv + u.c0 + cc, 4, (size_t)DPAD * p.dv))
+                  x = *reinterpret_cast<const float4*>(src + (size_t)a * p.dv + u.c0 + cc);
                 else if (cc == W) x.x = src[(size_t)DPAD * p.dv + a];
               }
               r[4 * e4] = __float_as_uint(x.x);

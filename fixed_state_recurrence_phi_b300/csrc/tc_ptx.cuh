@@ -18,6 +18,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
+#include "debug_check.cuh"
 
 // Timeline trace points. They expand to nothing unless a diagnostic build
 // defines TSA_TRACE_DECL (declared once per kernel thread) and
@@ -45,6 +46,60 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
   d |= (uint64_t)1 << 46;
   return d;
 }
+
+// ---- checks of the debug build (debug_check.cuh) ------------------------------
+#ifdef TSA_DEBUG
+// The CTA's dynamic shared memory: [dyn_smem_lo, dyn_smem_lo + dyn_smem_size)
+// (every extern shared array starts where the dynamic shared memory does).
+__device__ __forceinline__ uint32_t dyn_smem_lo() {
+  extern __shared__ __align__(16) uint8_t tsa_dynamic_smem[];
+  return smem_u32(tsa_dynamic_smem);
+}
+__device__ __forceinline__ uint32_t dyn_smem_size() {
+  uint32_t r;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+  return r;
+}
+// ncols columns from the address's column lie inside the 512 allocated
+__device__ __forceinline__ bool chk_tmem_cols(uint32_t taddr, uint32_t ncols) {
+  const uint32_t col = taddr & 0xFFFFu;
+  return TSA_DCHECK(col + ncols <= 512u, dbg::kTmemColumns, col, ncols);
+}
+// a tcgen05.ld/st of this warp: its own 32-lane quarter, columns inside
+__device__ __forceinline__ bool chk_tmem_warp(uint32_t taddr, uint32_t ncols) {
+  const uint32_t lane = taddr >> 16, quarter = 32u * ((threadIdx.x >> 5) & 3u);
+  return TSA_DCHECK(lane == quarter, dbg::kTmemLanes, lane, quarter) && chk_tmem_cols(taddr, ncols);
+}
+// an MMA accumulator or A operand in TMEM: lane 0, columns inside
+__device__ __forceinline__ bool chk_tmem_mma(uint32_t taddr, uint32_t ncols) {
+  return TSA_DCHECK((taddr >> 16) == 0u, dbg::kTmemLanes, taddr >> 16, 0) && chk_tmem_cols(taddr, ncols);
+}
+// the bytes of a no-swizzle operand of `rows` rows (M or N) and K = 16
+__device__ __forceinline__ bool chk_smem_operand(uint64_t desc, uint32_t rows) {
+  const uint32_t start = (uint32_t)(desc & 0x3FFFu) << 4;
+  const uint32_t lbo = (uint32_t)((desc >> 16) & 0x3FFFu) << 4;
+  const uint32_t sbo = (uint32_t)((desc >> 32) & 0x3FFFu) << 4;
+  const uint32_t end = start + (rows / 8u - 1u) * sbo + lbo + 128u;
+  // a descriptor holds the low 18 bits of the address; in a cluster the
+  // shared-window address of the CTA's own memory carries its rank above them
+  const uint32_t lo = dyn_smem_lo() & 0x3FFFFu, hi = lo + dyn_smem_size();
+  return TSA_DCHECK(start >= lo && end <= hi, dbg::kSmemOperand, ((uint64_t)lo << 32) | start,
+                    ((uint64_t)hi << 32) | end);
+}
+// a shared-memory address with `align`-byte alignment inside the CTA's
+// dynamic shared memory, `bytes` of it
+__device__ __forceinline__ bool chk_smem_range(uint32_t saddr, uint32_t bytes, uint32_t align) {
+  const uint32_t lo = dyn_smem_lo(), hi = lo + dyn_smem_size();
+  return TSA_DCHECK(saddr % align == 0u && saddr >= lo && saddr + bytes <= hi, dbg::kBulkCopy,
+                    ((uint64_t)lo << 32) | saddr, ((uint64_t)hi << 32) | bytes);
+}
+#else
+__device__ __forceinline__ bool chk_tmem_cols(uint32_t, uint32_t) { return true; }
+__device__ __forceinline__ bool chk_tmem_warp(uint32_t, uint32_t) { return true; }
+__device__ __forceinline__ bool chk_tmem_mma(uint32_t, uint32_t) { return true; }
+__device__ __forceinline__ bool chk_smem_operand(uint64_t, uint32_t) { return true; }
+__device__ __forceinline__ bool chk_smem_range(uint32_t, uint32_t, uint32_t) { return true; }
+#endif
 
 // Instruction descriptor of kind::f16 with bf16 A and B and an fp32 accumulator.
 // a_mn / b_mn select MN-major (transposed) operands.
@@ -81,6 +136,10 @@ __device__ __forceinline__ void fence_proxy_async() {
 // issue cost per MMA low.
 __device__ __forceinline__ void mma_bf16_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                                uint32_t idesc, uint32_t accumulate) {
+  if (dbg::kEnabled) {
+    const uint32_t n = ((idesc >> 17) & 0x3Fu) << 3, m = ((idesc >> 24) & 0x1Fu) << 4;
+    if (!(chk_tmem_mma(d_tmem, n) && chk_smem_operand(adesc, m) && chk_smem_operand(bdesc, n))) return;
+  }
   asm volatile(
       "{\n\t.reg .pred p, e;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -93,6 +152,10 @@ __device__ __forceinline__ void mma_bf16_elect(uint32_t d_tmem, uint64_t adesc, 
 // (8 columns), K-major.
 __device__ __forceinline__ void mma_bf16_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
                                                   uint32_t idesc, uint32_t accumulate) {
+  if (dbg::kEnabled) {
+    const uint32_t n = ((idesc >> 17) & 0x3Fu) << 3;
+    if (!(chk_tmem_mma(d_tmem, n) && chk_tmem_mma(a_tmem, 8u) && chk_smem_operand(bdesc, n))) return;
+  }
   asm volatile(
       "{\n\t.reg .pred p, e;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -116,6 +179,10 @@ __device__ __forceinline__ bool elect_one() {
 
 // 32 lanes x 16 columns of 32 bits: thread t of the warp gets lane (base + t).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  if (dbg::kEnabled && !chk_tmem_warp(taddr, 16u)) {
+    for (int e = 0; e < 16; ++e) r[e] = 0u;
+    return;
+  }
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -126,6 +193,10 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 // 32 lanes x 32 columns of 32 bits in one load.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  if (dbg::kEnabled && !chk_tmem_warp(taddr, 32u)) {
+    for (int e = 0; e < 32; ++e) r[e] = 0u;
+    return;
+  }
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -137,6 +208,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  if (dbg::kEnabled && !chk_tmem_warp(taddr, 16u)) return;
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
       "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
@@ -212,6 +284,9 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // 4-D tiled load of a box into shared memory, completing on `bar` (tx bytes).
 __device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1,
                                             int c2, int c3) {
+  if (dbg::kEnabled && !(TSA_DCHECK(c0 % 8 == 0, dbg::kTmaCoord, 0, c0) && chk_smem_range(smem_u32(dst), 16u, 16u) &&
+                         chk_smem_range(smem_u32(bar), 8u, 8u)))
+    return;
   asm volatile(
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%3, %4, %5, %6}], [%2];"
@@ -222,6 +297,11 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, uint64_
 // Untiled bulk copy global -> shared (both 16-byte aligned, size a multiple
 // of 16), completing on `bar` (tx bytes).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  if (dbg::kEnabled &&
+      !(TSA_DCHECK(reinterpret_cast<uintptr_t>(src) % 16 == 0 && bytes % 16 == 0, dbg::kBulkCopy,
+                   reinterpret_cast<uintptr_t>(src), bytes) &&
+        chk_smem_range(smem_u32(dst), bytes, 16u)))
+    return;
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
@@ -229,6 +309,11 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // 4-D tiled store of a box from shared memory (bulk-group completion). The
 // caller makes its shared-memory writes visible to the async proxy first.
 __device__ __forceinline__ void tma_store_4d(const void* tmap, const void* src, int c0, int c1, int c2, int c3) {
+  if (dbg::kEnabled &&
+      !(TSA_DCHECK(c0 % 8 == 0, dbg::kTmaCoord, 0, c0) && TSA_DCHECK(c1 >= 0, dbg::kTmaCoord, 1, c1) &&
+        TSA_DCHECK(c2 >= 0, dbg::kTmaCoord, 2, c2) && TSA_DCHECK(c3 >= 0, dbg::kTmaCoord, 3, c3) &&
+        chk_smem_range(smem_u32(src), 16u, 16u)))
+    return;
   asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];"
                :: "l"(tmap), "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
                : "memory");

@@ -16,6 +16,7 @@
 #include "../../include/tsa.h"
 #include "tsa_internal.h"
 #include "common.cuh"
+#include "tc_ptx.cuh"
 #include "prefill_simt.cuh"
 #include "decode.cuh"
 
@@ -35,6 +36,52 @@ tsa_status fail(tsa_status s, const char* fmt, ...) {
 
 tsa_status cuda_fail(cudaError_t e, const char* what) {
   return fail(TSA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+// This translation unit's device-check report (debug build; debug_check.cuh).
+TSA_DEBUG_REPORT_READER(debug_report_abi)
+
+// What a failed device check was about.
+static const char* check_name(unsigned long long what) {
+  switch (what) {
+    case dbg::kTmemColumns: return "TMEM columns beyond the allocation (first column, columns)";
+    case dbg::kTmemLanes: return "TMEM lanes outside the warp's quarter (lane, quarter)";
+    case dbg::kSmemOperand:
+      return "MMA operand outside the dynamic shared memory (shared-memory start << 32 | first byte, end << 32 | "
+             "one past the last byte)";
+    case dbg::kTmaCoord: return "TMA coordinate (index, value)";
+    case dbg::kBulkCopy:
+      return "bulk copy address, size or extent (shared-memory start << 32 | address, end << 32 | bytes)";
+    case dbg::kStateIndex: return "state element index (index, elements)";
+    case dbg::kWorkUnit: return "work unit beyond the launch (index, count)";
+  }
+  return "unknown check";
+}
+
+// Collect and clear the device-check reports of every translation unit; the
+// first one found is returned as TSA_ERR_DEVICE_CHECK. Release build: TSA_OK.
+tsa_status take_debug_reports() {
+  using Reader = cudaError_t (*)(unsigned long long*);
+  const Reader readers[] = {debug_report_abi, debug_report_tc, debug_report_tc32, debug_report_pair,
+                            debug_report_short};
+  unsigned long long first[4] = {0, 0, 0, 0};
+  for (Reader rd : readers) {
+    unsigned long long rep[4];
+    const cudaError_t e = rd(rep);
+    if (e != cudaSuccess) return cuda_fail(e, "read device-check report");
+    if (rep[0] != 0 && first[0] == 0) memcpy(first, rep, sizeof(first));
+  }
+  if (first[0] == 0) return TSA_OK;
+  return fail(TSA_ERR_DEVICE_CHECK, "device check failed: %s = (%lld, %lld) [0x%llx, 0x%llx] in block %llu, thread %llu",
+              check_name(first[0]), (long long)first[1], (long long)first[2], first[1], first[2], first[3] >> 32,
+              first[3] & 0xFFFFFFFFull);
+}
+
+// Runs the wrappers' TMEM-column check on 16 columns from `col` without any
+// TMEM access (nothing is allocated): with col > 496 it fails, which tests
+// the debug build's report path end to end.
+__global__ void debug_selftest_kernel(uint32_t col) {
+  if (threadIdx.x == 0) tc::chk_tmem_cols(col, 16u);
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -695,7 +742,22 @@ tsa_status tsa_sync_status(void* stream) {
   NvtxRange nvtx_range("tsa_sync_status");
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  return take_device_error();
+  const tsa_status waits = take_device_error();
+  // a failed device check (debug build) is reported before the waits it may
+  // have cut short
+  const tsa_status checks = take_debug_reports();
+  return checks != TSA_OK ? checks : waits;
+}
+
+int tsa_debug_build(void) { return dbg::kEnabled ? 1 : 0; }
+
+tsa_status tsa_debug_check_selftest(void* stream) {
+  NvtxRange nvtx_range("tsa_debug_check_selftest");
+  if (!dbg::kEnabled) return fail(TSA_ERR_UNSUPPORTED, "device checks exist only in the debug build");
+  debug_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(510u);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "debug_selftest_kernel");
+  return TSA_OK;
 }
 
 const char* tsa_status_string(tsa_status s) {
@@ -705,6 +767,7 @@ const char* tsa_status_string(tsa_status s) {
     case TSA_ERR_UNSUPPORTED: return "TSA_ERR_UNSUPPORTED";
     case TSA_ERR_CUDA: return "TSA_ERR_CUDA";
     case TSA_ERR_TIMEOUT: return "TSA_ERR_TIMEOUT";
+    case TSA_ERR_DEVICE_CHECK: return "TSA_ERR_DEVICE_CHECK";
   }
   return "TSA_UNKNOWN_STATUS";
 }

@@ -3,7 +3,10 @@
 Argument marshalling only: every step of the computation runs in the CUDA
 kernels behind the C ABI. Tensors are passed as raw device pointers (torch is
 used for device memory and streams). If the library is not built, importing
-this module raises: there is no fallback path.
+this module raises: there is no fallback path. With TSA_DEBUG=1 in the
+environment the debug build (libtsa_debug.so: the same kernels with device-side
+checks before each TMEM, shared-memory operand, TMA and state access) is
+loaded instead.
 """
 from __future__ import annotations
 
@@ -14,9 +17,9 @@ from dataclasses import dataclass
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libtsa.so")
+LIB_PATH = os.path.join(_HERE, "libtsa_debug.so" if os.environ.get("TSA_DEBUG") == "1" else "libtsa.so")
 
-TSA_OK, TSA_ERR_INVALID, TSA_ERR_UNSUPPORTED, TSA_ERR_CUDA, TSA_ERR_TIMEOUT = range(5)
+TSA_OK, TSA_ERR_INVALID, TSA_ERR_UNSUPPORTED, TSA_ERR_CUDA, TSA_ERR_TIMEOUT, TSA_ERR_DEVICE_CHECK = range(6)
 TSA_F32, TSA_BF16 = 0, 1
 TSA_PREFILL_ACCUMULATE = 1
 TSA_PATH_SIMT, TSA_PATH_TC, TSA_PATH_TC_F32, TSA_PATH_SHORT = 0, 1, 2, 3
@@ -29,6 +32,7 @@ EXPORTS = (
     "tsa_state_merge", "tsa_state_to_canonical", "tsa_sync_status",
     "tsa_status_string", "tsa_last_error",
     "tsa_debug_set_wait_limit", "tsa_debug_withhold_publication",
+    "tsa_debug_build", "tsa_debug_check_selftest",
 )
 
 
@@ -77,6 +81,8 @@ def _load():
         "tsa_last_error": (ctypes.c_char_p, []),
         "tsa_debug_set_wait_limit": (I, [ctypes.c_uint64]),
         "tsa_debug_withhold_publication": (I, [I]),
+        "tsa_debug_build": (I, []),
+        "tsa_debug_check_selftest": (I, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -219,8 +225,20 @@ def debug_set_wait_limit(ns: int):
 
 
 def debug_withhold_publication(what: int):
-    """Testing hook: 1 = the fp32 output pass withholds its first publication."""
+    """Testing hook: 1 = the fp32 output pass withholds its first publication;
+    2 = rank 0 of each CTA pair withholds its first exchange publication."""
     _check("tsa_debug_withhold_publication", _lib.tsa_debug_withhold_publication(int(what)))
+
+
+def debug_build() -> bool:
+    """True when the loaded library is the debug build (device-side checks)."""
+    return bool(_lib.tsa_debug_build())
+
+
+def debug_check_selftest(stream=None):
+    """Debug build: queue one kernel whose TMEM-column check fails on purpose
+    (no TMEM access); the next sync_status raises TSA_ERR_DEVICE_CHECK."""
+    _check("tsa_debug_check_selftest", _lib.tsa_debug_check_selftest(_stream(stream)))
 
 
 # ---- small torch conveniences (allocation only) ----------------------------

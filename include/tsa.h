@@ -49,7 +49,8 @@ typedef enum {
   TSA_ERR_INVALID = 1,      /* bad pointer, size, alignment or flag          */
   TSA_ERR_UNSUPPORTED = 2,  /* valid but not built: (d_k, d_v, n_terms, chunk) */
   TSA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed           */
-  TSA_ERR_TIMEOUT = 4       /* a device-side bounded wait gave up             */
+  TSA_ERR_TIMEOUT = 4,      /* a device-side bounded wait gave up             */
+  TSA_ERR_DEVICE_CHECK = 5  /* a device-side check of the debug build failed  */
 } tsa_status;
 
 typedef enum { TSA_F32 = 0, TSA_BF16 = 1 } tsa_dtype;
@@ -221,7 +222,8 @@ tsa_status tsa_state_to_canonical(const tsa_config* cfg, const float* states, fl
  * tensor-core kernels bound every wait on their mbarriers at 1 s; a CTA whose
  * wait runs out records it here, stops, releases its tensor memory and exits,
  * leaving its outputs incomplete). The flag is per device and is cleared by
- * this call. */
+ * this call. In the debug build (below) a failed device-side check since the
+ * last call is reported first, as TSA_ERR_DEVICE_CHECK. */
 tsa_status tsa_sync_status(void* cuda_stream);
 
 /* Testing hooks for the failure path of the bounded waits; not for use in
@@ -244,6 +246,28 @@ tsa_status tsa_sync_status(void* cuda_stream);
  *    0 turns it off; other values are TSA_ERR_INVALID. */
 tsa_status tsa_debug_set_wait_limit(uint64_t ns);
 tsa_status tsa_debug_withhold_publication(int what);
+
+/* The debug build (libtsa_debug.so, compiled with -DTSA_DEBUG; same API and
+ * kernels) checks on the device, before each access: that TMEM accesses and
+ * MMA accumulators stay inside the 512 allocated columns and a warp's TMEM
+ * loads and stores inside its own 32-lane quarter; that every MMA operand
+ * read from shared memory lies inside the CTA's dynamic shared memory; that
+ * tiled TMA copies start at an innermost coordinate that is a multiple of 8
+ * elements and stores at no negative coordinate; that bulk copies have
+ * 16-byte aligned addresses and sizes and end inside shared memory; and that
+ * CTAs map to heads of the launch and state indices to elements of their
+ * head's state. A failed check skips that access (a load returns zeros),
+ * records what failed and two values (the first failure since the last
+ * tsa_sync_status), and the kernel runs on or gives up at its next bounded
+ * wait; nothing traps. tsa_sync_status then returns TSA_ERR_DEVICE_CHECK and
+ * tsa_last_error names the check, its values, the block and the thread.
+ *  - tsa_debug_build: 1 in the debug build, 0 in the release build.
+ *  - tsa_debug_check_selftest: queues on the stream one kernel whose TMEM
+ *    column check fails on purpose (columns 510..525 of 512; only the check
+ *    runs, no TMEM is allocated or touched), so that the next tsa_sync_status
+ *    returns TSA_ERR_DEVICE_CHECK. TSA_ERR_UNSUPPORTED in the release build. */
+int tsa_debug_build(void);
+tsa_status tsa_debug_check_selftest(void* cuda_stream);
 
 const char* tsa_status_string(tsa_status s);
 const char* tsa_last_error(void);

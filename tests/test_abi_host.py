@@ -183,3 +183,21 @@ def test_chunk_lengths_built(T):
     with pytest.raises(T.TsaError) as e:
         T.prefill_plan(T.Config(1, 8, 16, 64, 3, "f32", 256), 8192, num_sms=148)
     assert e.value.status == T.TSA_ERR_UNSUPPORTED
+
+
+def test_release_and_debug_builds(T):
+    """The release library has no device checks (tsa_debug_build() == 0, the
+    self-test is refused before any launch); the debug build exports the same
+    symbols and reports itself as the debug build (host only)."""
+    assert T.LIB_PATH.endswith("libtsa.so") or os.environ.get("TSA_DEBUG") == "1"
+    if not T.debug_build():
+        assert T._lib.tsa_debug_check_selftest(None) == T.TSA_ERR_UNSUPPORTED
+        assert "debug build" in T.last_error()
+    assert T.status_string(T.TSA_ERR_DEVICE_CHECK) == "TSA_ERR_DEVICE_CHECK"
+    dbg_path = tsa_build.build(debug=True)
+    lib = ctypes.CDLL(dbg_path)
+    lib.tsa_debug_build.restype = ctypes.c_int
+    assert lib.tsa_debug_build() == 1
+    out = os.popen(f"nm -D --defined-only {dbg_path}").read()
+    for name in _header_functions():
+        assert re.search(rf"\bT {name}$", out, flags=re.M), name
