@@ -233,16 +233,53 @@ def _oracle_head_prefill(args):
     return time.perf_counter() - t0
 
 
-def cpu_baseline_prefill(w, max_heads=None):
-    """The float64 oracle (recurrent form, as it stands) on one host core."""
+def cpu_baseline_prefill(w, inputs=None, max_heads=None):
+    """The float64 oracle (recurrent form, as it stands) on one host core.
+    With `inputs` (host float64 q, k, v of the GPU run, [heads, N, d]) it runs
+    on those and also returns its outputs and states per head, for the parity
+    figures; otherwise on freshly drawn inputs of the same recipe."""
+    from fixed_state_recurrence_phi_b300.inputs import np_qkv
+    from oracle import tsa_oracle as O
     heads = w["B"] * w["H"] if max_heads is None else max_heads
-    t = sum(_oracle_head_prefill((w, h)) for h in range(heads))
+    t, refs = 0.0, []
+    for h in range(heads):
+        if inputs is None:
+            q, k, v = np_qkv(w["N"], w["d_k"], w["d_v"], seed=[w["seed"], h])
+        else:
+            q, k, v = inputs[0][h], inputs[1][h], inputs[2][h]
+        t0 = time.perf_counter()
+        refs.append(O.prefill_recurrent(q, k, v, w["n_terms"]))
+        t += time.perf_counter() - t0
     per_head = t / heads
     all_heads = w["B"] * w["H"]
+    src = "the GPU run's own inputs" if inputs is not None else "inputs of the same recipe"
     return {"value": w["B"] * w["N"] / (per_head * all_heads), "unit": "tokens/s", "cores": 1,
             "kind": "oracle",
             "sample": f"recurrent float64 prefill, {heads} of {all_heads} heads x {w['N']} tokens on 1 "
-                      f"core; tokens/s = B*N / (mean head time x {all_heads} heads)"}
+                      f"core ({src}); tokens/s = B*N / (mean head time x {all_heads} heads)"}, refs
+
+
+def parity_vs_oracle(out_g, S_g, refs, dv, tol):
+    """The timed call's results against the oracle's, per head: normwise
+    max|g - r| / max|r| (the parity measure, tolerance `tol`) and elementwise
+    |g - r| / |r| over the elements with |r| >= 1% of max|r|, for the outputs,
+    the state's value part and its normaliser column (worst head of each)."""
+    def pair(g, r):
+        a = float(np.abs(r).max())
+        d = np.abs(g - r)
+        big = np.abs(r) >= 0.01 * a
+        return float(d.max() / a), float((d[big] / np.abs(r[big])).max())
+    worst = {"out": [0.0, 0.0], "state": [0.0, 0.0], "normaliser": [0.0, 0.0]}
+    for h, (o_r, S_r) in enumerate(refs):
+        for key, g, r in (("out", out_g[h], o_r), ("state", S_g[h][:, :dv], S_r[:, :dv]),
+                          ("normaliser", S_g[h][:, dv], S_r[:, dv])):
+            nw, ew = pair(g, r)
+            worst[key] = [max(worst[key][0], nw), max(worst[key][1], ew)]
+    r3 = lambda x: float(f"{x:.3g}")
+    return {"heads": len(refs), "tol_normwise": tol,
+            "normwise": {k: r3(v[0]) for k, v in worst.items()},
+            "elementwise_ge_1pct": {k: r3(v[1]) for k, v in worst.items()},
+            "ok": all(v[0] <= tol for v in worst.values())}
 
 
 def cpu_baseline_prefill_cores(w):
@@ -366,6 +403,7 @@ def _run_ours(args, clk):
     timing = "n/a"
     dec_us = eager_us = long_prefill_ms = merge_ms = float("nan")
     append_lines = []
+    pre_result = None
     steps, reps = 1024, 3
     dw = DECODE
     dcfg = T.Config(dw["B"], dw["H"], dw["d_k"], dw["d_v"], dw["n_terms"], dw["dtype"])
@@ -395,6 +433,10 @@ def _run_ours(args, clk):
           torch.cuda.synchronize()
           host_us = statistics.median(hs)
           ms_eager = ms
+          if ws == 1 and not args.no_cpu_baseline:
+              # the timed call's results, checked against the oracle below
+              pre_result = (out[0].double().cpu().numpy(), T.canonical_states(cfg, st)[0].double().cpu().numpy(),
+                            [x[0].double().cpu().numpy() for x in (q, k, v)])
 
           # the same call captured once in a CUDA graph and replayed: device
           # time of the step, independent of how fast the host issues it
@@ -695,9 +737,11 @@ def _run_ours(args, clk):
     ach = pre_bytes / (ms / 1e3) / 1e9 if do_pre else float("nan")
     if rank != 0:
         return
-    cpu = None
+    cpu = parity = None
     if ws == 1 and do_pre and not args.no_cpu_baseline:
-        cpu = cpu_baseline_prefill(w)
+        cpu, refs = cpu_baseline_prefill(w, inputs=pre_result[2] if pre_result else None)
+        if pre_result:
+            parity = parity_vs_oracle(pre_result[0], pre_result[1], refs, w["d_v"], 1e-4)
         cpu["legs"] = [dict(cpu_baseline_prefill_cores(w), what="prefill, heads over cores")]
         if do_dec:
             cpu["legs"].append(dict(cpu_baseline_decode(dw), what=f"decode step, {dw['workload']}"))
@@ -729,6 +773,8 @@ def _run_ours(args, clk):
         "orders": [{"n": o["n_terms"], "ms": r3(o["ms"]), "state_B_per_head": o["state_bytes_per_head"],
                     "path": o["path"]} for o in order_lines],
         "merge": {"ms": r3(merge_ms), "GBps": r3(3 * T.state_bytes(dcfg) / (merge_ms / 1e3) / 1e9)},
+        # the timed 8192-token call against the float64 oracle, every head
+        "parity": parity,
         "chunks": [{"chunk": c_["chunk"], "ms": r3(c_["ms"]), "path": c_["path"], "n_spans": c_["n_spans"]}
                    for c_ in chunk_lines],
         "prefill_tensor_core": [

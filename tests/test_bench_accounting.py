@@ -43,3 +43,25 @@ def test_tensor_core_flops():
     assert order4 == 550_099_746_816 and wide == 1_300_586_561_536
     assert b._algorithmic_prefill_flops(b.ORDER4) == order4
     assert b._algorithmic_prefill_flops(b.WIDE) == wide
+
+
+def test_parity_figures():
+    """The bench's parity figures: normwise max|g-r|/max|r| and elementwise
+    |g-r|/|r| over the elements with |r| >= 1% of max|r|, worked by hand."""
+    import numpy as np
+    b = _bench()
+    dv = 2
+    o_r = np.array([[1.0, -2.0], [0.5, 0.001]])          # 0.001 is under 1% of 2.0
+    S_r = np.array([[4.0, 1.0, 10.0], [2.0, -1.0, 5.0]])  # value part | normaliser column
+    o_g = o_r.copy(); o_g[1, 0] = 0.51; o_g[1, 1] = 0.011   # |d| 0.01 (rel 0.02) and 0.01 (excluded)
+    S_g = S_r.copy(); S_g[0, 1] = 1.004                      # |d| 0.004, rel 0.004; normwise 0.004/4
+    p = b.parity_vs_oracle([o_g], [S_g], [(o_r, S_r)], dv, 1e-4)
+    assert p["heads"] == 1
+    assert abs(p["normwise"]["out"] - 0.01 / 2.0) < 1e-12
+    assert abs(p["elementwise_ge_1pct"]["out"] - 0.02) < 1e-12
+    assert abs(p["normwise"]["state"] - 0.001) < 1e-12
+    assert abs(p["elementwise_ge_1pct"]["state"] - 0.004) < 1e-12
+    assert p["normwise"]["normaliser"] == 0.0 and p["elementwise_ge_1pct"]["normaliser"] == 0.0
+    assert p["ok"] is False
+    exact = b.parity_vs_oracle([o_r], [S_r], [(o_r, S_r)], dv, 1e-4)
+    assert exact["ok"] and max(exact["normwise"].values()) == 0.0
