@@ -435,33 +435,59 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
   const uint32_t col_O = (uint32_t)(NB * nm);
   const int i = wq * 32 + lane;   // TMEM lane = query row / feature row of a block
 
-  // initial state: span prefix (several spans), caller's state (ACCUMULATE) or 0
+  // the first chunk's q, k, v at once: they land while the state is read
+  if (warp == 8 && u.n_chunks > 0) {
+    tc_issue_qk(L, smem, B.qkfull(), &tm_q, &tm_k, u.t_begin, u.head, DK);
+    tc_issue_v(L, smem, B.vfull(0), 0, &tm_v, u.t_begin, u.head, u.c0, W);
+    __syncwarp();
+  }
+  // initial state: span prefix (several spans), caller's state (ACCUMULATE) or 0;
+  // thread = feature row, its half of the column groups, up to three groups'
+  // 16-byte loads in flight at once
   if (tid < TC_WORKERS) {
     const float* src = nullptr;
     if (!single) src = p.scratch + ((size_t)u.head * p.n_spans + u.span) * st_elems;
     else if (p.accumulate) src = p.states + (size_t)u.head * st_elems;
+    constexpr int GB = 3;
     for (int f = 0; f < NB; ++f) {
       const int a = f * 128 + i;
-      for (int g = half; g < nm / 16; g += 2) {
-        float v[16];
+      const bool have = src != nullptr && a < D;
+      for (int g0 = half; g0 < nm / 16; g0 += 2 * GB) {
+        float4 x[GB][4];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c = g * 16 + e;
-          float x = 0.0f;
-          if (src != nullptr && a < D) {
-            if (c < W && TSA_DCHECK_STATE((size_t)a * p.dv + u.c0 + c, 1, (size_t)DPAD * p.dv))
-              x = src[(size_t)a * p.dv + u.c0 + c];
-            else if (c == W) x = src[(size_t)DPAD * p.dv + a];
+        for (int j = 0; j < GB; ++j) {
+          const int g = g0 + 2 * j;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[j][e] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (have && g < nm / 16) {
+            if (g * 16 < W) {
+              if (TSA_DCHECK_STATE((size_t)a * p.dv + u.c0 + g * 16, 16, (size_t)DPAD * p.dv)) {
+                const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)a * p.dv + u.c0 + g * 16);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) x[j][e] = s4[e];
+              }
+            } else if (g * 16 == W) {
+              x[j][0].x = src[(size_t)DPAD * p.dv + a];
+            }
           }
-          v[e] = x;
         }
-        uint32_t r[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(v[e]);
-        tc::tmem_st16(tm + lane_off + f * nm + g * 16, r);
-        uint8_t* d = sS + f * L.sblk + i * 16;
-        *reinterpret_cast<uint4*>(d + (2 * g) * 2048) = tc_pack8(v);
-        *reinterpret_cast<uint4*>(d + (2 * g + 1) * 2048) = tc_pack8(v + 8);
+        for (int j = 0; j < GB; ++j) {
+          const int g = g0 + 2 * j;
+          if (g >= nm / 16) break;
+          float v[16];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            v[4 * e] = x[j][e].x; v[4 * e + 1] = x[j][e].y; v[4 * e + 2] = x[j][e].z; v[4 * e + 3] = x[j][e].w;
+          }
+          uint32_t r[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(v[e]);
+          tc::tmem_st16(tm + lane_off + f * nm + g * 16, r);
+          uint8_t* d = sS + f * L.sblk + i * 16;
+          *reinterpret_cast<uint4*>(d + (2 * g) * 2048) = tc_pack8(v);
+          *reinterpret_cast<uint4*>(d + (2 * g + 1) * 2048) = tc_pack8(v + 8);
+        }
       }
     }
     tc::tmem_wait_st();
@@ -492,9 +518,7 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
       };
       bool ok = true;
       if (u.n_chunks > 0) {
-        tc_issue_qk(L, smem, B.qkfull(), &tm_q, &tm_k, u.t_begin, u.head, DK);
-        tc_issue_v(L, smem, B.vfull(0), 0, &tm_v, u.t_begin, u.head, u.c0, W);
-        qk_req = v_req = 1;
+        qk_req = v_req = 1;   // issued before the initial state was read
         ok = tc_wait_warp(B, B.qkfull(), 0u);
         if (ok) {
           ++qk_got;
