@@ -111,6 +111,20 @@ bool tc_slicing(int dk, int nt, int dv, TcSlicing* ts) {
   return ts->smem <= kSmemLimit;
 }
 
+// The slim single-chunk form (span_output_tc_kernel<..., K64 = true>): the
+// state, a 64-key score block and O in 256 TMEM columns, one ring slot and one
+// v buffer, two CTAs per SM.
+bool tc_slim_fits(int dk, int nt, int dv, size_t* smem) {
+  TcSlicing ts;
+  if (!tc_slicing(dk, nt, dv, &ts) || ts.n_slices != 1) return false;
+  const int nm = dv + 16;
+  if (ts.nb > 2 || ts.nb * nm + std::max(64, nm) > kTmemCols / 2) return false;
+  const size_t s = TcSmem(dk, ts.nmax, ts.nb, 1, 1).total;
+  if (s + 1024 > kSmemLimit / 2) return false;
+  if (smem) *smem = s;
+  return true;
+}
+
 bool tc_supported(int dk, int nt) {
   return (dk == 16 && nt >= 1 && nt <= 4) || (dk == 32 && nt >= 1 && nt <= 3);
 }
@@ -208,6 +222,21 @@ tsa_status launch_tc(const tsa_plan& pl, const TcSlicing& ts, const PrefillParam
   if ((st = make_tmap(&mk, pp.k, DK, pp.N, pp.heads, DK / 8)) != TSA_OK) return st;
   if ((st = make_tmap(&mv, pp.v, pp.dv, pp.N, pp.heads, 2)) != TSA_OK) return st;
   const unsigned grid = (unsigned)((long long)pp.heads * ts.n_slices * pl.n_spans);
+  if constexpr (FeatConst<DK, NT>::NB <= 2) {
+    if (pl.ctas_per_sm == 2) {   // the slim single-chunk form (tc_slim_fits)
+      size_t slim = 0;
+      if (pl.n_spans != 1 || pp.N > 64 || !tc_slim_fits(DK, NT, pp.dv, &slim))
+        return fail(TSA_ERR_UNSUPPORTED, "two CTAs per SM only for one chunk of up to 64 tokens");
+      p.ring = 1;
+      cudaError_t e = set_smem(span_output_tc_kernel<__nv_bfloat16, DK, NT, true>, (int)slim);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_output_tc, slim)");
+      span_output_tc_kernel<__nv_bfloat16, DK, NT, true><<<grid, TC_THREADS, slim, s>>>(p, mq, mk, mv);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return cuda_fail(e, "launch span_output_tc (slim)");
+      return TSA_OK;
+    }
+  }
+  if (pl.ctas_per_sm != 1) return fail(TSA_ERR_UNSUPPORTED, "no slim form for d_k=%d n=%d", DK, NT);
   const int smem = (int)ts.smem;
   cudaError_t e = set_smem(span_output_tc_kernel<__nv_bfloat16, DK, NT>, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_output_tc)");

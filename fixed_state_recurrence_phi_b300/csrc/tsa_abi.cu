@@ -290,7 +290,15 @@ tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl
         pl->cluster = cs;
         return st;
       }
-      return make_plan_tc(c, N, num_sms, ts, pl, TSA_PATH_TC);
+      tsa_status st = make_plan_tc(c, N, num_sms, ts, pl, TSA_PATH_TC);
+      // one chunk of at most 64 tokens (a short append): the slim form, two
+      // CTAs per SM
+      size_t slim = 0;
+      if (st == TSA_OK && N <= 64 && pl->n_spans == 1 && tc_slim_fits(c->d_k, c->n_terms, c->d_v, &slim)) {
+        pl->ctas_per_sm = 2;
+        pl->smem_bytes = slim;
+      }
+      return st;
     }
   }
   if (c->dtype == TSA_F32 && tc32_fits(c->d_k, c->n_terms, c->d_v) && (c->chunk == 0 || c->chunk == 128)) {

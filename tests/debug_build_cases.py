@@ -115,6 +115,7 @@ def main():
     prefill_case(16, 64, 3, "f32", 500, chunk=64, expect_path=T.TSA_PATH_SIMT)
     prefill_case(16, 64, 3, "f32", 16, expect_path=T.TSA_PATH_SHORT, accumulate_pre=40)
     prefill_case(16, 64, 3, "bf16", 200, accumulate_pre=129)
+    prefill_case(16, 64, 3, "bf16", 50, H=4, accumulate_pre=100)   # the slim single-chunk form
     decode_merge_states_case()
     feature_map_case()
     print("debug build ok")
