@@ -208,7 +208,7 @@ static constexpr size_t kSmemPerSm = 228 * 1024;
 // TMEM budget, one CTA per SM. A span-state chunk costs about half an output
 // chunk (phi(K) and the update only).
 static tsa_status make_plan_tc(const tsa_config* c, long long N, int num_sms, const TcSlicing& ts,
-                               tsa_plan* pl, int path) {
+                               tsa_plan* pl, int path, size_t max_scratch) {
   const int chunk = 128;
   const long long heads = (long long)c->B * c->H;
   const long long n_chunks = (N + chunk - 1) / chunk;
@@ -226,7 +226,7 @@ static tsa_status make_plan_tc(const tsa_config* c, long long N, int num_sms, co
     // write, prefix read): charged at ~6 TB/s against ~4 us per chunk step
     const double scratch_bytes = (double)heads * s_eff * state_floats_per_head(c) * 4.0;
     const double scratch_cost = s_eff > 1 ? 2.0 + 4.0 * scratch_bytes / 6e12 / 4e-6 : 0.0;
-    if (s_eff > 1 && scratch_bytes > (double)(1ull << 30)) continue;
+    if (s_eff > 1 && (scratch_bytes > (double)(1ull << 30) || scratch_bytes > (double)max_scratch)) continue;
     const double cost = (double)waves * cps * (s_eff > 1 ? 1.5 : 1.0) + scratch_cost;
     if (cost < best_cost - 1e-9) { best_cost = cost; best_s = (int)s_eff; }
   }
@@ -250,7 +250,7 @@ static tsa_status make_plan_tc(const tsa_config* c, long long N, int num_sms, co
 // chooses (chunk = 0); chunk = 16 asks for it at any length.
 static constexpr long long kShortAutoMaxN = 32;
 
-tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl) {
+tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl, size_t max_scratch) {
   memset(pl, 0, sizeof(*pl));
   // Short segments: each head's state stays in shared memory for the whole
   // segment (read once, written once), 16-token blocks on the CUDA cores.
@@ -284,13 +284,13 @@ tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl
         tp.n_slices = cs;   // CTAs per (head, span), for the cost of the plan
         tp.w[0] = c->d_v;
         tp.smem = psmem;
-        tsa_status st = make_plan_tc(c, N, num_sms, tp, pl, TSA_PATH_TC);
+        tsa_status st = make_plan_tc(c, N, num_sms, tp, pl, TSA_PATH_TC, max_scratch);
         pl->n_slices = 1;
         pl->slice_width = c->d_v;
         pl->cluster = cs;
         return st;
       }
-      tsa_status st = make_plan_tc(c, N, num_sms, ts, pl, TSA_PATH_TC);
+      tsa_status st = make_plan_tc(c, N, num_sms, ts, pl, TSA_PATH_TC, max_scratch);
       // one chunk of at most 64 tokens (a short append): the slim form, two
       // CTAs per SM
       size_t slim = 0;
@@ -309,7 +309,7 @@ tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl
     ts.w[0] = c->d_v;
     ts.nmax = c->d_v + 16;
     ts.smem = tc32_smem(c->d_k, c->n_terms, c->d_v);
-    return make_plan_tc(c, N, num_sms, ts, pl, TSA_PATH_TC_F32);
+    return make_plan_tc(c, N, num_sms, ts, pl, TSA_PATH_TC_F32, max_scratch);
   }
   const int chunk = 64;
   if (c->chunk != 0 && c->chunk != chunk)
@@ -333,6 +333,7 @@ tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl
     const long long waves = (units * s_eff + slots - 1) / slots;
     // span_state costs about 0.45 of a span_output chunk; the scan and the
     // two extra launches about one chunk.
+    if (s_eff > 1 && (double)heads * s_eff * state_floats_per_head(c) * 4.0 > (double)max_scratch) continue;
     const double cost = (double)waves * cps * (s_eff > 1 ? 1.45 : 1.0) + (s_eff > 1 ? 1.0 : 0.0);
     if (cost < best_cost - 1e-9) { best_cost = cost; best_s = (int)s_eff; }
   }

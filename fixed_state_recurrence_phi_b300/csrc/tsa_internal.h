@@ -1,5 +1,6 @@
 // tsa_internal.h -- host helpers shared by the translation units of libtsa.so.
 #pragma once
+#include <cstdint>
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 #include "../../include/tsa.h"
@@ -23,7 +24,10 @@ int device_sm_count();
 // Raise a kernel's dynamic shared-memory limit to `smem` bytes once per device
 // (the attribute call costs microseconds of host time per prefill otherwise).
 cudaError_t set_smem_once(const void* kernel, int smem);
-tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl);
+// max_scratch: only span counts whose scratch fits are considered (one span
+// needs none, so a plan always exists)
+tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl,
+                     size_t max_scratch = SIZE_MAX);
 tsa_status launch_prefill(const tsa_config* c, const tsa_plan& pl, PrefillParams p, cudaStream_t s);
 
 // Tensor-core prefill (prefill_tc.cu).

@@ -83,12 +83,12 @@ extern "C" tsa_status tsa_prefill_noalloc(const tsa_config* c, int64_t N, const 
   const int sms = device_sm_count();
   if (sms <= 0) return fail(TSA_ERR_CUDA, "no CUDA device");
   tsa_plan pl;
-  st = make_plan(c, (long long)N, sms, &pl);
+  // only span counts whose scratch fits the fixed array (fewer spans per head
+  // where tsa_prefill would use more)
+  st = make_plan(c, (long long)N, sms, &pl, kNoAllocScratchBytes);
   if (st != TSA_OK) return st;
-  if (pl.scratch_bytes > kNoAllocScratchBytes)
-    return fail(TSA_ERR_UNSUPPORTED,
-                "tsa_prefill_noalloc: this shape needs %zu bytes of scratch, more than the %zu-byte "
-                "static buffer; use tsa_prefill, or split the heads over several calls",
+  if (pl.scratch_bytes > kNoAllocScratchBytes)   // not reached: one span needs no scratch
+    return fail(TSA_ERR_UNSUPPORTED, "tsa_prefill_noalloc: plan needs %zu bytes of scratch (> %zu)",
                 pl.scratch_bytes, kNoAllocScratchBytes);
   PrefillParams p;
   p.q = q; p.k = k; p.v = v; p.out = out; p.states = states; p.scratch = nullptr;

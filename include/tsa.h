@@ -166,10 +166,11 @@ tsa_status tsa_prefill(const tsa_config* cfg, int64_t N, const void* q, const vo
  * whose memory budget belongs to its own allocator, a serving loop that must
  * not allocate after start-up, or a GPU without the stream-ordered allocator.
  * Its scratch is one fixed 16 MiB array in device memory that every GPU
- * loading libtsa.so holds until the process exits. Shapes whose plan needs
- * more scratch than that (tsa_prefill_plan's scratch_bytes > 16 MiB) are
- * rejected with TSA_ERR_UNSUPPORTED before any work is queued; shapes with a
- * single span per head need none.
+ * loading libtsa.so holds until the process exits. Its plan considers only
+ * span counts whose span states fit that array: where tsa_prefill's plan
+ * (tsa_prefill_plan) needs more scratch, this call splits each head into
+ * fewer spans (one span needs none), so every shape tsa_prefill takes runs,
+ * with the same results up to the rounding order of the span sums.
  *  - The first call on each device looks up the array's device address (once,
  *    with that device current); make that first call before any stream
  *    capture. The address is kept for the life of the process: after a

@@ -63,20 +63,22 @@ def test_noalloc_matches_prefill_on_two_calls(T):
             assert _rel(st, ref_st) <= tol, (cfg, call)
 
 
-def test_noalloc_refuses_oversize_plan(T):
-    # 64 fp32 heads of 65,536 tokens: the plan spreads each head over several
-    # spans, whose states need about 40 MiB of scratch on a 148-SM part
-    cfg = T.Config(1, 64, 16, 64, 3, "f32")
+def test_noalloc_caps_its_plan_at_the_static_scratch(T):
+    # 2 bf16 heads of order 4 and 65,536 tokens: tsa_prefill's plan spreads
+    # each head over spans whose states need about 17.8 MiB of scratch, more
+    # than the no-alloc array holds; the no-alloc call takes fewer spans and
+    # gives the same results (up to the rounding order of the span sums)
+    cfg = T.Config(1, 2, 16, 64, 4, "bf16")
     N = 65536
     plan = T.prefill_plan(cfg, N)
     assert plan["scratch_bytes"] > 16 << 20, plan
-    q = torch.zeros((1, 64, N, 16), dtype=torch.float32, device="cuda")
-    v = torch.zeros((1, 64, N, 64), dtype=torch.float32, device="cuda")
-    out = torch.full_like(v, 7.0)
-    st = T.new_states(cfg)
-    with pytest.raises(T.TsaError) as e:
-        T.prefill_noalloc(cfg, N, q, q, v, out, st)
-    assert e.value.status == T.TSA_ERR_UNSUPPORTED
-    assert "static buffer" in T.last_error()
-    torch.cuda.synchronize()
-    assert bool((out == 7.0).all())
+    from fixed_state_recurrence_phi_b300.inputs import torch_qkv
+    q, k, v = torch_qkv(1, 2, N, 16, 64, "bf16", seed=91, device="cuda")
+    out_a = torch.empty_like(v)
+    out_b = torch.empty_like(v)
+    st_a, st_b = T.new_states(cfg), T.new_states(cfg)
+    T.prefill(cfg, N, q, k, v, out_a, st_a)
+    T.prefill_noalloc(cfg, N, q, k, v, out_b, st_b)
+    T.sync_status()
+    assert _rel(out_b, out_a) <= 2e-2
+    assert _rel(st_b, st_a) <= 1e-4
