@@ -214,4 +214,21 @@ __device__ __forceinline__ void build_phi_half(int f, int half, const float (&x)
   }
 }
 
+// Quarter `qtr` (groups 4*qtr .. 4*qtr + 3) of feature block f for one token.
+template <int DK, int NT, int F = 0>
+__device__ __forceinline__ void build_phi_quarter(int f, int qtr, const float (&x)[DK + 1], uint8_t* row) {
+  if constexpr (F < FeatConst<DK, NT>::NB) {
+    if (f == F) {
+      switch (qtr) {
+        case 0: PhiGroups<DK, NT, F * 128, 4>::run(x, row); break;
+        case 1: PhiGroups<DK, NT, F * 128 + 32, 4>::run(x, row); break;
+        case 2: PhiGroups<DK, NT, F * 128 + 64, 4>::run(x, row); break;
+        default: PhiGroups<DK, NT, F * 128 + 96, 4>::run(x, row); break;
+      }
+      return;
+    }
+    build_phi_quarter<DK, NT, F + 1>(f, qtr, x, row);
+  }
+}
+
 }  // namespace tsa

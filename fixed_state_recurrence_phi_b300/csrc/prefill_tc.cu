@@ -112,14 +112,14 @@ bool tc_slicing(int dk, int nt, int dv, TcSlicing* ts) {
 }
 
 // The slim single-chunk form (span_output_tc_kernel<..., K64 = true>): the
-// state, a 64-key score block and O in 256 TMEM columns, one ring slot and one
-// v buffer, two CTAs per SM.
+// state, a 64-key score block and O in 256 TMEM columns, two 16 KB ring slots
+// and one v buffer, two CTAs per SM.
 bool tc_slim_fits(int dk, int nt, int dv, size_t* smem) {
   TcSlicing ts;
   if (!tc_slicing(dk, nt, dv, &ts) || ts.n_slices != 1) return false;
   const int nm = dv + 16;
   if (ts.nb > 2 || ts.nb * nm + std::max(64, nm) > kTmemCols / 2) return false;
-  const size_t s = TcSmem(dk, ts.nmax, ts.nb, 1, 1).total;
+  const size_t s = TcSmem(dk, ts.nmax, ts.nb, 2, 1, 16384).total;
   if (s + 1024 > kSmemLimit / 2) return false;
   if (smem) *smem = s;
   return true;
@@ -227,7 +227,7 @@ tsa_status launch_tc(const tsa_plan& pl, const TcSlicing& ts, const PrefillParam
       size_t slim = 0;
       if (pl.n_spans != 1 || pp.N > 64 || !tc_slim_fits(DK, NT, pp.dv, &slim))
         return fail(TSA_ERR_UNSUPPORTED, "two CTAs per SM only for one chunk of up to 64 tokens");
-      p.ring = 1;
+      p.ring = 2;
       cudaError_t e = set_smem(span_output_tc_kernel<__nv_bfloat16, DK, NT, true>, (int)slim);
       if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_output_tc, slim)");
       span_output_tc_kernel<__nv_bfloat16, DK, NT, true><<<grid, TC_THREADS, slim, s>>>(p, mq, mk, mv);

@@ -75,23 +75,31 @@ struct TcParams {
 // TMA while the current one is still read by the update MMAs), `ring` slots of
 // 32 KB, the bf16 state copy (NB blocks), then the barriers.
 struct TcSmem {
-  size_t xt, vt, s, sblk, bar, total;
+  size_t xt, vt, s, sblk, bar, total, tile;
   int ring, vbufs;
-  // vbufs: v tile buffers (2; 1 for a single-chunk segment)
-  __host__ __device__ TcSmem(int dk, int nmax, int nb, int ring_slots, int v_buffers = 2) {
+  // vbufs: v tile buffers (2; 1 for a single-chunk segment); tile: bytes of
+  // a ring slot (32 KB: 128 rows of 128 features; 16 KB: the 64 rows a short
+  // segment fills)
+  __host__ __device__ TcSmem(int dk, int nmax, int nb, int ring_slots, int v_buffers = 2,
+                             size_t tile_bytes = 32768) {
     ring = ring_slots;
     vbufs = v_buffers;
+    tile = tile_bytes;
     xt = (size_t)128 * dk * 2;
     vt = (size_t)128 * nmax * 2;
-    s = 2 * xt + (size_t)vbufs * vt + (size_t)ring * 32768;
+    s = 2 * xt + (size_t)vbufs * vt + (size_t)ring * tile;
     sblk = vt;
     bar = s + (size_t)nb * sblk;
     total = bar + 256;
+    // A readout MMA reads 128 rows (32 KB) from a slot: with 16 KB slots,
+    // rows 64..127 come from the bytes after it, which must be allocated
+    const size_t reach = 2 * xt + (size_t)vbufs * vt + (size_t)(ring - 1) * tile + 32768;
+    if (total < reach) total = reach;
   }
   __host__ __device__ size_t q() const { return 0; }
   __host__ __device__ size_t k() const { return xt; }
   __host__ __device__ size_t v(int b) const { return 2 * xt + b * vt; }
-  __host__ __device__ size_t slot(int r) const { return 2 * xt + (size_t)vbufs * vt + (size_t)r * 32768; }
+  __host__ __device__ size_t slot(int r) const { return 2 * xt + (size_t)vbufs * vt + (size_t)r * tile; }
 };
 
 // The d inputs of token t from a [e/8][t][8] bf16 tile, as fp32.
@@ -409,9 +417,12 @@ span_state_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
 //
 // K64: the slim form for a single chunk of at most 64 tokens (short appends
 // to existing states): scores and P over 64 keys, so that the state, the
-// shared A / O columns fit in 256 TMEM columns; one ring slot and one v
-// buffer (about 100 KB of shared memory); two CTAs per SM, whose latencies
-// overlap.
+// shared A / O columns fit in 256 TMEM columns; feature and P tiles of the 64
+// rows the chunk fills (16 KB ring slots, two of them) and one v buffer
+// (about 100 KB of shared memory); two CTAs per SM, whose latencies overlap.
+// The readout MMAs (M = 128) read rows 64..127 of a feature tile from the
+// 16 KB that follow its slot (the next slot or the state copy): those output
+// rows are past the segment and never stored.
 // ---------------------------------------------------------------------------
 template <typename T, int DK, int NT, bool K64 = false>
 __global__ void __launch_bounds__(TC_THREADS, K64 ? 2 : 1)
@@ -422,7 +433,8 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
   constexpr int KEYS = K64 ? 64 : 128;               // keys of a chunk's scores
   constexpr uint32_t TMEM_COLS = K64 ? 256u : 512u;
   extern __shared__ __align__(1024) uint8_t smem[];
-  const TcSmem L(DK, p.nmax, NB, p.ring, K64 ? 1 : 2);
+  const TcSmem L(DK, p.nmax, NB, p.ring, K64 ? 1 : 2, K64 ? 16384 : 32768);
+  constexpr uint32_t PSBO = K64 ? 1024u : 2048u;     // P tile: bytes between 8-row groups
   const TcBars B{reinterpret_cast<uint64_t*>(smem + L.bar)};
   uint8_t* sS = smem + L.s;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wq = warp & 3, half = (warp >> 2) & 1;
@@ -561,7 +573,7 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
         // O = P [V, 1]
         if (!(ok = ring.take(B, pos.s))) break;
         {
-          const uint64_t dP = tc::sdesc(tc::smem_u32(smem + L.slot(pos.s)), 128, 2048);
+          const uint64_t dP = tc::sdesc(tc::smem_u32(smem + L.slot(pos.s)), 128, PSBO);
 #pragma unroll
           for (int k = 0; k < KEYS / 16; ++k)
             tc::mma_bf16_elect(tm + col_O, dP + (uint64_t)(k * 16), dV + (uint64_t)(k * 16), id_pv, k > 0 ? 1u : 0u);
@@ -606,7 +618,8 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
     }
   } else {
     // ------------------------------ workers --------------------------------
-    const int t = tid & 127;
+    // feature tiles: token t, half of a block (K64: token t < 64, a quarter)
+    const int t = K64 ? (tid & 63) : (tid & 127);
     const int prow = (t / 8) * 2048 + (t % 8) * 16;
     const int row_hi = wq * 32 + 31;
     T* og = static_cast<T*>(p.out) + (size_t)u.head * p.N * p.dv + u.c0;
@@ -638,10 +651,10 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
       tc_warp_arrive(B.qkempty(), lane);
       if (!tc_wait_warp(B, B.qk(), c & 1u)) break;
       tc::fence_after_sync();
-      // P = mask(T_n(A)) -> bf16 ring slot: (i/8)*2048 + (j/8)*128 + (i%8)*16
+      // P = mask(T_n(A)) -> bf16 ring slot: (i/8)*PSBO + (j/8)*128 + (i%8)*16
       if (!ring.acquire(B, pos.s)) break;
       {
-        uint8_t* prow_p = smem + L.slot(pos.s) + (i / 8) * 2048 + (i % 8) * 16;
+        uint8_t* prow_p = smem + L.slot(pos.s) + (i / 8) * PSBO + (i % 8) * 16;
 #pragma unroll
         for (int q2 = 0; q2 < KEYS / 64; ++q2) {
           const int jb = half * (KEYS / 2) + 32 * q2;
@@ -710,7 +723,8 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
         float x[DK + 1];
 #pragma unroll
         for (int e = 0; e <= DK; ++e) x[e] = upd ? xk[e] : xq[e];
-        build_phi_half<DK, NT>(f, half, x, smem + L.slot(pos.s) + prow);
+        if constexpr (K64) build_phi_quarter<DK, NT>(f, tid >> 6, x, smem + L.slot(pos.s) + prow);
+        else build_phi_half<DK, NT>(f, half, x, smem + L.slot(pos.s) + prow);
         ring.release(B, pos.s, lane);
         pos.next();
       }
