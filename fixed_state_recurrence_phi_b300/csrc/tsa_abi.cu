@@ -247,15 +247,21 @@ static tsa_status make_plan_tc(const tsa_config* c, long long N, int num_sms, co
 }
 
 // Segments up to this length go to the short-segment prefill when the library
-// chooses (chunk = 0); chunk = 16 asks for it at any length.
+// chooses (chunk = 0): 16 tokens where the slim tensor-core form takes the
+// shape (bf16 inputs; it is faster from 17 tokens on 1,024 heads), 32
+// otherwise; chunk = 16 asks for it at any length.
 static constexpr long long kShortAutoMaxN = 32;
+static constexpr long long kShortAutoMaxNSlim = 16;
 
 tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl, size_t max_scratch) {
   memset(pl, 0, sizeof(*pl));
+  const bool slim_ok = c->dtype == TSA_BF16 && tc_supported(c->d_k, c->n_terms) &&
+                       tc_slim_fits(c->d_k, c->n_terms, c->d_v, nullptr);
+  const long long short_max = slim_ok ? kShortAutoMaxNSlim : kShortAutoMaxN;
   // Short segments: each head's state stays in shared memory for the whole
   // segment (read once, written once), 16-token blocks on the CUDA cores.
   if (short_supported(c->d_k, c->n_terms, c->d_v) &&
-      (c->chunk == 16 || (c->chunk == 0 && N <= kShortAutoMaxN))) {
+      (c->chunk == 16 || (c->chunk == 0 && N <= short_max))) {
     const size_t smem = short_smem(c->d_k, c->n_terms, c->d_v);
     pl->chunk = 16;
     pl->slice_width = c->d_v;

@@ -155,11 +155,11 @@ def test_tc_deterministic_and_padding_zero(G):
 
 
 def test_slim_plans(G):
-    """Segments of up to 64 tokens that one CTA holds whole take the slim
+    """Segments of 17 to 64 tokens that one CTA holds whole take the slim
     single-chunk form: two CTAs per SM, about 100 KB of shared memory."""
     T = G.T
     for d, dv, n in [(16, 64, 3), (32, 64, 2), (16, 32, 1)]:
-        for N in (33, 64):
+        for N in (17, 33, 64):
             p = T.prefill_plan(T.Config(64, 16, d, dv, n, "bf16"), N, num_sms=148)
             assert p["path"] == T.TSA_PATH_TC and p["ctas_per_sm"] == 2, (d, dv, n, N, p)
             assert p["smem_bytes"] + 1024 <= 227 * 1024 // 2 and p["n_spans"] == 1
@@ -169,7 +169,8 @@ def test_slim_plans(G):
     assert T.prefill_plan(T.Config(1, 2, 16, 128, 3, "bf16"), 64, num_sms=148)["ctas_per_sm"] == 1
 
 
-@pytest.mark.parametrize("d,dv,n,L", [(16, 64, 3, 33), (16, 64, 3, 64), (32, 64, 2, 50), (16, 32, 1, 64)])
+@pytest.mark.parametrize("d,dv,n,L", [(16, 64, 3, 17), (16, 64, 3, 32), (16, 64, 3, 33), (16, 64, 3, 64),
+                                      (32, 64, 2, 50), (16, 32, 1, 64)])
 def test_slim_append_many_heads(G, d, dv, n, L):
     """Appends of L tokens with ACCUMULATE to the states of a 300-token
     prefix, on 512 heads (several waves of two CTAs per SM): sampled heads
