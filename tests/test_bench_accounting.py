@@ -62,6 +62,9 @@ def test_parity_figures():
     assert abs(p["normwise"]["state"] - 0.001) < 1e-12
     assert abs(p["elementwise_ge_1pct"]["state"] - 0.004) < 1e-12
     assert p["normwise"]["normaliser"] == 0.0 and p["elementwise_ge_1pct"]["normaliser"] == 0.0
+    # all elements, |r| floored at 1e-6 max|r|: the small output 0.001 (error 0.01) dominates
+    assert abs(p["elementwise_floor_1e-6"]["out"] - float(f"{0.01 / (0.001 + 2e-6):.3g}")) < 1e-9
+    assert abs(p["elementwise_floor_1e-6"]["state"] - float(f"{0.004 / (1.0 + 4e-6):.3g}")) < 1e-12
     assert p["ok"] is False
     exact = b.parity_vs_oracle([o_r], [S_r], [(o_r, S_r)], dv, 1e-4)
     assert exact["ok"] and max(exact["normwise"].values()) == 0.0
