@@ -642,6 +642,10 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
       const long long t0 = u.t_begin + (long long)c * TC_C;
       const int valid = (int)min((long long)TC_C, u.t_end - t0);
       const bool need_update = single || (c + 1 < u.n_chunks);
+      // the bf16 copy of the updated state is the next chunk's readout operand;
+      // after the last chunk nothing reads it (the issuer's drain orders the
+      // final state store after the updates)
+      const bool need_copy = need_update && (c + 1 < u.n_chunks);
       if (!tc_wait_warp(B, B.qkfull(), c & 1u)) break;
       float xq[DK + 1], xk[DK + 1];
       tc_load_x<DK>(smem + L.q(), t, xq);
@@ -716,7 +720,7 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
         const bool upd = (k >= NB);
         const int f = upd ? k - NB : k;
         if (!(ok = ring.acquire(B, pos.s))) break;
-        if (upd && f >= pos.R) {   // the slot last held update f - R: convert that block
+        if (need_copy && upd && f >= pos.R) {   // the slot last held update f - R: convert that block
           tc::fence_after_sync();
           convert_block(f - pos.R);
         }
@@ -729,7 +733,7 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
         pos.next();
       }
       if (!ok) break;
-      if (need_update) {
+      if (need_copy) {
         for (int f = (NB > pos.R ? NB - pos.R : 0); f < NB; ++f) {
           const int s = (s_upd0 + f) % pos.R;
           if (!(ok = ring.acquire(B, s))) break;
