@@ -1,0 +1,485 @@
+// prefill_append.cuh -- a segment of at most 64 tokens appended to each
+// head's state (or started from zero) on the tensor cores, three CTAs per SM.
+//
+// The computation is one chunk step of prefill_tc.cuh (Expanding Attention,
+// arXiv 2610.20637 abstract: additive states, so a segment continues a prefix
+// through its state alone; Hacker News thread on the paper: (Q'K)V = Q'(KV)
+// and the "+1" normaliser column):
+//     A  = Q K^T                      P = mask_{j<=i}(T_n(A))
+//     O  = P [V, 1] + phi(Q) [S, z]   out = O[:, :W] / O[:, W]
+//     S' = S + phi(K)^T [V, 1]
+// but the fp32 state never enters tensor memory. Its bf16 copy, the B operand
+// of the readout, is built in shared memory from one TMA tile of the old
+// state; the update dS_f = phi(K_f)^T [V, 1] of each feature block is
+// accumulated from zero in TMEM and added to the old rows by the CUDA cores
+// on the way out (the old rows come back from L2, where the tile load left
+// them). A, O and each dS_f take turns in the same 128 TMEM columns, and the
+// CTA needs about 73 KB of shared memory, so three heads are in flight per SM.
+//
+// Shapes: bf16 q, k, v, d_v <= 64, at most two 128-feature blocks. The last
+// block's bf16 copy holds only its K_f = round_up(rows, 16) rows, and the
+// readout of that block runs over K_f features.
+//
+// Shared memory (no swizzle; byte offsets of element (row, col)):
+//   q    [e/8][t][8], 128 rows     (K-major A of Q K^T; rows >= N are zero)
+//   k    [e/8][t][8], 64 rows      (K-major B of Q K^T)
+//   v    [c/8][t][8], 64 rows      (MN-major B of P [V,1] and of the updates)
+//   slot 0, 1 (16 KB each): first the fp32 tile of block 0 of the old state,
+//        [c/4][a][4]; then P, phi(Q_f) and phi(K_f) in turn
+//        P   : (i/8)*1024 + (j/8)*128 + (i%8)*16 + (j%8)*2
+//        phi : (t/8)*2048 + (a/8)*128 + (t%8)*16 + (a%8)*2
+//   sS_f [c/8][a][8], K_f rows     (MN-major B of the readout of block f)
+// A readout MMA (M = 128) reads 128 token rows (32 KB) of a phi tile: rows
+// 64..127, past the segment, come from the bytes after the slot, which the
+// layout keeps allocated; those output rows are never stored.
+//
+// Warp roles as in prefill_tc.cuh: 8 worker warps and one issuer warp, hand-
+// offs through mbarriers only, every wait bounded; on time-out the CTA sets
+// the error word, stops, waits (bounded) for what it has in flight and frees
+// its TMEM.
+#pragma once
+#include <cuda.h>
+#include "common.cuh"
+#include "tc_ptx.cuh"
+#include "feature_build.cuh"
+#include "prefill_tc.cuh"
+
+namespace tsa {
+
+constexpr int APP_KEYS = 64;        // tokens of a segment at most
+constexpr uint32_t APP_TMEM_COLS = 128;
+
+// Byte offsets of the shared-memory regions (identical on host and device).
+struct AppSmem {
+  size_t q, k, v, slot0, s0, s1, bar, total;
+  int k0, k1;   // rows of the bf16 state copy of blocks 0 and 1
+  __host__ __device__ AppSmem(int dk, int dv, int D) {
+    const int nm = dv + 16;
+    const int r0 = D < 128 ? D : 128, r1 = D > 128 ? D - 128 : 0;
+    k0 = (r0 + 15) / 16 * 16;
+    k1 = (r1 + 15) / 16 * 16;
+    q = 0;
+    k = q + (size_t)128 * dk * 2;
+    v = k + (size_t)APP_KEYS * dk * 2;
+    slot0 = v + (size_t)APP_KEYS * nm * 2;
+    s0 = slot0 + 2 * 16384;
+    s1 = s0 + (size_t)(nm / 8) * k0 * 16;
+    bar = s1 + (size_t)(nm / 8) * k1 * 16;
+    total = bar + 256;
+    const size_t reach = slot0 + 16384 + 32768;   // a readout of slot 1 reads 32 KB
+    if (total < reach) total = reach;
+  }
+  __host__ __device__ size_t slot(int s) const { return slot0 + (size_t)s * 16384; }
+};
+
+// mbarriers (shared memory, in this order) and their arrival counts:
+//   qkfull   q, k tiles landed                         (1 + tx)
+//   vfull    v tile landed                             (1 + tx)
+//   stfull   the old state's block-0 tile landed       (1 + tx)
+//   sready   workers wrote the bf16 state copy         (8)
+//   qk       A = Q K^T is in TMEM                      (1, commit)
+//   sfull[2] workers wrote slot s                      (8)
+//   sempty[2] the MMAs reading slot s are done         (1, commit)
+//   odone    O is complete                             (1, commit)
+//   ofree    workers have read O                       (8)
+//   upd      dS_f is complete (phase f)                (1, commit)
+//   dfree    workers have read dS_0                    (8)
+//   drain    every MMA issued is done                  (1, commit)
+struct AppBars {
+  uint64_t* b;
+  __device__ uint64_t* qkfull() const { return b + 0; }
+  __device__ uint64_t* vfull() const { return b + 1; }
+  __device__ uint64_t* stfull() const { return b + 2; }
+  __device__ uint64_t* sready() const { return b + 3; }
+  __device__ uint64_t* qk() const { return b + 4; }
+  __device__ uint64_t* sfull(int s) const { return b + 5 + s; }
+  __device__ uint64_t* sempty(int s) const { return b + 7 + s; }
+  __device__ uint64_t* odone() const { return b + 9; }
+  __device__ uint64_t* ofree() const { return b + 10; }
+  __device__ uint64_t* upd() const { return b + 11; }
+  __device__ uint64_t* dfree() const { return b + 12; }
+  __device__ uint64_t* drain() const { return b + 13; }
+  __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(b + 16); }
+  __device__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(b + 16) + 1; }
+  __device__ uint64_t* wait_limit() const { return b + 24; }
+  __device__ void init(uint64_t wait_ns) const {
+    const uint32_t cnt[14] = {1, 1, 1, 8, 1, 8, 8, 1, 1, 1, 8, 1, 8, 1};
+    for (int k = 0; k < 14; ++k) tc::mbar_init(b + k, cnt[k]);
+    *abort_flag() = 0;
+    *wait_limit() = wait_ns;
+    tc::mbar_fence_init();
+  }
+  __device__ bool wait(uint64_t* bar, uint32_t parity) const {
+    return tc::mbar_wait_or_abort(bar, parity, *wait_limit(), abort_flag());
+  }
+  // a warp waits as one: if any lane gives up, the whole warp does
+  __device__ bool wait_warp(uint64_t* bar, uint32_t parity) const {
+    return __all_sync(0xffffffffu, wait(bar, parity));
+  }
+};
+
+// 8 fp32 values -> 8 bf16 (16 bytes)
+__device__ __forceinline__ uint4 app_pack8(float4 a, float4 b) {
+  return make_uint4(tc::pack_bf16x2(a.x, a.y), tc::pack_bf16x2(a.z, a.w), tc::pack_bf16x2(b.x, b.y),
+                    tc::pack_bf16x2(b.z, b.w));
+}
+
+// The d inputs of token t from a [e/8][t][8] bf16 tile of `rows` rows, as fp32.
+template <int DK>
+__device__ __forceinline__ void app_load_x(const uint8_t* tile, int rows, int t, float (&x)[DK + 1]) {
+#pragma unroll
+  for (int g = 0; g < DK / 8; ++g) {
+    const uint4 u = *reinterpret_cast<const uint4*>(tile + (size_t)g * rows * 16 + t * 16);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[8 * g + 2 * e] = __uint_as_float(w[e] << 16);
+      x[8 * g + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// append_tc_kernel: one CTA per head (grid = heads), the whole segment of
+// p.N <= 64 tokens as one chunk; the state read (ACCUMULATE) or zero, and
+// written back.
+// ---------------------------------------------------------------------------
+template <int DK, int NT>
+__global__ void __launch_bounds__(TC_THREADS, 3)
+append_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_s) {
+  using FC = FeatConst<DK, NT>;
+  constexpr int D = FC::D, NB = FC::NB, DPAD = round_up(D, 4);
+  constexpr int R0 = D < 128 ? D : 128;       // feature rows of block 0
+  constexpr int R1 = D > 128 ? D - 128 : 0;   // ... of block 1
+  static_assert(NB <= 2, "the append form holds at most two feature blocks");
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int W = p.dv, nm = W + 16, G8 = W / 8;
+  const AppSmem L(DK, W, D);
+  const int K0 = L.k0, K1 = L.k1;
+  const AppBars B{reinterpret_cast<uint64_t*>(smem + L.bar)};
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wq = warp & 3, half = (warp >> 2) & 1;
+  const int head = blockIdx.x;
+  const int valid = (int)p.N;
+  const size_t st_elems = (size_t)DPAD * (W + 1);
+  const float* src = p.accumulate ? p.states + (size_t)head * st_elems : nullptr;
+  float* dst = p.states + (size_t)head * st_elems;
+  TSA_DCHECK(head < p.heads && valid <= APP_KEYS, dbg::kWorkUnit, head, valid);
+
+  if (warp == 0) tc::tmem_alloc(B.tmem_slot(), APP_TMEM_COLS);
+  if (tid == 0) B.init(p.wait_ns);
+  // the ones column of the value tile: column W is 1, W+1..W+15 zero
+  if (tid < TC_WORKERS) {
+    for (int e = tid; e < APP_KEYS * 2; e += TC_WORKERS) {
+      const int t = e >> 1, g = e & 1;
+      *reinterpret_cast<uint4*>(smem + L.v + (size_t)(G8 + g) * (APP_KEYS * 16) + t * 16) =
+          make_uint4(g == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
+    }
+  }
+  tc::fence_proxy_async();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tm = *B.tmem_slot();
+  const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+  const int i = wq * 32 + lane;   // TMEM lane: query row / feature row of a block
+
+  if (warp == 8) {
+    // ------------------------------ issuer ---------------------------------
+    const int n_st = src ? 1 : 0;
+    if (tc::elect_one()) {
+      // the small q, k, v tiles first: the scores and P need them before the
+      // state copy is built
+      tc::mbar_arrive_expect_tx(B.qkfull(), (uint32_t)((128 + APP_KEYS) * DK * 2));
+      tc::tma_load_4d(smem + L.q, &tm_q, B.qkfull(), 0, 0, 0, head);
+      tc::tma_load_4d(smem + L.k, &tm_k, B.qkfull(), 0, 0, 0, head);
+      tc::mbar_arrive_expect_tx(B.vfull(), (uint32_t)(APP_KEYS * W * 2));
+      for (int u = 0; u < W / 16; ++u)
+        tc::tma_load_4d(smem + L.v + (size_t)u * (2 * APP_KEYS * 16), &tm_v, B.vfull(), 0, 0, 2 * u, head);
+      if (src) {
+        tc::mbar_arrive_expect_tx(B.stfull(), (uint32_t)(R0 * W * 4));
+        tc::tma_load_4d(smem + L.slot0, &tm_s, B.stfull(), 0, 0, 0, head);
+      }
+    }
+    __syncwarp();
+    const uint32_t id_qk = tc::idesc_bf16(128, APP_KEYS, false, false);
+    const uint32_t id_pv = tc::idesc_bf16(128, nm, false, true);
+    const uint32_t id_up = tc::idesc_bf16(128, nm, true, true);
+    const uint64_t dQ = tc::sdesc(tc::smem_u32(smem + L.q), 128 * 16, 128);
+    const uint64_t dK = tc::sdesc(tc::smem_u32(smem + L.k), APP_KEYS * 16, 128);
+    const uint64_t dV = tc::sdesc(tc::smem_u32(smem + L.v), 128, APP_KEYS * 16);
+    int qk_got = 0, v_got = 0, st_got = 0;
+    uint32_t fph = 0;   // sfull phase per slot
+    auto take = [&](int s) {
+      const bool r = B.wait_warp(B.sfull(s), (fph >> s) & 1u);
+      fph ^= 1u << s;
+      tc::fence_after_sync();
+      return r;
+    };
+    bool ok = B.wait_warp(B.qkfull(), 0u);
+    if (ok) {
+      ++qk_got;
+      tc::fence_after_sync();
+#pragma unroll
+      for (int kk = 0; kk < DK / 16; ++kk)
+        tc::mma_bf16_elect(tm, dQ + (uint64_t)(kk * 256), dK + (uint64_t)(kk * 128), id_qk, kk > 0 ? 1u : 0u);
+      tc::mma_commit_elect(B.qk());
+    }
+    if (ok && (ok = B.wait_warp(B.vfull(), 0u))) ++v_got;
+    // O = P [V, 1]   (use 0: slot 0)
+    if (ok && (ok = take(0))) {
+      const uint64_t dP = tc::sdesc(tc::smem_u32(smem + L.slot(0)), 128, 1024);
+#pragma unroll
+      for (int kk = 0; kk < APP_KEYS / 16; ++kk)
+        tc::mma_bf16_elect(tm, dP + (uint64_t)(kk * 16), dV + (uint64_t)(kk * 16), id_pv, kk > 0 ? 1u : 0u);
+      tc::mma_commit_elect(B.sempty(0));
+    }
+    // O += phi(Q_f) [S_f, z_f]   (uses 1..NB), once the bf16 copy is written
+    if (ok) {
+      ok = B.wait_warp(B.sready(), 0u);
+      if (ok) st_got = n_st;   // the workers waited for the tile before sready
+    }
+    for (int f = 0; f < NB && ok; ++f) {
+      const int s = (1 + f) & 1;
+      if (!(ok = take(s))) break;
+      const uint64_t dA = tc::sdesc(tc::smem_u32(smem + L.slot(s)), 128, 2048);
+      const int kf = f == 0 ? K0 : K1;
+      const uint64_t dS = tc::sdesc(tc::smem_u32(smem + (f == 0 ? L.s0 : L.s1)), 128, (uint32_t)kf * 16);
+      for (int kk = 0; kk < kf / 16; ++kk)
+        tc::mma_bf16_elect(tm, dA + (uint64_t)(kk * 16), dS + (uint64_t)(kk * 16), id_pv, 1u);
+      tc::mma_commit_elect(B.sempty(s));
+    }
+    if (ok) tc::mma_commit_elect(B.odone());
+    // dS_f = phi(K_f)^T [V, 1]   (uses NB+1..2NB), each into the O columns
+    // once the workers have read what was there
+    for (int f = 0; f < NB && ok; ++f) {
+      const int s = (1 + NB + f) & 1;
+      if (!(ok = take(s))) break;
+      if (!(ok = B.wait_warp(f == 0 ? B.ofree() : B.dfree(), 0u))) break;
+      tc::fence_after_sync();
+      const uint64_t dA = tc::sdesc(tc::smem_u32(smem + L.slot(s)), 2048, 128);
+#pragma unroll
+      for (int kk = 0; kk < APP_KEYS / 16; ++kk)
+        tc::mma_bf16_elect(tm, dA + (uint64_t)(kk * 256), dV + (uint64_t)(kk * 16), id_up, kk > 0 ? 1u : 0u);
+      tc::mma_commit_elect(B.sempty(s));
+      tc::mma_commit_elect(B.upd());
+    }
+    // drain: every MMA issued and every load requested has completed
+    tc::mma_commit_elect(B.drain());
+    tc::mbar_wait(B.drain(), 0, TC_WAIT_NS);
+    if (qk_got == 0) tc::mbar_wait(B.qkfull(), 0, TC_WAIT_NS);
+    if (v_got == 0) tc::mbar_wait(B.vfull(), 0, TC_WAIT_NS);
+    if (st_got < n_st) tc::mbar_wait(B.stfull(), 0, TC_WAIT_NS);
+  } else {
+    // ------------------------------ workers --------------------------------
+    bool ok = true;
+    // (1) the bf16 copy of the old state. Block 1's rows and every z come by
+    // plain loads (issued first), block 0's values from the TMA tile.
+    float4 b1[2][2];
+    float zr = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      b1[j][0] = b1[j][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int u = tid + TC_WORKERS * j;
+      if (src != nullptr && NB == 2 && u < K1 * G8) {
+        const int a1 = u % K1, cg = u / K1;
+        if (a1 < R1) {
+          const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)(128 + a1) * W + cg * 8);
+          b1[j][0] = s4[0];
+          b1[j][1] = s4[1];
+        }
+      }
+    }
+    if (src != nullptr && tid < D) zr = src[(size_t)DPAD * W + tid];
+    if (src != nullptr) ok = B.wait_warp(B.stfull(), 0u);
+    {
+      const uint8_t* stg = smem + L.slot0;
+      for (int u = tid; u < K0 * G8; u += TC_WORKERS) {
+        const int a = u % K0, cg = u / K0;
+        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+        if (src != nullptr && ok && a < R0) {
+          x0 = *reinterpret_cast<const float4*>(stg + ((size_t)(2 * cg) * R0 + a) * 16);
+          x1 = *reinterpret_cast<const float4*>(stg + ((size_t)(2 * cg + 1) * R0 + a) * 16);
+        }
+        *reinterpret_cast<uint4*>(smem + L.s0 + (size_t)cg * K0 * 16 + a * 16) = app_pack8(x0, x1);
+      }
+      // the normaliser group (z, then zeros) and the padding group of each row
+      const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 zv = make_float4(zr, 0.f, 0.f, 0.f);
+      if (tid < K0) {
+        *reinterpret_cast<uint4*>(smem + L.s0 + (size_t)G8 * K0 * 16 + tid * 16) = app_pack8(zv, zero4);
+        *reinterpret_cast<uint4*>(smem + L.s0 + (size_t)(G8 + 1) * K0 * 16 + tid * 16) = app_pack8(zero4, zero4);
+      }
+      if (NB == 2) {
+        const int a1 = tid - 128;
+        if (a1 >= 0 && a1 < K1) {
+          *reinterpret_cast<uint4*>(smem + L.s1 + (size_t)G8 * K1 * 16 + a1 * 16) = app_pack8(zv, zero4);
+          *reinterpret_cast<uint4*>(smem + L.s1 + (size_t)(G8 + 1) * K1 * 16 + a1 * 16) = app_pack8(zero4, zero4);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int u = tid + TC_WORKERS * j;
+          if (u < K1 * G8) {
+            const int b1row = u % K1, cg = u / K1;
+            *reinterpret_cast<uint4*>(smem + L.s1 + (size_t)cg * K1 * 16 + b1row * 16) = app_pack8(b1[j][0], b1[j][1]);
+          }
+        }
+      }
+    }
+    tc::fence_proxy_async();
+    // every worker has read the staged tile before any writes slot 0 or 1
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    {
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(B.sready());
+    }
+    // (2) P = mask(T_n(A)) -> slot 0 (use 0)
+    if (ok) ok = B.wait_warp(B.qk(), 0u);
+    if (ok) {
+      tc::fence_after_sync();
+      uint8_t* prow_p = smem + L.slot(0) + (i / 8) * 1024 + (i % 8) * 16;
+      const int jb = half * 32;
+      if (jb <= wq * 32 + 31) {   // warp-uniform: 32 keys above the diagonal are zero
+        uint32_t rr[32];
+        tc::tmem_ld32(tm + lane_off + jb, rr);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          float pv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int j = jb + 8 * g + e;
+            pv[e] = (j <= i && i < valid) ? taylor_T<NT>(__uint_as_float(rr[8 * g + e])) : 0.0f;
+          }
+          *reinterpret_cast<uint4*>(prow_p + ((jb + 8 * g) / 8) * 128) = tc_pack8(pv);
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          *reinterpret_cast<uint4*>(prow_p + ((jb + 8 * g) / 8) * 128) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      tc::fence_proxy_async();
+      tc_warp_arrive(B.sfull(0), lane);
+    }
+    // (3) the token's inputs: thread = (token t, quarter of a feature block)
+    const int t = tid & 63, qtr = tid >> 6;
+    const int prow = (t / 8) * 2048 + (t % 8) * 16;
+    float xq[DK + 1], xk[DK + 1];
+    if (ok) ok = B.wait_warp(B.qkfull(), 0u);
+    app_load_x<DK>(smem + L.q, 128, t, xq);
+    app_load_x<DK>(smem + L.k, APP_KEYS, t, xk);
+    xq[DK] = 1.0f;
+    xk[DK] = (t < valid) ? 1.0f : 0.0f;
+    // Old state rows of block f for S' = S + dS_f (read back from L2): this
+    // thread's row a = f*128 + i, its column groups g = half, half + 2 and
+    // half + 4 (d_v <= 64: the third is at most the normaliser group).
+    float4 old[2][4];
+    float zold = 0.0f;
+    auto load_old = [&](int f) {
+      const int a = f * 128 + i;
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) old[j][e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      zold = 0.0f;
+      if (src == nullptr || a >= D) return;
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const int g = half + 2 * j;
+        if (j < 2 && g * 16 < W) {
+          const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)a * W + g * 16);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) old[j][e] = s4[e];
+        } else if (g * 16 == W) {
+          zold = src[(size_t)DPAD * W + a];
+        }
+      }
+    };
+    // (4) phi(Q_0..NB-1), then phi(K_0..NB-1): uses 1..2NB, slot = use % 2; a
+    // slot's earlier use must have been read by its MMAs
+    uint32_t eph = 0;
+    for (int use = 1; use <= 2 * NB && ok; ++use) {
+      const int s = use & 1;
+      if (use >= 2) {
+        if (!(ok = B.wait_warp(B.sempty(s), (eph >> s) & 1u))) break;
+        eph ^= 1u << s;
+      }
+      const bool upd = use > NB;
+      const int f = upd ? use - 1 - NB : use - 1;
+      float x[DK + 1];
+#pragma unroll
+      for (int e = 0; e <= DK; ++e) x[e] = upd ? xk[e] : xq[e];
+      build_phi_quarter<DK, NT>(f, qtr, x, smem + L.slot(s) + prow);
+      tc::fence_proxy_async();
+      tc_warp_arrive(B.sfull(s), lane);
+    }
+    // block 0's old rows, in flight while the readouts finish
+    load_old(0);
+    // out = O[:, :W] / O[:, W]  (rows i < valid live in warps 0, 1, 4, 5)
+    if (ok) ok = B.wait_warp(B.odone(), 0u);
+    if (ok) {
+      tc::fence_after_sync();
+      if (wq * 32 < valid) {
+        uint32_t rr[16];
+        tc::tmem_ld16(tm + lane_off + W, rr);
+        tc::tmem_wait_ld();
+        const float inv = 1.0f / __uint_as_float(rr[0]);
+        __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out) + ((size_t)head * p.N + i) * W;
+        for (int g = half; g < W / 16; g += 2) {
+          tc::tmem_ld16(tm + lane_off + g * 16, rr);
+          tc::tmem_wait_ld();
+          if (i < valid) {
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+              Elem<__nv_bfloat16>::store4(og + g * 16 + e,
+                                          make_float4(__uint_as_float(rr[e]) * inv, __uint_as_float(rr[e + 1]) * inv,
+                                                      __uint_as_float(rr[e + 2]) * inv,
+                                                      __uint_as_float(rr[e + 3]) * inv));
+          }
+        }
+      }
+      tc_warp_arrive(B.ofree(), lane);
+    }
+    // (5) S' = S + dS_f, block by block; rows D..DPAD-1 written as zeros
+    for (int f = 0; f < NB && ok; ++f) {
+      const int a = f * 128 + i;
+      if (f * 128 + wq * 32 >= DPAD) break;   // warp-uniform: no rows of this block
+      const bool live = a < D;
+      if (f > 0) load_old(f);
+      if (!(ok = B.wait_warp(B.upd(), (uint32_t)f))) break;
+      tc::fence_after_sync();
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const int g = half + 2 * j;
+        if (g >= nm / 16) break;
+        uint32_t rr[16];
+        tc::tmem_ld16(tm + lane_off + g * 16, rr);
+        tc::tmem_wait_ld();
+        if (a < DPAD) {
+          if (j < 2 && g * 16 < W) {
+            if (!TSA_DCHECK_STATE((size_t)a * W + g * 16, 16, (size_t)DPAD * W)) continue;
+            float4* o = reinterpret_cast<float4*>(dst + (size_t)a * W + g * 16);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              o[e] = live ? make_float4(old[j][e].x + __uint_as_float(rr[4 * e]),
+                                        old[j][e].y + __uint_as_float(rr[4 * e + 1]),
+                                        old[j][e].z + __uint_as_float(rr[4 * e + 2]),
+                                        old[j][e].w + __uint_as_float(rr[4 * e + 3]))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+          } else if (g * 16 == W) {
+            dst[(size_t)DPAD * W + a] = live ? zold + __uint_as_float(rr[0]) : 0.0f;
+          }
+        }
+      }
+      if (f == 0 && NB == 2) tc_warp_arrive(B.dfree(), lane);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (*B.abort_flag() != 0 && tid == 0) atomicExch(p.err, 1);
+  if (warp == 0) tc::tmem_dealloc(tm, APP_TMEM_COLS);
+}
+
+}  // namespace tsa

@@ -13,6 +13,7 @@
 
 #include "tsa_internal.h"
 #include "prefill_tc.cuh"
+#include "prefill_append.cuh"
 #include "prefill_simt.cuh"
 
 namespace tsa {
@@ -30,6 +31,7 @@ int* g_err_addr[64];
 bool g_err_ready[64];
 
 constexpr size_t kSmemLimit = 227 * 1024;
+constexpr size_t kSmemPerSm = 228 * 1024;
 constexpr int kTmemCols = 512;
 
 // Testing hooks (tsa_debug_set_wait_limit, tsa_debug_withhold_publication).
@@ -111,17 +113,18 @@ bool tc_slicing(int dk, int nt, int dv, TcSlicing* ts) {
   return ts->smem <= kSmemLimit;
 }
 
-// The slim single-chunk form (span_output_tc_kernel<..., K64 = true>): the
-// state, a 64-key score block and O in 256 TMEM columns, two 16 KB ring slots
-// and one v buffer, two CTAs per SM.
-bool tc_slim_fits(int dk, int nt, int dv, size_t* smem) {
-  TcSlicing ts;
-  if (!tc_slicing(dk, nt, dv, &ts) || ts.n_slices != 1) return false;
-  const int nm = dv + 16;
-  if (ts.nb > 2 || ts.nb * nm + std::max(64, nm) > kTmemCols / 2) return false;
-  const size_t s = TcSmem(dk, ts.nmax, ts.nb, 2, 1, 16384).total;
-  if (s + 1024 > kSmemLimit / 2) return false;
-  if (smem) *smem = s;
+// The append form (append_tc_kernel): one chunk of at most 64 tokens, the
+// fp32 state outside TMEM (128 columns per CTA), three CTAs per SM; d_v <= 64
+// and at most two feature blocks, the second with at most 64 rows of value
+// loads per thread pair.
+bool tc_append_fits(int dk, int nt, int dv, size_t* smem) {
+  if (!tc_supported(dk, nt) || dv % 16 != 0 || dv < 16 || dv > 64) return false;
+  const int D = feat_dim(dk, nt);
+  if (D > 256) return false;
+  const AppSmem L(dk, dv, D);
+  if (L.k1 * (dv / 8) > 2 * TC_WORKERS) return false;
+  if (L.total + 1024 > kSmemPerSm / 3) return false;
+  if (smem) *smem = L.total;
   return true;
 }
 
@@ -152,10 +155,11 @@ tsa_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* out) {
 // [heads][N][inner] bf16 viewed as 4-D (8, N, inner/8, heads) so that a box
 // (8, 128, groups, 1) lands in shared memory as [group][token][8] -- the
 // core-matrix layout of the MMA operands.
-tsa_status make_tmap(CUtensorMap* m, const void* base, int inner, long long N, int heads, int groups) {
+tsa_status make_tmap(CUtensorMap* m, const void* base, int inner, long long N, int heads, int groups,
+                     int rows = TC_C) {
   cuuint64_t dims[4] = {8, (cuuint64_t)N, (cuuint64_t)(inner / 8), (cuuint64_t)heads};
   cuuint64_t strides[3] = {(cuuint64_t)inner * 2, 16, (cuuint64_t)N * inner * 2};
-  cuuint32_t box[4] = {8, (cuuint32_t)TC_C, (cuuint32_t)groups, 1};
+  cuuint32_t box[4] = {8, (cuuint32_t)rows, (cuuint32_t)groups, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   tsa_status st = encode_fn(&enc);
@@ -165,6 +169,26 @@ tsa_status make_tmap(CUtensorMap* m, const void* base, int inner, long long N, i
                                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(TSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return TSA_OK;
+}
+
+// The fp32 value rows of each head's state ([heads][DPAD*(dv+1)], rows of dv
+// floats) viewed as 4-D (4, D, dv/4, heads), so that a box (4, rows, dv/4, 1)
+// lands in shared memory as [c/4][a][4]: the 16 bytes of a row's column
+// group are contiguous across rows.
+tsa_status make_state_tmap(CUtensorMap* m, const float* states, int D, int dv, int heads, int rows) {
+  const size_t per_head = (size_t)round_up(D, 4) * (dv + 1) * 4;
+  cuuint64_t dims[4] = {4, (cuuint64_t)D, (cuuint64_t)(dv / 4), (cuuint64_t)heads};
+  cuuint64_t strides[3] = {(cuuint64_t)dv * 4, 16, (cuuint64_t)per_head};
+  cuuint32_t box[4] = {4, (cuuint32_t)rows, (cuuint32_t)(dv / 4), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  tsa_status st = encode_fn(&enc);
+  if (st != TSA_OK) return st;
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(states), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(TSA_ERR_CUDA, "cuTensorMapEncodeTiled (states) failed (%d)", (int)r);
   return TSA_OK;
 }
 
@@ -223,20 +247,24 @@ tsa_status launch_tc(const tsa_plan& pl, const TcSlicing& ts, const PrefillParam
   if ((st = make_tmap(&mv, pp.v, pp.dv, pp.N, pp.heads, 2)) != TSA_OK) return st;
   const unsigned grid = (unsigned)((long long)pp.heads * ts.n_slices * pl.n_spans);
   if constexpr (FeatConst<DK, NT>::NB <= 2) {
-    if (pl.ctas_per_sm == 2) {   // the slim single-chunk form (tc_slim_fits)
-      size_t slim = 0;
-      if (pl.n_spans != 1 || pp.N > 64 || !tc_slim_fits(DK, NT, pp.dv, &slim))
-        return fail(TSA_ERR_UNSUPPORTED, "two CTAs per SM only for one chunk of up to 64 tokens");
-      p.ring = 2;
-      cudaError_t e = set_smem(span_output_tc_kernel<__nv_bfloat16, DK, NT, true>, (int)slim);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_output_tc, slim)");
-      span_output_tc_kernel<__nv_bfloat16, DK, NT, true><<<grid, TC_THREADS, slim, s>>>(p, mq, mk, mv);
+    if (pl.ctas_per_sm == 3) {   // the append form (tc_append_fits)
+      size_t asmem = 0;
+      if (pl.n_spans != 1 || pp.N > APP_KEYS || !tc_append_fits(DK, NT, pp.dv, &asmem))
+        return fail(TSA_ERR_UNSUPPORTED, "three CTAs per SM only for one chunk of up to 64 tokens");
+      constexpr int D = FeatConst<DK, NT>::D;
+      CUtensorMap ak, av, as;
+      if ((st = make_tmap(&ak, pp.k, DK, pp.N, pp.heads, DK / 8, APP_KEYS)) != TSA_OK) return st;
+      if ((st = make_tmap(&av, pp.v, pp.dv, pp.N, pp.heads, 2, APP_KEYS)) != TSA_OK) return st;
+      if ((st = make_state_tmap(&as, pp.states, D, pp.dv, pp.heads, D < 128 ? D : 128)) != TSA_OK) return st;
+      cudaError_t e = set_smem(append_tc_kernel<DK, NT>, (int)asmem);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(append_tc)");
+      append_tc_kernel<DK, NT><<<(unsigned)pp.heads, TC_THREADS, asmem, s>>>(p, mq, ak, av, as);
       e = cudaGetLastError();
-      if (e != cudaSuccess) return cuda_fail(e, "launch span_output_tc (slim)");
+      if (e != cudaSuccess) return cuda_fail(e, "launch append_tc");
       return TSA_OK;
     }
   }
-  if (pl.ctas_per_sm != 1) return fail(TSA_ERR_UNSUPPORTED, "no slim form for d_k=%d n=%d", DK, NT);
+  if (pl.ctas_per_sm != 1) return fail(TSA_ERR_UNSUPPORTED, "no append form for d_k=%d n=%d", DK, NT);
   const int smem = (int)ts.smem;
   cudaError_t e = set_smem(span_output_tc_kernel<__nv_bfloat16, DK, NT>, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(span_output_tc)");

@@ -75,31 +75,22 @@ struct TcParams {
 // TMA while the current one is still read by the update MMAs), `ring` slots of
 // 32 KB, the bf16 state copy (NB blocks), then the barriers.
 struct TcSmem {
-  size_t xt, vt, s, sblk, bar, total, tile;
-  int ring, vbufs;
-  // vbufs: v tile buffers (2; 1 for a single-chunk segment); tile: bytes of
-  // a ring slot (32 KB: 128 rows of 128 features; 16 KB: the 64 rows a short
-  // segment fills)
-  __host__ __device__ TcSmem(int dk, int nmax, int nb, int ring_slots, int v_buffers = 2,
-                             size_t tile_bytes = 32768) {
+  static constexpr size_t tile = 32768;   // a ring slot: 128 rows of 128 features
+  size_t xt, vt, s, sblk, bar, total;
+  int ring;
+  __host__ __device__ TcSmem(int dk, int nmax, int nb, int ring_slots) {
     ring = ring_slots;
-    vbufs = v_buffers;
-    tile = tile_bytes;
     xt = (size_t)128 * dk * 2;
     vt = (size_t)128 * nmax * 2;
-    s = 2 * xt + (size_t)vbufs * vt + (size_t)ring * tile;
+    s = 2 * xt + 2 * vt + (size_t)ring * tile;
     sblk = vt;
     bar = s + (size_t)nb * sblk;
     total = bar + 256;
-    // A readout MMA reads 128 rows (32 KB) from a slot: with 16 KB slots,
-    // rows 64..127 come from the bytes after it, which must be allocated
-    const size_t reach = 2 * xt + (size_t)vbufs * vt + (size_t)(ring - 1) * tile + 32768;
-    if (total < reach) total = reach;
   }
   __host__ __device__ size_t q() const { return 0; }
   __host__ __device__ size_t k() const { return xt; }
   __host__ __device__ size_t v(int b) const { return 2 * xt + b * vt; }
-  __host__ __device__ size_t slot(int r) const { return 2 * xt + (size_t)vbufs * vt + (size_t)r * tile; }
+  __host__ __device__ size_t slot(int r) const { return 2 * xt + 2 * vt + (size_t)r * tile; }
 };
 
 // The d inputs of token t from a [e/8][t][8] bf16 tile, as fp32.
@@ -414,27 +405,15 @@ span_state_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
 
 // ---------------------------------------------------------------------------
 // span_output_tc: outputs of one span (one slice), state carried in TMEM.
-//
-// K64: the slim form for a single chunk of at most 64 tokens (short appends
-// to existing states): scores and P over 64 keys, so that the state, the
-// shared A / O columns fit in 256 TMEM columns; feature and P tiles of the 64
-// rows the chunk fills (16 KB ring slots, two of them) and one v buffer
-// (about 100 KB of shared memory); two CTAs per SM, whose latencies overlap.
-// The readout MMAs (M = 128) read rows 64..127 of a feature tile from the
-// 16 KB that follow its slot (the next slot or the state copy): those output
-// rows are past the segment and never stored.
 // ---------------------------------------------------------------------------
-template <typename T, int DK, int NT, bool K64 = false>
-__global__ void __launch_bounds__(TC_THREADS, K64 ? 2 : 1)
+template <typename T, int DK, int NT>
+__global__ void __launch_bounds__(TC_THREADS, 1)
 span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   using FC = FeatConst<DK, NT>;
   constexpr int D = FC::D, NB = FC::NB, DPAD = round_up(D, 4);
-  constexpr int KEYS = K64 ? 64 : 128;               // keys of a chunk's scores
-  constexpr uint32_t TMEM_COLS = K64 ? 256u : 512u;
   extern __shared__ __align__(1024) uint8_t smem[];
-  const TcSmem L(DK, p.nmax, NB, p.ring, K64 ? 1 : 2, K64 ? 16384 : 32768);
-  constexpr uint32_t PSBO = K64 ? 1024u : 2048u;     // P tile: bytes between 8-row groups
+  const TcSmem L(DK, p.nmax, NB, p.ring);
   const TcBars B{reinterpret_cast<uint64_t*>(smem + L.bar)};
   uint8_t* sS = smem + L.s;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wq = warp & 3, half = (warp >> 2) & 1;
@@ -443,11 +422,11 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
   const bool single = (p.n_spans == 1);
   const size_t st_elems = (size_t)DPAD * (p.dv + 1);
 
-  if (warp == 0) tc::tmem_alloc(B.tmem_slot(), TMEM_COLS);
+  if (warp == 0) tc::tmem_alloc(B.tmem_slot(), 512);
   if (tid == 0) B.init(p.wait_ns);
   if (tid < TC_WORKERS) {
     tc_write_ones(smem + L.v(0), W, tid);
-    if (!K64) tc_write_ones(smem + L.v(1), W, tid);
+    tc_write_ones(smem + L.v(1), W, tid);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -524,7 +503,7 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
   if (warp == 8) {
     // ------------------------------ issuer ---------------------------------
     {   // the whole issuer warp runs the loop; one elected lane issues
-      const uint32_t id_qk = tc::idesc_bf16(128, KEYS, false, false);
+      const uint32_t id_qk = tc::idesc_bf16(128, 128, false, false);
       const uint32_t id_pv = tc::idesc_bf16(128, nm, false, true);
       const uint32_t id_up = tc::idesc_bf16(128, nm, true, true);
       const uint64_t dQ = tc::sdesc(tc::smem_u32(smem + L.q()), 2048, 128);
@@ -573,9 +552,9 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
         // O = P [V, 1]
         if (!(ok = ring.take(B, pos.s))) break;
         {
-          const uint64_t dP = tc::sdesc(tc::smem_u32(smem + L.slot(pos.s)), 128, PSBO);
+          const uint64_t dP = tc::sdesc(tc::smem_u32(smem + L.slot(pos.s)), 128, 2048);
 #pragma unroll
-          for (int k = 0; k < KEYS / 16; ++k)
+          for (int k = 0; k < 8; ++k)
             tc::mma_bf16_elect(tm + col_O, dP + (uint64_t)(k * 16), dV + (uint64_t)(k * 16), id_pv, k > 0 ? 1u : 0u);
           tc::mma_commit_elect(B.sempty(pos.s));
           pos.next();
@@ -600,7 +579,7 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
           if (!(ok = ring.take(B, pos.s))) break;
           const uint64_t dA = tc::sdesc(tc::smem_u32(smem + L.slot(pos.s)), 2048, 128);
 #pragma unroll
-          for (int k = 0; k < KEYS / 16; ++k)   // tokens (K64: the 64 a chunk can hold)
+          for (int k = 0; k < 8; ++k)
             tc::mma_bf16_elect(tm + f * nm, dA + (uint64_t)(k * 256), dV + (uint64_t)(k * 16), id_up, 1u);
           tc::mma_commit_elect(B.sempty(pos.s));
           if (f == 0 && has_next) {
@@ -618,8 +597,8 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
     }
   } else {
     // ------------------------------ workers --------------------------------
-    // feature tiles: token t, half of a block (K64: token t < 64, a quarter)
-    const int t = K64 ? (tid & 63) : (tid & 127);
+    // feature tiles: token t, half of a block
+    const int t = tid & 127;
     const int prow = (t / 8) * 2048 + (t % 8) * 16;
     const int row_hi = wq * 32 + 31;
     T* og = static_cast<T*>(p.out) + (size_t)u.head * p.N * p.dv + u.c0;
@@ -655,13 +634,13 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
       tc_warp_arrive(B.qkempty(), lane);
       if (!tc_wait_warp(B, B.qk(), c & 1u)) break;
       tc::fence_after_sync();
-      // P = mask(T_n(A)) -> bf16 ring slot: (i/8)*PSBO + (j/8)*128 + (i%8)*16
+      // P = mask(T_n(A)) -> bf16 ring slot: (i/8)*2048 + (j/8)*128 + (i%8)*16
       if (!ring.acquire(B, pos.s)) break;
       {
-        uint8_t* prow_p = smem + L.slot(pos.s) + (i / 8) * PSBO + (i % 8) * 16;
+        uint8_t* prow_p = smem + L.slot(pos.s) + (i / 8) * 2048 + (i % 8) * 16;
 #pragma unroll
-        for (int q2 = 0; q2 < KEYS / 64; ++q2) {
-          const int jb = half * (KEYS / 2) + 32 * q2;
+        for (int q2 = 0; q2 < 2; ++q2) {
+          const int jb = half * 64 + 32 * q2;
           if (jb <= row_hi) {   // warp-uniform: 32 keys above the diagonal are zero
             uint32_t rr[32];
             tc::tmem_ld32(tm + lane_off + col_O + jb, rr);
@@ -727,8 +706,7 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
         float x[DK + 1];
 #pragma unroll
         for (int e = 0; e <= DK; ++e) x[e] = upd ? xk[e] : xq[e];
-        if constexpr (K64) build_phi_quarter<DK, NT>(f, tid >> 6, x, smem + L.slot(pos.s) + prow);
-        else build_phi_half<DK, NT>(f, half, x, smem + L.slot(pos.s) + prow);
+        build_phi_half<DK, NT>(f, half, x, smem + L.slot(pos.s) + prow);
         ring.release(B, pos.s, lane);
         pos.next();
       }
@@ -758,7 +736,7 @@ span_output_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q
   __syncthreads();
   if (warp == 0) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tm, TMEM_COLS);
+    tc::tmem_dealloc(tm, 512);
   }
 }
 

@@ -247,17 +247,17 @@ static tsa_status make_plan_tc(const tsa_config* c, long long N, int num_sms, co
 }
 
 // Segments up to this length go to the short-segment prefill when the library
-// chooses (chunk = 0): 16 tokens where the slim tensor-core form takes the
+// chooses (chunk = 0): 16 tokens where the tensor-core append form takes the
 // shape (bf16 inputs; it is faster from 17 tokens on 1,024 heads), 32
 // otherwise; chunk = 16 asks for it at any length.
 static constexpr long long kShortAutoMaxN = 32;
-static constexpr long long kShortAutoMaxNSlim = 16;
+static constexpr long long kShortAutoMaxNAppend = 16;
 
 tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl, size_t max_scratch) {
   memset(pl, 0, sizeof(*pl));
-  const bool slim_ok = c->dtype == TSA_BF16 && tc_supported(c->d_k, c->n_terms) &&
-                       tc_slim_fits(c->d_k, c->n_terms, c->d_v, nullptr);
-  const long long short_max = slim_ok ? kShortAutoMaxNSlim : kShortAutoMaxN;
+  const bool append_ok = c->dtype == TSA_BF16 && tc_supported(c->d_k, c->n_terms) &&
+                         tc_append_fits(c->d_k, c->n_terms, c->d_v, nullptr);
+  const long long short_max = append_ok ? kShortAutoMaxNAppend : kShortAutoMaxN;
   // Short segments: each head's state stays in shared memory for the whole
   // segment (read once, written once), 16-token blocks on the CUDA cores.
   if (short_supported(c->d_k, c->n_terms, c->d_v) &&
@@ -297,12 +297,12 @@ tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl
         return st;
       }
       tsa_status st = make_plan_tc(c, N, num_sms, ts, pl, TSA_PATH_TC, max_scratch);
-      // one chunk of at most 64 tokens (a short append): the slim form, two
-      // CTAs per SM
-      size_t slim = 0;
-      if (st == TSA_OK && N <= 64 && pl->n_spans == 1 && tc_slim_fits(c->d_k, c->n_terms, c->d_v, &slim)) {
-        pl->ctas_per_sm = 2;
-        pl->smem_bytes = slim;
+      // one chunk of at most 64 tokens (a short append) of a state of at
+      // most two feature blocks: the append form, three CTAs per SM
+      size_t asmem = 0;
+      if (st == TSA_OK && N <= 64 && pl->n_spans == 1 && tc_append_fits(c->d_k, c->n_terms, c->d_v, &asmem)) {
+        pl->ctas_per_sm = 3;
+        pl->smem_bytes = asmem;
       }
       return st;
     }

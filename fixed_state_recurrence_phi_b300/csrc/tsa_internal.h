@@ -60,7 +60,7 @@ tsa_status launch_states_tc32(const tsa_config* c, const tsa_plan& pl, const Pre
 tsa_status make_states_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl);
 tsa_status launch_states(const tsa_config* c, const tsa_plan& pl, PrefillParams p, cudaStream_t s);
 tsa_status take_device_error();
-bool tc_slim_fits(int dk, int nt, int dv, size_t* smem);
+bool tc_append_fits(int dk, int nt, int dv, size_t* smem);
 // The device-check reports of the translation units with kernels (debug
 // build; each copies out and clears its own report, debug_check.cuh).
 cudaError_t debug_report_abi(unsigned long long* out);

@@ -120,12 +120,13 @@ tsa_status tsa_feature_map(int d_k, int n_terms, int64_t rows, const float* x, f
  * memory for the whole segment, so the state is read and written once; fp32
  * on the CUDA cores in blocks of chunk = 16 tokens). The library takes
  * TSA_PATH_SHORT where the state fits (d_k = 16 with n <= 3, or d_k = 32 with
- * n <= 2) for N <= 16 with bf16 inputs whose shape the slim tensor-core form
- * takes, for N <= 32 otherwise; cfg->chunk = 16 asks for it at any N.
+ * n <= 2) for N <= 16 with bf16 inputs whose shape the tensor-core append
+ * form takes, for N <= 32 otherwise; cfg->chunk = 16 asks for it at any N.
  * ctas_per_sm: CTAs of the output pass resident per SM. On TSA_PATH_TC it is
- * 2 for the slim single-chunk form that bf16 segments of at most 64 tokens
- * take where one CTA holds the head's state (a short append: 64-key scores,
- * about 100 KB of shared memory and 256 TMEM columns per CTA), 1 otherwise. */
+ * 3 for the append form that bf16 segments of at most 64 tokens take where
+ * d_v <= 64 and the state has at most two 128-feature blocks (a short append:
+ * the state's bf16 copy in shared memory and its update accumulated apart in
+ * 128 TMEM columns, at most 75 KB of shared memory per CTA), 1 otherwise. */
 #define TSA_PATH_SIMT 0
 #define TSA_PATH_TC 1
 #define TSA_PATH_TC_F32 2

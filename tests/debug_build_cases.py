@@ -115,9 +115,10 @@ def main():
     prefill_case(16, 64, 3, "f32", 500, chunk=64, expect_path=T.TSA_PATH_SIMT)
     prefill_case(16, 64, 3, "f32", 16, expect_path=T.TSA_PATH_SHORT, accumulate_pre=40)
     prefill_case(16, 64, 3, "bf16", 200, accumulate_pre=129)
-    prefill_case(16, 64, 3, "bf16", 50, H=4, accumulate_pre=100)   # the slim single-chunk form
-    prefill_case(16, 32, 1, "bf16", 64, H=4, accumulate_pre=100)   # slim, the smallest state
-    prefill_case(32, 64, 2, "bf16", 40, H=4, accumulate_pre=100)   # slim, d_k 32
+    prefill_case(16, 64, 3, "bf16", 50, H=4, accumulate_pre=100)   # the append form, two feature blocks
+    prefill_case(16, 32, 1, "bf16", 64, H=4, accumulate_pre=100)   # append form, the smallest state
+    prefill_case(32, 64, 2, "bf16", 40, H=4, accumulate_pre=100)   # append form, d_k 32
+    prefill_case(16, 64, 3, "bf16", 24, H=4)                       # append form from a zero state
     decode_merge_states_case()
     feature_map_case()
     print("debug build ok")

@@ -90,12 +90,12 @@ def test_plan_short_segments(T):
     fits; chunk = 16 asks for it at any length; chunk = 128 keeps the chunked
     tensor-core path."""
     for dt in ("f32", "bf16"):
-        # bf16 segments of 17..64 tokens take the slim tensor-core form instead
+        # bf16 segments of 17..64 tokens take the tensor-core append form instead
         n_max = 16 if dt == "bf16" else 32
         for N in (1, 16, 32):
             p = T.prefill_plan(T.Config(64, 16, 16, 64, 3, dt), N, num_sms=148)
             if N > n_max:
-                assert p["path"] == T.TSA_PATH_TC and p["ctas_per_sm"] == 2, (dt, N, p)
+                assert p["path"] == T.TSA_PATH_TC and p["ctas_per_sm"] == 3, (dt, N, p)
                 continue
             assert p["path"] == T.TSA_PATH_SHORT and p["chunk"] == 16, (dt, N, p)
             assert p["chunks_per_span"] == -(-N // 16) and p["launches"] == 1 and p["scratch_bytes"] == 0
@@ -105,7 +105,7 @@ def test_plan_short_segments(T):
                               num_sms=148)["path"] == T.TSA_PATH_SHORT
         assert T.prefill_plan(T.Config(64, 16, 16, 64, 3, dt, chunk=128), 8,
                               num_sms=148)["path"] != T.TSA_PATH_SHORT
-    # bf16 states the slim form does not take keep the short path up to 32 tokens
+    # bf16 states the append form does not take keep the short path up to 32 tokens
     assert T.prefill_plan(T.Config(4, 4, 32, 128, 2, "bf16"), 32, num_sms=148)["path"] == T.TSA_PATH_SHORT
     # shared memory of the layout: state, phi(q) and phi(k) of a block, the
     # block's values and inputs, intra-block kernel values, the 8 warps'
