@@ -119,6 +119,7 @@ def main():
     prefill_case(16, 32, 1, "bf16", 64, H=4, accumulate_pre=100)   # append form, the smallest state
     prefill_case(32, 64, 2, "bf16", 40, H=4, accumulate_pre=100)   # append form, d_k 32
     prefill_case(16, 64, 3, "bf16", 24, H=4)                       # append form from a zero state
+    prefill_case(16, 64, 3, "bf16", 1, H=4, chunk=128, accumulate_pre=129)   # append form, one token
     decode_merge_states_case()
     feature_map_case()
     print("debug build ok")

@@ -192,6 +192,29 @@ def test_append_form_from_zero(G, d, dv, n, N):
     assert torch.count_nonzero(sv[:, Dp * dv:][:, D:]) == 0
 
 
+@pytest.mark.parametrize("N", [1, 2, 7, 15, 16, 63])
+def test_append_form_short_and_ragged(G, N):
+    """chunk = 128 keeps bf16 segments of 1..16 tokens off the short path, so
+    the append form runs the smallest segments too (a single token: one key,
+    one query row): every head against the oracle, from zero and continuing
+    a prefix."""
+    T, O = G.T, G.O
+    cfg = T.Config(2, 4, 16, 64, 3, "bf16", chunk=128)
+    assert T.prefill_plan(cfg, N)["ctas_per_sm"] == 3
+    _check_all_heads(G, cfg, N, seed=600 + N)
+    P = 129
+    q, k, v = G.make_inputs(cfg, P + N, seed=610 + N)
+    sl = lambda x, a, b: x[:, :, a:b].contiguous()
+    _, st = G.gpu_prefill(cfg, sl(q, 0, P), sl(k, 0, P), sl(v, 0, P))
+    out, st = G.gpu_prefill(cfg, sl(q, P, P + N), sl(k, P, P + N), sl(v, P, P + N), states=st, accumulate=True)
+    Sg, og = G.canonical(cfg, st), G.host(out)
+    qh, kh, vh = G.host(q), G.host(k), G.host(v)
+    for b in range(2):
+        for h in range(4):
+            o_r, S_r = O.prefill_recurrent(qh[b, h], kh[b, h], vh[b, h], 3)
+            G.check_head(cfg, og[b, h], Sg[b, h], o_r[P:], S_r, G.TOL["bf16"], f"append N={N} ({b},{h})")
+
+
 @pytest.mark.parametrize("d,dv,n,L", [(16, 64, 3, 17), (16, 64, 3, 32), (16, 64, 3, 33), (16, 64, 3, 64),
                                       (32, 64, 2, 50), (16, 32, 1, 64), (16, 32, 3, 40)])
 def test_append_many_heads(G, d, dv, n, L):
