@@ -13,7 +13,10 @@ Timing: CUDA events on the launching stream; between timed prefill steps the
 L2 is flushed by writing a buffer larger than L2 (outside the events). The
 headline prefill step is one tsa_prefill call captured in a CUDA graph and
 replayed, so that it measures the device and not the host's issue rate (the
-per-call timing is reported beside it as ms_per_step_eager). Decode
+per-call timing is reported beside it as ms_per_step_eager). Host-side timings
+(eager steps, host time per call, the end-to-end steps) start after a short
+busy wait of the host thread, so that they measure the library's host work
+and not an idle core's wake-up. Decode
 steps rotate over 8 independent state sets (8 x 41.5 MB > L2), captured in a
 CUDA graph, so every step streams its state from HBM.
 
@@ -72,6 +75,17 @@ def rank_seed(seed: int, rank: int) -> int:
     """Weak scaling: every rank runs its own batch of the workload, drawn from
     its own seed."""
     return seed + 1000 * rank
+
+
+def warm_host(seconds: float = 0.2) -> None:
+    """Keep this thread busy for a moment before a host-side timing. A host
+    core that has idled (sleeps, blocking synchronizations) first runs the
+    library's host code (argument checks, plan, tensor maps, launches)
+    several times slower: measured 65-95 us per prefill call instead of
+    15 us, and eager steps that wait for their launches."""
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        pass
 
 
 def max_over_ranks(x: float, ws: int, device) -> float:
@@ -436,6 +450,7 @@ def _run_ours(args, clk):
           barrier()
           evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                  for _ in range(args.steps)]
+          warm_host()
           for i in range(args.steps):
               flush.fill_(float(i))
               evs[i][0].record(stream)
@@ -446,7 +461,8 @@ def _run_ours(args, clk):
           ms = slowest(statistics.mean(step_ms))
           # host time of one call (argument checks, plan, tensor maps, launches)
           hs = []
-          for _ in range(5):
+          warm_host()
+          for _ in range(9):
               torch.cuda.synchronize()
               h0 = time.perf_counter()
               prefill_step()
@@ -516,6 +532,7 @@ def _run_ours(args, clk):
               e2e_step(i)
           barrier()
           a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+          warm_host()
           a.record(stream)
           for es in e2e_streams:
               es.wait_stream(stream)
@@ -688,6 +705,7 @@ def _run_ours(args, clk):
           decode_all(stream)
           barrier()
           eager = []
+          warm_host()
           for t in range(64):
               a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
               a.record(stream)
