@@ -31,15 +31,17 @@
 
 namespace tsa {
 
-template <int DK, int NT, int W>
-struct SimtLayout {
+// Shared-memory layout (floats) for feature tiles of DT features.
+template <int DK, int NT, int W, int DT_>
+struct SimtLayoutDT {
   static constexpr int D = feat_dim(DK, NT);
   static constexpr int DPAD = round_up(D, 4);
   static constexpr int C = 64;
-  static constexpr int DT = 32;
+  static constexpr int DT = DT_;
   static constexpr int NTILE = (D + DT - 1) / DT;
   static constexpr int DROWS = NTILE * DT;
   static constexpr int TN = W / 16;      // value columns per thread
+  static constexpr int RPT = DT / 16;    // state rows per thread in the update
   static constexpr int XS = DK + 1;      // x row stride; x[DK] = 1.0
   static constexpr int PKS = DT + 4;     // phiK row stride
   static constexpr int NTHR = 256;
@@ -56,8 +58,24 @@ struct SimtLayout {
   static constexpr int total = oPhK + C * PKS;
   static constexpr size_t bytes = (size_t)total * 4;
   static_assert(W == 32 || W == 64, "slice width");
+  static_assert(DT == 32 || DT == 64, "feature tile");
   static_assert(C == 64 && NTHR == 256, "thread mapping assumes 64 tokens x 256 threads");
 };
+
+// Tiles of 64 features where that layout fits and keeps as many CTAs per SM
+// as tiles of 32 (each update thread then holds 4 state rows instead of 2,
+// so that its shared-memory loads feed twice the FMAs); else 32.
+__host__ __device__ constexpr int simt_ctas(size_t bytes) {
+  return bytes > 227 * 1024 ? 0 : (2 * (bytes + 1024) <= 228 * 1024 ? 2 : 1);
+}
+template <int DK, int NT, int W>
+struct SimtDT {
+  static constexpr size_t b32 = SimtLayoutDT<DK, NT, W, 32>::bytes;
+  static constexpr size_t b64 = SimtLayoutDT<DK, NT, W, 64>::bytes;
+  static constexpr int value = (simt_ctas(b64) > 0 && simt_ctas(b64) >= simt_ctas(b32)) ? 64 : 32;
+};
+template <int DK, int NT, int W>
+struct SimtLayout : SimtLayoutDT<DK, NT, W, SimtDT<DK, NT, W>::value> {};
 
 // Load the chunk's x rows (q or k) into smem as fp32 with x[DK] = 1.0; rows at
 // or beyond `valid` are zero.
@@ -123,11 +141,12 @@ __device__ __forceinline__ void build_phi_tile(float* sm, int a0, int valid, int
   const float* xk = sm + L::oXk;
   float* phq = sm + L::oPhQ;
   float* phk = sm + L::oPhK;
-  const int tok = tid & (L::C - 1), fg = tid >> 6;  // 4 groups of 8 features
-  float fk[8];
+  constexpr int FPG = L::DT / 4;                      // features per thread
+  const int tok = tid & (L::C - 1), fg = tid >> 6;  // 4 groups of DT/4 features
+  float fk[FPG];
 #pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const int a = a0 + fg * 8 + u;
+  for (int u = 0; u < FPG; ++u) {
+    const int a = a0 + fg * FPG + u;
     float vq = 0.f, vk = 0.f;
     if (a < L::D) {
       const uint32_t cd = code[a];
@@ -137,33 +156,43 @@ __device__ __forceinline__ void build_phi_tile(float* sm, int a0, int valid, int
       vk = w * xk[tok * L::XS + i] * xk[tok * L::XS + j] * xk[tok * L::XS + l];
     }
     if (tok >= valid) vk = 0.f;
-    if (WITH_Q) phq[(fg * 8 + u) * L::C + tok] = vq;
+    if (WITH_Q) phq[(fg * FPG + u) * L::C + tok] = vq;
     fk[u] = vk;
   }
-  *reinterpret_cast<float4*>(phk + tok * L::PKS + fg * 8) = make_float4(fk[0], fk[1], fk[2], fk[3]);
-  *reinterpret_cast<float4*>(phk + tok * L::PKS + fg * 8 + 4) = make_float4(fk[4], fk[5], fk[6], fk[7]);
+#pragma unroll
+  for (int u = 0; u < FPG; u += 4)
+    *reinterpret_cast<float4*>(phk + tok * L::PKS + fg * FPG + u) = make_float4(fk[u], fk[u + 1], fk[u + 2], fk[u + 3]);
 }
 
-// S[a0 + 2ta + r][tc*TN + c] += sum_t phiK[t][2ta + r] * V[t][tc*TN + c]
-// z[a0 + 2ta + r]            += sum_t phiK[t][2ta + r]
+// S[a0 + RPT*ta + r][tc*TN + c] += sum_t phiK[t][RPT*ta + r] * V[t][tc*TN + c]
+// z[a0 + RPT*ta + r]             += sum_t phiK[t][RPT*ta + r]
 template <int DK, int NT, int W>
 __device__ __forceinline__ void update_tile(float* sm, int a0, int tid) {
   using L = SimtLayout<DK, NT, W>;
-  constexpr int TN = L::TN;
+  constexpr int TN = L::TN, RPT = L::RPT;
   float* S = sm + L::oS;
   float* z = sm + L::oZ;
   const float* phk = sm + L::oPhK;
   const float* vs = sm + L::oV;
   const int ta = tid >> 4, tc = tid & 15;
-  float s[2][TN];
+  float s[RPT][TN];
 #pragma unroll
-  for (int r = 0; r < 2; ++r)
+  for (int r = 0; r < RPT; ++r)
 #pragma unroll
-    for (int c = 0; c < TN; ++c) s[r][c] = S[(a0 + 2 * ta + r) * W + tc * TN + c];
-  float zp0 = 0.f, zp1 = 0.f;
+    for (int c = 0; c < TN; ++c) s[r][c] = S[(a0 + RPT * ta + r) * W + tc * TN + c];
+  float zp[RPT];
+#pragma unroll
+  for (int r = 0; r < RPT; ++r) zp[r] = 0.f;
 #pragma unroll 4
   for (int t = 0; t < L::C; ++t) {
-    const float2 kk = *reinterpret_cast<const float2*>(phk + t * L::PKS + 2 * ta);
+    float kk[RPT];
+    if constexpr (RPT == 4) {
+      const float4 x = *reinterpret_cast<const float4*>(phk + t * L::PKS + 4 * ta);
+      kk[0] = x.x; kk[1] = x.y; kk[2] = x.z; kk[3] = x.w;
+    } else {
+      const float2 x = *reinterpret_cast<const float2*>(phk + t * L::PKS + 2 * ta);
+      kk[0] = x.x; kk[1] = x.y;
+    }
     float vv[TN];
     if constexpr (TN == 4) {
       const float4 x = *reinterpret_cast<const float4*>(vs + t * W + tc * 4);
@@ -173,22 +202,26 @@ __device__ __forceinline__ void update_tile(float* sm, int a0, int tid) {
       vv[0] = x.x; vv[1] = x.y;
     }
 #pragma unroll
-    for (int c = 0; c < TN; ++c) {
-      s[0][c] = fmaf(kk.x, vv[c], s[0][c]);
-      s[1][c] = fmaf(kk.y, vv[c], s[1][c]);
+    for (int r = 0; r < RPT; ++r)
+#pragma unroll
+      for (int c = 0; c < TN; ++c) s[r][c] = fmaf(kk[r], vv[c], s[r][c]);
+    if ((t & 15) == tc) {
+#pragma unroll
+      for (int r = 0; r < RPT; ++r) zp[r] += kk[r];
     }
-    if ((t & 15) == tc) { zp0 += kk.x; zp1 += kk.y; }
   }
 #pragma unroll
-  for (int r = 0; r < 2; ++r)
+  for (int r = 0; r < RPT; ++r)
 #pragma unroll
-    for (int c = 0; c < TN; ++c) S[(a0 + 2 * ta + r) * W + tc * TN + c] = s[r][c];
+    for (int c = 0; c < TN; ++c) S[(a0 + RPT * ta + r) * W + tc * TN + c] = s[r][c];
 #pragma unroll
-  for (int off = 8; off >= 1; off >>= 1) {
-    zp0 += __shfl_xor_sync(0xffffffffu, zp0, off);
-    zp1 += __shfl_xor_sync(0xffffffffu, zp1, off);
+  for (int r = 0; r < RPT; ++r)
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) zp[r] += __shfl_xor_sync(0xffffffffu, zp[r], off);
+  if (tc == 0) {
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) z[a0 + RPT * ta + r] += zp[r];
   }
-  if (tc == 0) { z[a0 + 2 * ta] += zp0; z[a0 + 2 * ta + 1] += zp1; }
 }
 
 template <int DK, int NT>
@@ -447,7 +480,7 @@ span_output_kernel(PrefillParams p) {
           for (int c = 0; c < TN; ++c) acc[r][c] = fmaf(qr[r], ss[c], acc[r][c]);
       }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < L::DT / 16; ++h) {
         const int a = tc + 16 * h;
         const float4 qq = *reinterpret_cast<const float4*>(phq + a * C + 4 * tr);
         const float zz = z[a0 + a];
