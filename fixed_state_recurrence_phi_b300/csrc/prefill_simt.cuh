@@ -183,7 +183,7 @@ __device__ __forceinline__ void update_tile(float* sm, int a0, int tid) {
   float zp[RPT];
 #pragma unroll
   for (int r = 0; r < RPT; ++r) zp[r] = 0.f;
-#pragma unroll 4
+#pragma unroll 8
   for (int t = 0; t < L::C; ++t) {
     float kk[RPT];
     if constexpr (RPT == 4) {
@@ -462,7 +462,7 @@ span_output_kernel(PrefillParams p) {
       const int a0 = tile * L::DT;
       build_phi_tile<DK, NT, W, true>(sm, a0, valid, tid);
       __syncthreads();
-#pragma unroll 4
+#pragma unroll 8
       for (int a = 0; a < L::DT; ++a) {
         const float4 qq = *reinterpret_cast<const float4*>(phq + a * C + 4 * tr);
         float ss[TN];
