@@ -249,7 +249,9 @@ append_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_q, con
         tc::mma_bf16_elect(tm, dA + (uint64_t)(kk * 16), dS + (uint64_t)(kk * 16), id_pv, 1u);
       tc::mma_commit_elect(B.sempty(s));
     }
-    if (ok) tc::mma_commit_elect(B.odone());
+    // (testing only: with dbg_withhold, O's completion is never published, so
+    // the workers' bounded wait for it runs out)
+    if (ok && !p.dbg_withhold) tc::mma_commit_elect(B.odone());
     // dS_f = phi(K_f)^T [V, 1]   (uses NB+1..2NB), each into the O columns
     // once the workers have read what was there
     for (int f = 0; f < NB && ok; ++f) {

@@ -252,6 +252,12 @@ tsa_status launch_tc(const tsa_plan& pl, const TcSlicing& ts, const PrefillParam
       if (pl.n_spans != 1 || pp.N > APP_KEYS || !tc_append_fits(DK, NT, pp.dv, &asmem))
         return fail(TSA_ERR_UNSUPPORTED, "three CTAs per SM only for one chunk of up to 64 tokens");
       constexpr int D = FeatConst<DK, NT>::D;
+      {   // testing hook 3: the append form withholds O's completion
+        unsigned long long wn;
+        int wh;
+        tc_debug_params(&wn, &wh);
+        p.dbg_withhold = (wh == 3);
+      }
       CUtensorMap ak, av, as;
       if ((st = make_tmap(&ak, pp.k, DK, pp.N, pp.heads, DK / 8, APP_KEYS)) != TSA_OK) return st;
       if ((st = make_tmap(&av, pp.v, pp.dv, pp.N, pp.heads, 2, APP_KEYS)) != TSA_OK) return st;
@@ -308,7 +314,7 @@ extern "C" tsa_status tsa_debug_set_wait_limit(uint64_t ns) {
 }
 
 extern "C" tsa_status tsa_debug_withhold_publication(int what) {
-  if (what < 0 || what > 2) return tsa::fail(TSA_ERR_INVALID, "withhold must be 0, 1 or 2 (got %d)", what);
+  if (what < 0 || what > 3) return tsa::fail(TSA_ERR_INVALID, "withhold must be 0..3 (got %d)", what);
   tsa::g_withhold.store(what);
   return TSA_OK;
 }

@@ -226,7 +226,8 @@ def debug_set_wait_limit(ns: int):
 
 def debug_withhold_publication(what: int):
     """Testing hook: 1 = the fp32 output pass withholds its first publication;
-    2 = rank 0 of each CTA pair withholds its first exchange publication."""
+    2 = rank 0 of each CTA pair withholds its first exchange publication;
+    3 = the bf16 append form withholds its output's completion."""
     _check("tsa_debug_withhold_publication", _lib.tsa_debug_withhold_publication(int(what)))
 
 

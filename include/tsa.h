@@ -250,6 +250,11 @@ tsa_status tsa_sync_status(void* cuda_stream);
  *    in the peer's shared memory; the peer's wait runs out, the peer gives up
  *    and makes rank 0 give up too, both release their tensor memory and
  *    exit, and tsa_sync_status returns TSA_ERR_TIMEOUT.
+ *    tsa_debug_withhold_publication(3): the bf16 append form (tsa_plan
+ *    ctas_per_sm = 3) never publishes that its output accumulator is
+ *    complete; the waits for it run out, each CTA gives up, releases its
+ *    tensor memory and exits with its outputs and state incomplete, and
+ *    tsa_sync_status returns TSA_ERR_TIMEOUT.
  *    0 turns it off; other values are TSA_ERR_INVALID. */
 tsa_status tsa_debug_set_wait_limit(uint64_t ns);
 tsa_status tsa_debug_withhold_publication(int what);

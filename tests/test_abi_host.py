@@ -174,10 +174,12 @@ def test_validation_codes(T):
 
 def test_debug_hooks_validate(T):
     """The testing hooks take only their documented values (host only)."""
-    with pytest.raises(T.TsaError) as e:
-        T.debug_withhold_publication(3)
-    assert e.value.status == T.TSA_ERR_INVALID
-    T.debug_withhold_publication(0)
+    for bad in (4, -1):
+        with pytest.raises(T.TsaError) as e:
+            T.debug_withhold_publication(bad)
+        assert e.value.status == T.TSA_ERR_INVALID
+    for good in (1, 2, 3, 0):
+        T.debug_withhold_publication(good)
     T.debug_set_wait_limit(0)
 
 

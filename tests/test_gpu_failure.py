@@ -93,3 +93,42 @@ def test_pair_exchange_withheld_times_out_then_prefill_is_correct(T):
     for h in range(2):
         o_r, S_r = oracle_prefill(qh[0, h], kh[0, h], vh[0, h], 4)
         check_head(cfg, host(out[0, h]), S[0, h], o_r, S_r, TOL["bf16"], f"head {h}")
+
+
+def test_append_form_withheld_times_out_then_append_is_correct(T):
+    """The bf16 append form (three CTAs per SM, 64-token segments): the issuer
+    never publishes that O is complete, the workers' bounded wait runs out,
+    every CTA gives up and releases its tensor memory, TSA_ERR_TIMEOUT is
+    reported; the same append afterwards, continuing a prefix, matches the
+    oracle."""
+    from gpu_helpers import check_head, host, make_inputs, canonical, gpu_prefill, TOL
+    from oracle import tsa_oracle as O
+    cfg = T.Config(2, 8, 16, 64, 3, "bf16")
+    P, L = 150, 40
+    assert T.prefill_plan(cfg, L)["ctas_per_sm"] == 3
+    q, k, v = make_inputs(cfg, P + L, seed=33)
+    sl = lambda x, a, b: x[:, :, a:b].contiguous()
+    _, st0 = gpu_prefill(cfg, sl(q, 0, P), sl(k, 0, P), sl(v, 0, P))
+    aq, ak, av = sl(q, P, P + L), sl(k, P, P + L), sl(v, P, P + L)
+    out = torch.zeros((2, 8, L, 64), dtype=torch.bfloat16, device="cuda")
+    st = st0.clone()
+    T.sync_status()
+    T.debug_set_wait_limit(2_000_000)
+    T.debug_withhold_publication(3)
+    try:
+        T.prefill(cfg, L, aq, ak, av, out, st, accumulate=True)
+        with pytest.raises(T.TsaError) as e:
+            T.sync_status()
+        assert e.value.status == T.TSA_ERR_TIMEOUT, T.last_error()
+    finally:
+        T.debug_withhold_publication(0)
+        T.debug_set_wait_limit(0)
+    T.sync_status()
+    st = st0.clone()
+    T.prefill(cfg, L, aq, ak, av, out, st, accumulate=True)
+    T.sync_status()
+    S = canonical(cfg, st)
+    qh, kh, vh = host(q), host(k), host(v)
+    for b, h in [(0, 0), (1, 7), (0, 5)]:
+        o_r, S_r = O.prefill_recurrent(qh[b, h], kh[b, h], vh[b, h], 3)
+        check_head(cfg, host(out[b, h]), S[b, h], o_r[P:], S_r, TOL["bf16"], f"head ({b},{h})")
