@@ -286,8 +286,10 @@ span_scan_kernel(float* __restrict__ states, float* __restrict__ scratch, int he
   // reads the prefixes. This grid waits for the span pass likewise.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int head = blockIdx.y;
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  // heads along x (up to 2^31 - 1 of them), element blocks along y (a few
+  // hundred at most)
+  const int head = blockIdx.x;
+  const int e = blockIdx.y * blockDim.x + threadIdx.x;
   if (e >= elems4 || head >= heads) return;
   float4* st = reinterpret_cast<float4*>(states) + (size_t)head * elems4;
   float4* sc = reinterpret_cast<float4*>(scratch) + (size_t)head * n_spans * elems4;
@@ -321,7 +323,7 @@ static inline cudaError_t launch_span_scan(float* states, float* scratch, int he
   // launched with a programmatic dependency on the span pass before it
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3((elems4 + 127) / 128, heads);
+  cfg.gridDim = dim3((unsigned)heads, (elems4 + 127) / 128);
   cfg.blockDim = dim3(128);
   cfg.stream = s;
   cudaLaunchAttribute at;

@@ -377,3 +377,31 @@ def test_full_wide_B2_H32_N65536_with_merge(G):
         assert G.rel_err(Sm[b, h][:, 128], S_r[:, 128]) <= G.TOL["bf16"]
     # and the merged state agrees with the single-pass state on every head
     assert G.rel_err(G.host(sa), G.host(st)) <= 1e-4
+
+
+def test_more_heads_than_a_grid_y_dimension(G):
+    """70,000 heads (beyond the 65,535 blocks a grid's y dimension allows):
+    the state-only prefill (span pass and scan), the prefill and a decode
+    step all cover every head; the two prefills give the same states, and
+    sampled heads match the oracle."""
+    T, O = G.T, G.O
+    cfg = T.Config(70, 1000, 16, 32, 1, "f32")
+    N = 5
+    q, k, v = G.make_inputs(cfg, N + 1, seed=77)
+    sl = lambda x, a, b: x[:, :, a:b].contiguous()
+    s1 = T.new_states(cfg)
+    T.prefill_states(cfg, N, sl(k, 0, N), sl(v, 0, N), s1)
+    out, s2 = G.gpu_prefill(cfg, sl(q, 0, N), sl(k, 0, N), sl(v, 0, N))
+    T.sync_status()
+    # (the state-only call takes the split-bf16 tensor cores, the prefill the
+    # CUDA cores: equal up to the fp32 parity tolerance)
+    assert G.rel_err(G.host(s1), G.host(s2)) <= G.TOL["f32"]
+    od = torch.empty((70, 1000, 32), device="cuda")
+    T.decode_step(cfg, q[:, :, N].contiguous(), k[:, :, N].contiguous(), v[:, :, N].contiguous(), od, s2)
+    T.sync_status()
+    Sg, og, odh = G.canonical(cfg, s2), G.host(out), G.host(od)
+    for b, h in [(0, 0), (69, 999), (35, 512), (65, 535)]:
+        qh, kh, vh = (G.host(x[b, h]) for x in (q, k, v))
+        o_r, S_r = O.prefill_recurrent(qh, kh, vh, 1)
+        G.check_head(cfg, og[b, h], Sg[b, h], o_r[:N], S_r, G.TOL["f32"], f"head ({b},{h})")
+        assert G.rel_err(odh[b, h], o_r[N]) <= G.TOL["f32"], (b, h)
