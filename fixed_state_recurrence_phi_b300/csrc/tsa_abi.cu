@@ -252,9 +252,13 @@ static tsa_status make_plan_tc(const tsa_config* c, long long N, int num_sms, co
 // otherwise; chunk = 16 asks for it at any length.
 static constexpr long long kShortAutoMaxN = 32;
 static constexpr long long kShortAutoMaxNAppend = 16;
+// Token coordinates of the TMA tensor copies and of the kernels'
+// chunk indexing are 32-bit: one call takes at most 2^31 - 1 tokens.
+static constexpr long long kMaxTokens = INT_MAX;
 
 tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl, size_t max_scratch) {
   memset(pl, 0, sizeof(*pl));
+  if (N > kMaxTokens) return fail(TSA_ERR_INVALID, "N = %lld exceeds 2^31 - 1 tokens a call", N);
   const bool append_ok = c->dtype == TSA_BF16 && tc_supported(c->d_k, c->n_terms) &&
                          tc_append_fits(c->d_k, c->n_terms, c->d_v, nullptr);
   const long long short_max = append_ok ? kShortAutoMaxNAppend : kShortAutoMaxN;
@@ -437,6 +441,7 @@ static tsa_status dispatch_states_simt(const tsa_config* c, const tsa_plan& pl, 
 // no output part, so more spans cost only the scan's share).
 tsa_status make_states_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl) {
   memset(pl, 0, sizeof(*pl));
+  if (N > kMaxTokens) return fail(TSA_ERR_INVALID, "N = %lld exceeds 2^31 - 1 tokens a call", N);
   const long long heads = (long long)c->B * c->H;
   int chunk = 64, n_slices = 1, slice_w = c->d_v, path = TSA_PATH_SIMT;
   size_t smem = 0;

@@ -158,8 +158,9 @@ tsa_status tsa_prefill_plan(const tsa_config* cfg, int64_t N, int num_sms, tsa_p
  *         (the state before them) and the outputs attend to it.
  * The library may take stream-ordered scratch from its own memory pool.
  * N = 0 is a no-op (TSA_OK; states untouched unless ACCUMULATE is clear, in
- * which case they are zeroed). Errors: NULL pointers, N < 0, misalignment ->
- * TSA_ERR_INVALID; unsupported shapes -> TSA_ERR_UNSUPPORTED. */
+ * which case they are zeroed). Errors: NULL pointers, N < 0, N > 2^31 - 1
+ * (token coordinates are 32-bit), misalignment -> TSA_ERR_INVALID;
+ * unsupported shapes -> TSA_ERR_UNSUPPORTED. */
 tsa_status tsa_prefill(const tsa_config* cfg, int64_t N, const void* q, const void* k,
                        const void* v, void* out, float* states, unsigned flags,
                        void* cuda_stream);

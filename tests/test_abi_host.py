@@ -169,6 +169,11 @@ def test_validation_codes(T):
     with pytest.raises(T.TsaError) as e:
         T.prefill_plan(ok, -5, num_sms=148)
     assert e.value.status == T.TSA_ERR_INVALID
+    # token coordinates are 32-bit: 2^31 - 1 tokens plan, 2^31 do not
+    assert T.prefill_plan(ok, (1 << 31) - 1, num_sms=148)["n_spans"] >= 1
+    with pytest.raises(T.TsaError) as e:
+        T.prefill_plan(ok, 1 << 31, num_sms=148)
+    assert e.value.status == T.TSA_ERR_INVALID and "2^31" in T.last_error()
     assert T.status_string(T.TSA_ERR_TIMEOUT) == "TSA_ERR_TIMEOUT"
 
 
