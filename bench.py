@@ -784,6 +784,11 @@ def _run_ours(args, clk):
               m_ms.append((a, b))
           barrier()
           merge_ms = statistics.median([a.elapsed_time(b) for a, b in m_ms])
+
+      # ---------------- the exact-softmax comparison (one GPU) ---------------
+      softmax = None
+      if args.only in ("all", "softmax") and ws == 1:
+          softmax = softmax_comparison(T, dev, stream, flush, ws, rank)
     clocks = clk.summary()
 
     # ---------------- report -------------------------------------------------
@@ -839,6 +844,9 @@ def _run_ours(args, clk):
         "parity": parity,
         "chunks": [{"chunk": c_["chunk"], "ms": r3(c_["ms"]), "path": c_["path"], "n_spans": c_["n_spans"]}
                    for c_ in chunk_lines],
+        # the pages' speed comparison re-measured here: states path against
+        # exact softmax on the library's fastest attention backend
+        "softmax": softmax,
         "prefill_tensor_core": [
             {"workload": t["workload"], "ms": r3(t["ms"]), "tokens_per_s": r3(t["tokens_per_s"]),
              "plan": t["plan"],
@@ -856,6 +864,136 @@ def _run_ours(args, clk):
                    "gpu_launches": reps * steps, "states_prefill_ms": r3(long_prefill_ms)},
     }
     print(json.dumps(line), flush=True)
+
+
+SOFTMAX_PREFILL_N = (256, 512, 1024, 2048, 4096, 8192, 16384, 32768, 65536)
+SOFTMAX_DECODE_N = (1024, 4096, 16384, 65536)
+SOFTMAX_FIT_MIN_N = 2048
+
+
+def loglog_slope(ns, ts) -> float:
+    """Least-squares exponent p of t ~ N^p."""
+    return float(np.polyfit(np.log(np.asarray(ns, float)), np.log(np.asarray(ts, float)), 1)[0])
+
+
+def crossover_n(ns, ours, soft):
+    """The sequence length above which the states path stays faster than
+    softmax: log-log interpolation across the last sweep interval where the
+    sign of log(soft / ours) changes. ns[0] if ours is faster everywhere,
+    None if never."""
+    r = [float(np.log(s / o)) for s, o in zip(soft, ours)]
+    if r[-1] <= 0:
+        return None
+    i = max([j for j, x in enumerate(r) if x <= 0], default=-1)
+    if i < 0:
+        return ns[0]
+    x0, x1 = np.log(ns[i]), np.log(ns[i + 1])
+    return float(np.exp(x0 + (0.0 - r[i]) / (r[i + 1] - r[i]) * (x1 - x0)))
+
+
+def softmax_comparison(T, dev, stream, flush, ws, rank):
+    """The pages' speed comparison re-measured on this GPU: the states path
+    (tsa_prefill, tsa_decode_step) against exact causal softmax attention on
+    the library's fastest backend (fixed_state_recurrence_phi_b300.softmax_
+    baseline), prefill over a sweep of N on the 8-head d_k=16, d_v=64, n=3
+    shape in fp32 and bf16, and one KV-cache decode step on the B=64, H=16
+    decode shape (bf16) over a sweep of context lengths. Both sides are timed
+    the same way: eager calls on the same stream, CUDA events around each
+    call, median; the L2 is flushed before each prefill call; the decode
+    steps stream caches and rotated state sets larger than L2."""
+    import torch
+    from fixed_state_recurrence_phi_b300 import softmax_baseline as SB
+    from fixed_state_recurrence_phi_b300.inputs import torch_qkv
+
+    def median_ms(fn, reps, do_flush):
+        fn()
+        torch.cuda.synchronize()
+        evs = []
+        warm_host()
+        for i in range(reps):
+            if do_flush:
+                flush.fill_(float(i))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn(i)
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.median([a.elapsed_time(b) for a, b in evs])
+
+    r4 = lambda x: None if x is None else float(f"{x:.4g}")
+    B, H, d, dv, n = 1, 8, 16, 64, 3
+    prefill = []
+    for dtype in ("f32", "bf16"):
+        cfg = T.Config(B, H, d, dv, n, dtype)
+        comp = tried = None
+        ours, soft = [], []
+        for N in SOFTMAX_PREFILL_N:
+            q, k, v = torch_qkv(B, H, N, d, dv, dtype, rank_seed(21, rank), 0, dev)
+            out = torch.empty((B, H, N, dv), dtype=q.dtype, device=dev)
+            st = T.new_states(cfg, dev)
+            if comp is None:
+                sq, sk, sv = torch_qkv(B, H, 8192, d, dv, dtype, rank_seed(22, rank), 0, dev)
+                comp, tried = SB.select(sq, sk, sv)
+                del sq, sk, sv
+            qq, kk = comp.keys(q, dv), comp.keys(k, dv)
+            reps = 10 if N <= 16384 else 5
+            ours.append(median_ms(lambda i=0: T.prefill(cfg, N, q, k, v, out, st, stream=stream), reps, True))
+            soft.append(median_ms(lambda i=0: comp.prefill(qq, kk, v), reps, True))
+            del q, k, v, out, st, qq, kk
+        T.sync_status(stream)
+        fit = [j for j, N in enumerate(SOFTMAX_PREFILL_N) if N >= SOFTMAX_FIT_MIN_N]
+        sel = lambda xs: [xs[j] for j in fit]
+        ns_fit = sel(SOFTMAX_PREFILL_N)
+        prefill.append({
+            "dtype": dtype, "backend": comp.name, "backends_tried_ms_at_8192": tried,
+            "N": list(SOFTMAX_PREFILL_N), "ours_ms": [r4(x) for x in ours], "softmax_ms": [r4(x) for x in soft],
+            "exponent": {"ours": r4(loglog_slope(ns_fit, sel(ours))),
+                         "softmax": r4(loglog_slope(ns_fit, sel(soft))), "fit": f"N >= {SOFTMAX_FIT_MIN_N}"},
+            "crossover_N": r4(crossover_n(SOFTMAX_PREFILL_N, ours, soft)),
+            "speedup": {str(N): r4(s_ / o_) for N, o_, s_ in zip(SOFTMAX_PREFILL_N, ours, soft)
+                        if N in (8192, 65536)},
+        })
+        torch.cuda.empty_cache()
+
+    # one decode step, B=64, H=16, bf16
+    dcfg = T.Config(64, 16, d, dv, n, "bf16")
+    Bd, Hd = 64, 16
+    tq, tk, tv = (x.permute(2, 0, 1, 3).contiguous()
+                  for x in torch_qkv(Bd, Hd, 64, d, dv, "bf16", rank_seed(23, rank), 1, dev))
+    tout = torch.empty((Bd, Hd, dv), dtype=tq.dtype, device=dev)
+    sts = [T.new_states(dcfg, dev) for _ in range(DECODE_ROTATE)]
+    ours_us = 1e3 * median_ms(
+        lambda i=0: T.decode_step(dcfg, tq[i % 64], tk[i % 64], tv[i % 64], tout, sts[i % DECODE_ROTATE],
+                                  stream=stream),
+        64, False)
+    T.sync_status(stream)
+    del sts
+    soft_us, comp = [], None
+    for N in SOFTMAX_DECODE_N:
+        q, k, v = torch_qkv(Bd, Hd, N, d, dv, "bf16", rank_seed(24, rank), 0, dev)
+        if comp is None:
+            comp, dtried = SB.select(q[:, :, -1:], k, v, causal=False)
+        kc, vc = comp.cache(k, v)
+        # the new token's q in the comparator's form, made before the timed calls
+        q1 = comp.keys(q[:, :, -1], dv).contiguous()
+        k1, v1 = k[:, :, -1].contiguous(), v[:, :, -1].contiguous()
+        del q, k, v
+        soft_us.append(1e3 * median_ms(lambda i=0: comp.decode_step(q1, k1, v1, kc, vc, N - 1), 20, False))
+        del kc, vc
+        torch.cuda.empty_cache()
+    decode = {
+        "dtype": "bf16", "workload": f"B{Bd}_H{Hd}_d{d}_dv{dv}", "backend": comp.name,
+        "backends_tried_ms_at_1024": dtried, "N": list(SOFTMAX_DECODE_N),
+        "ours_us": r4(ours_us), "softmax_us": [r4(x) for x in soft_us],
+        "exponent_softmax": r4(loglog_slope(SOFTMAX_DECODE_N, soft_us)),
+        "speedup": {str(N): r4(s_ / ours_us) for N, s_ in zip(SOFTMAX_DECODE_N, soft_us)},
+        "ours_timing": "eager decode steps with the state operand in the library's own decode kernel, "
+                       f"{DECODE_ROTATE} rotated state sets",
+    }
+    return {"what": "exact causal softmax (weights exp(q.k), scale 1) on the library's fastest attention "
+                    "backend against the states path; eager calls, CUDA events, median per call",
+            "prefill": prefill, "decode": decode}
 
 
 def _profile_traffic():
@@ -876,7 +1014,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "order4", "wide", "orders"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "order4", "wide", "orders", "softmax"],
+                    default="all",
                     help="run one part (profiling captures on small cases)")
     ap.add_argument("--tc-n", type=int, default=0,
                     help="sequence length of the order4/wide workloads (default: theirs)")
