@@ -48,7 +48,7 @@ DECODE_ROTATE = 8
 APPEND_LENGTHS = (16, 32, 64, 256)
 # tsa_plan.path values (include/tsa.h)
 PATH_NAMES = ("simt", "tc", "tc_f32", "short")
-ORDER_SWEEP = (1, 2, 3, 4)
+ORDER_SWEEP = (1, 2, 3, 4, 5)
 # chunk lengths the library builds for the fp32 prefill (64: CUDA cores; 128:
 # tensor cores, the default)
 CHUNK_SWEEP = (64, 128)

@@ -28,13 +28,24 @@ __host__ __device__ constexpr int feat_dim(int dk, int nt) {
 
 __host__ __device__ constexpr int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
-// 1/sqrt(a!) for the multi-index factorials that occur up to degree 3.
-constexpr float kInvSqrt2 = 0.70710678118654752440f;  // a! = 2
-constexpr float kInvSqrt6 = 0.40824829046386301637f;  // a! = 6
+// 1/sqrt(a!) for the multi-index factorials that occur up to degree 4
+// (a! = 1, 2, 6, 24 for one repeated index, 2 * 2 = 4 for two pairs).
+constexpr float kInvSqrt2 = 0.70710678118654752440f;   // a! = 2
+constexpr float kInvSqrt6 = 0.40824829046386301637f;   // a! = 6
+constexpr float kInvSqrt24 = 0.20412414523193150818f;  // a! = 24
 
-// One entry per feature: three factor indices packed in bytes 0..2; the index
+__host__ __device__ constexpr float inv_sqrt_factorial(int f) {
+  return f == 1 ? 1.0f : f == 2 ? kInvSqrt2 : f == 4 ? 0.5f : f == 6 ? kInvSqrt6 : kInvSqrt24;
+}
+
+// The most orders any table is built for (degree NT - 1 <= 4).
+constexpr int kMaxTerms = 5;
+
+// One entry per feature: four factor indices packed in bytes 0..3; the index
 // DK names the constant 1.0 stored after the d_k inputs, so an order-m feature
-// is  w * x[i] * x[j] * x[l]  with (3 - m) of the indices equal to DK.
+// is  w * x[i] * x[j] * x[l] * x[m']  with (4 - m) of the indices equal to DK.
+// Up to order 3 byte 3 is always DK, so kernels built for NT <= 4 read three
+// factors only.
 template <int DK, int NT>
 struct FeatTab {
   static constexpr int D = feat_dim(DK, NT);
@@ -44,29 +55,42 @@ struct FeatTab {
 
 template <int DK, int NT>
 constexpr FeatTab<DK, NT> make_feat_tab() {
-  static_assert(NT >= 1 && NT <= 4, "orders 0..3 supported");
+  static_assert(NT >= 1 && NT <= kMaxTerms, "orders 0..4 supported");
   FeatTab<DK, NT> t{};
   int a = 0;
   const uint32_t one = (uint32_t)DK;
-  t.code[a] = one | (one << 8) | (one << 16); t.w[a] = 1.0f; ++a;
-  if (NT > 1)
-    for (int i = 0; i < DK; ++i) {
-      t.code[a] = (uint32_t)i | (one << 8) | (one << 16); t.w[a] = 1.0f; ++a;
+  // a multi-index given by non-decreasing factor indices (DK = no factor)
+  auto put = [&](uint32_t i, uint32_t j, uint32_t l, uint32_t m) {
+    t.code[a] = i | (j << 8) | (l << 16) | (m << 24);
+    // a! from the run lengths of the real indices
+    const uint32_t f[4] = {i, j, l, m};
+    int fact = 1, run = 1;
+    for (int u = 1; u < 4; ++u) {
+      if (f[u] != one && f[u] == f[u - 1]) {
+        ++run;
+        fact *= run;
+      } else {
+        run = 1;
+      }
     }
+    t.w[a] = inv_sqrt_factorial(fact);
+    ++a;
+  };
+  put(one, one, one, one);
+  if (NT > 1)
+    for (int i = 0; i < DK; ++i) put((uint32_t)i, one, one, one);
   if (NT > 2)
     for (int i = 0; i < DK; ++i)
-      for (int j = i; j < DK; ++j) {
-        t.code[a] = (uint32_t)i | ((uint32_t)j << 8) | (one << 16);
-        t.w[a] = (i == j) ? kInvSqrt2 : 1.0f; ++a;
-      }
+      for (int j = i; j < DK; ++j) put((uint32_t)i, (uint32_t)j, one, one);
   if (NT > 3)
     for (int i = 0; i < DK; ++i)
       for (int j = i; j < DK; ++j)
-        for (int l = j; l < DK; ++l) {
-          t.code[a] = (uint32_t)i | ((uint32_t)j << 8) | ((uint32_t)l << 16);
-          const bool ij = (i == j), jl = (j == l);
-          t.w[a] = (ij && jl) ? kInvSqrt6 : ((ij || jl) ? kInvSqrt2 : 1.0f); ++a;
-        }
+        for (int l = j; l < DK; ++l) put((uint32_t)i, (uint32_t)j, (uint32_t)l, one);
+  if (NT > 4)
+    for (int i = 0; i < DK; ++i)
+      for (int j = i; j < DK; ++j)
+        for (int l = j; l < DK; ++l)
+          for (int m = l; m < DK; ++m) put((uint32_t)i, (uint32_t)j, (uint32_t)l, (uint32_t)m);
   return t;
 }
 

@@ -84,6 +84,11 @@ decode_kernel(DecodeParams p) {
       const float w = __ldg(&g_feat<DK, NT>.w[a]);
       fq = w * xq[i] * xq[j] * xq[l];
       fk = w * xk[i] * xk[j] * xk[l];
+      if constexpr (NT > 4) {
+        const int m = cd >> 24;
+        fq *= xq[m];
+        fk *= xk[m];
+      }
     }
     phq[a] = fq; phk[a] = fk;
   }

@@ -22,6 +22,7 @@ namespace tsa {
 
 template <int DK, int NT>
 struct FeatConst {
+  static_assert(NT <= 4, "the tensor-core feature builders read three factors (orders 0..3)");
   static constexpr FeatTab<DK, NT> tab = make_feat_tab<DK, NT>();
   static constexpr int D = feat_dim(DK, NT);
   static constexpr int NB = (D + 127) / 128;   // 128-feature blocks (MMA M = 128)

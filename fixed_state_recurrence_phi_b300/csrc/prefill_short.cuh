@@ -109,6 +109,7 @@ short_prefill_kernel(ShortParams p) {
   constexpr int D = L::D, DPAD = L::DPAD, LB = L::LB, DKP = L::DKP, CG = L::CG, KW = L::KW,
                 KG = L::KG, QPT = L::QPT, VPT = L::VPT;
   static_assert(L::bytes == short_smem_bytes(DK, NT, DV), "layout size");
+  static_assert(NT <= 4, "three-factor features (orders 0..3)");
   extern __shared__ __align__(16) float sm[];
   float* st = sm + L::o_st;
   float* z = st + DPAD * DV;

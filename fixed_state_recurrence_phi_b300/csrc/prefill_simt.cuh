@@ -45,9 +45,14 @@ struct SimtLayoutDT {
   static constexpr int XS = DK + 1;      // x row stride; x[DK] = 1.0
   static constexpr int PKS = DT + 4;     // phiK row stride
   static constexpr int NTHR = 256;
+  // Order 4 (NT = 5): the state slice (4,845 rows at d_k = 16) does not fit
+  // shared memory; each CTA works on its own slice in global memory instead
+  // (in place in the caller's state or in its span's scratch slot, one value
+  // slice of W = d_v columns), read and written through L1/L2.
+  static constexpr bool SG = NT >= 5;
   static constexpr int oS = 0;
-  static constexpr int oZ = oS + DROWS * W;
-  static constexpr int oCode = oZ + DROWS;
+  static constexpr int oZ = oS + (SG ? 0 : DROWS * W);
+  static constexpr int oCode = oZ + (SG ? 0 : DROWS);
   static constexpr int oW = oCode + round_up(D, 4);
   static constexpr int oXq = oW + round_up(D, 4);
   static constexpr int oXk = oXq + round_up(C * XS, 4);
@@ -154,6 +159,11 @@ __device__ __forceinline__ void build_phi_tile(float* sm, int a0, int valid, int
       const float w = wt[a];
       if (WITH_Q) vq = w * xq[tok * L::XS + i] * xq[tok * L::XS + j] * xq[tok * L::XS + l];
       vk = w * xk[tok * L::XS + i] * xk[tok * L::XS + j] * xk[tok * L::XS + l];
+      if constexpr (NT > 4) {
+        const int m = cd >> 24;
+        if (WITH_Q) vq *= xq[tok * L::XS + m];
+        vk *= xk[tok * L::XS + m];
+      }
     }
     if (tok >= valid) vk = 0.f;
     if (WITH_Q) phq[(fg * FPG + u) * L::C + tok] = vq;
@@ -166,20 +176,21 @@ __device__ __forceinline__ void build_phi_tile(float* sm, int a0, int valid, int
 
 // S[a0 + RPT*ta + r][tc*TN + c] += sum_t phiK[t][RPT*ta + r] * V[t][tc*TN + c]
 // z[a0 + RPT*ta + r]             += sum_t phiK[t][RPT*ta + r]
+// S and z are the CTA's state slice (shared memory, or global memory in the
+// SG layout, whose rows stop at D: rows past it are neither read nor written).
 template <int DK, int NT, int W>
-__device__ __forceinline__ void update_tile(float* sm, int a0, int tid) {
+__device__ __forceinline__ void update_tile(float* sm, float* S, float* z, int a0, int tid) {
   using L = SimtLayout<DK, NT, W>;
   constexpr int TN = L::TN, RPT = L::RPT;
-  float* S = sm + L::oS;
-  float* z = sm + L::oZ;
   const float* phk = sm + L::oPhK;
   const float* vs = sm + L::oV;
   const int ta = tid >> 4, tc = tid & 15;
+  auto live = [&](int r) { return !L::SG || a0 + RPT * ta + r < L::D; };
   float s[RPT][TN];
 #pragma unroll
   for (int r = 0; r < RPT; ++r)
 #pragma unroll
-    for (int c = 0; c < TN; ++c) s[r][c] = S[(a0 + RPT * ta + r) * W + tc * TN + c];
+    for (int c = 0; c < TN; ++c) s[r][c] = live(r) ? S[(a0 + RPT * ta + r) * W + tc * TN + c] : 0.f;
   float zp[RPT];
 #pragma unroll
   for (int r = 0; r < RPT; ++r) zp[r] = 0.f;
@@ -213,14 +224,16 @@ __device__ __forceinline__ void update_tile(float* sm, int a0, int tid) {
 #pragma unroll
   for (int r = 0; r < RPT; ++r)
 #pragma unroll
-    for (int c = 0; c < TN; ++c) S[(a0 + RPT * ta + r) * W + tc * TN + c] = s[r][c];
+    for (int c = 0; c < TN; ++c)
+      if (live(r)) S[(a0 + RPT * ta + r) * W + tc * TN + c] = s[r][c];
 #pragma unroll
   for (int r = 0; r < RPT; ++r)
 #pragma unroll
     for (int off = 8; off >= 1; off >>= 1) zp[r] += __shfl_xor_sync(0xffffffffu, zp[r], off);
   if (tc == 0) {
 #pragma unroll
-    for (int r = 0; r < RPT; ++r) z[a0 + RPT * ta + r] += zp[r];
+    for (int r = 0; r < RPT; ++r)
+      if (live(r)) z[a0 + RPT * ta + r] += zp[r];
   }
 }
 
@@ -228,9 +241,20 @@ template <int DK, int NT>
 __device__ __forceinline__ void load_feat_table(uint32_t* code, float* w, int tid) {
   constexpr int D = feat_dim(DK, NT);
   for (int a = tid; a < D; a += 256) {
-    code[a] = c_feat<DK, NT>.code[a];
-    w[a] = c_feat<DK, NT>.w[a];
+    if constexpr (NT > 4) {   // 38 KB: from global memory, not the constant bank
+      code[a] = __ldg(&g_feat<DK, NT>.code[a]);
+      w[a] = __ldg(&g_feat<DK, NT>.w[a]);
+    } else {
+      code[a] = c_feat<DK, NT>.code[a];
+      w[a] = c_feat<DK, NT>.w[a];
+    }
   }
+}
+
+// Zero one head's state block of `elems` floats (a multiple of 4), by one CTA.
+__device__ __forceinline__ void zero_block(float* g, size_t elems, int tid) {
+  float4* g4 = reinterpret_cast<float4*>(g);
+  for (size_t e = tid; e < elems / 4; e += 256) g4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ---------------------------------------------------------------------------
@@ -252,8 +276,18 @@ span_state_kernel(PrefillParams p) {
   const long long t_end = min(p.N, t_begin + (long long)p.chunks_per_span * L::C);
 
   load_feat_table<DK, NT>(reinterpret_cast<uint32_t*>(sm + L::oCode), sm + L::oW, tid);
-  for (int e = tid; e < L::DROWS * W; e += 256) sm[L::oS + e] = 0.f;
-  for (int e = tid; e < L::DROWS; e += 256) sm[L::oZ + e] = 0.f;
+  float *S, *z;
+  if constexpr (L::SG) {   // the span's sum is built in its scratch slot (one slice, W = d_v)
+    float* g = p.scratch + ((size_t)head * p.n_spans + span) * (size_t)L::DPAD * (p.dv + 1);
+    zero_block(g, (size_t)L::DPAD * (p.dv + 1), tid);
+    S = g;
+    z = g + (size_t)L::DPAD * p.dv;
+  } else {
+    S = sm + L::oS;
+    z = sm + L::oZ;
+    for (int e = tid; e < L::DROWS * W; e += 256) sm[L::oS + e] = 0.f;
+    for (int e = tid; e < L::DROWS; e += 256) sm[L::oZ + e] = 0.f;
+  }
 
   const T* kg = static_cast<const T*>(p.k) + (size_t)head * p.N * DK;
   const T* vg = static_cast<const T*>(p.v) + (size_t)head * p.N * p.dv + c0;
@@ -266,13 +300,16 @@ span_state_kernel(PrefillParams p) {
     for (int tile = 0; tile < L::NTILE; ++tile) {
       build_phi_tile<DK, NT, W, false>(sm, tile * L::DT, valid, tid);
       __syncthreads();
-      update_tile<DK, NT, W>(sm, tile * L::DT, tid);
+      if constexpr (L::SG) update_tile<DK, NT, W>(sm, S, z, tile * L::DT, tid);
+      else update_tile<DK, NT, W>(sm, sm + L::oS, sm + L::oZ, tile * L::DT, tid);
       __syncthreads();
     }
   }
-  __syncthreads();
-  float* dst = p.scratch + ((size_t)head * p.n_spans + span) * (size_t)L::DPAD * (p.dv + 1);
-  state_slice_out<L::DROWS, W, L::D, L::DPAD>(dst, sm + L::oS, sm + L::oZ, p.dv, c0, slice == 0, tid);
+  if constexpr (!L::SG) {
+    __syncthreads();
+    float* dst = p.scratch + ((size_t)head * p.n_spans + span) * (size_t)L::DPAD * (p.dv + 1);
+    state_slice_out<L::DROWS, W, L::D, L::DPAD>(dst, sm + L::oS, sm + L::oZ, p.dv, c0, slice == 0, tid);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -346,8 +383,7 @@ span_output_kernel(PrefillParams p) {
   constexpr int C = L::C, TN = L::TN, XS = L::XS;
   extern __shared__ float4 smem4[];
   float* sm = reinterpret_cast<float*>(smem4);
-  float* S = sm + L::oS;
-  float* z = sm + L::oZ;
+  float *S, *z;
   const float* xq = sm + L::oXq;
   const float* xk = sm + L::oXk;
   const float* vs = sm + L::oV;
@@ -367,7 +403,16 @@ span_output_kernel(PrefillParams p) {
   const bool single = (p.n_spans == 1);
 
   load_feat_table<DK, NT>(reinterpret_cast<uint32_t*>(sm + L::oCode), sm + L::oW, tid);
-  if (single) {
+  if constexpr (L::SG) {
+    // in place: the caller's state (one span) or the span's prefix slot
+    float* g = single ? p.states + head * st_elems
+                      : p.scratch + ((size_t)head * p.n_spans + span) * st_elems;
+    if (single && !p.accumulate) zero_block(g, st_elems, tid);
+    S = g;
+    z = g + (size_t)L::DPAD * p.dv;
+  } else if (single) {
+    S = sm + L::oS;
+    z = sm + L::oZ;
     if (p.accumulate) {
       state_slice_in<L::DROWS, W, L::D, L::DPAD>(S, z, p.states + head * st_elems, p.dv, c0, tid);
     } else {
@@ -375,6 +420,8 @@ span_output_kernel(PrefillParams p) {
       for (int e = tid; e < L::DROWS; e += 256) z[e] = 0.f;
     }
   } else {
+    S = sm + L::oS;
+    z = sm + L::oZ;
     state_slice_in<L::DROWS, W, L::D, L::DPAD>(
         S, z, p.scratch + ((size_t)head * p.n_spans + span) * st_elems, p.dv, c0, tid);
   }
@@ -464,8 +511,9 @@ span_output_kernel(PrefillParams p) {
       const int a0 = tile * L::DT;
       build_phi_tile<DK, NT, W, true>(sm, a0, valid, tid);
       __syncthreads();
+      const int amax = L::SG ? min(L::DT, L::D - a0) : L::DT;   // rows past D: global state ends
 #pragma unroll 8
-      for (int a = 0; a < L::DT; ++a) {
+      for (int a = 0; a < amax; ++a) {
         const float4 qq = *reinterpret_cast<const float4*>(phq + a * C + 4 * tr);
         float ss[TN];
         if constexpr (TN == 4) {
@@ -485,13 +533,13 @@ span_output_kernel(PrefillParams p) {
       for (int h = 0; h < L::DT / 16; ++h) {
         const int a = tc + 16 * h;
         const float4 qq = *reinterpret_cast<const float4*>(phq + a * C + 4 * tr);
-        const float zz = z[a0 + a];
+        const float zz = (!L::SG || a0 + a < L::D) ? z[a0 + a] : 0.f;
         den[0] = fmaf(qq.x, zz, den[0]); den[1] = fmaf(qq.y, zz, den[1]);
         den[2] = fmaf(qq.z, zz, den[2]); den[3] = fmaf(qq.w, zz, den[3]);
       }
       __syncthreads();
       if (need_update) {
-        update_tile<DK, NT, W>(sm, a0, tid);
+        update_tile<DK, NT, W>(sm, S, z, a0, tid);
         __syncthreads();
       }
     }
@@ -517,7 +565,7 @@ span_output_kernel(PrefillParams p) {
     }
   }
 
-  if (single) {
+  if (!L::SG && single) {
     __syncthreads();
     state_slice_out<L::DROWS, W, L::D, L::DPAD>(p.states + head * st_elems, S, z, p.dv, c0,
                                                 slice == 0, tid);

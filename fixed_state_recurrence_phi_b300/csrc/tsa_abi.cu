@@ -98,10 +98,15 @@ tsa_status check_config(const tsa_config* c) {
   if (c->d_k != 16 && c->d_k != 32) return fail(TSA_ERR_UNSUPPORTED, "d_k=%d not built (16, 32)", c->d_k);
   if (c->d_v != 32 && c->d_v != 64 && c->d_v != 128)
     return fail(TSA_ERR_UNSUPPORTED, "d_v=%d not built (32, 64, 128)", c->d_v);
-  if (c->n_terms > 4) return fail(TSA_ERR_UNSUPPORTED, "n_terms=%d not built (1..4)", c->n_terms);
-  if (feat_dim(c->d_k, c->n_terms) > 1024)
+  if (c->n_terms > kMaxTerms) return fail(TSA_ERR_UNSUPPORTED, "n_terms=%d not built (1..5)", c->n_terms);
+  // up to 1,024 features (8 blocks of 128) on every path; the order-4 state of
+  // d_k = 16 (4,845 features) on the CUDA cores with the state in global memory
+  const bool wide_built = c->d_k == 16 && c->n_terms == 5;
+  if (feat_dim(c->d_k, c->n_terms) > 1024 && !wide_built)
     return fail(TSA_ERR_UNSUPPORTED, "feature dim %d > 1024 (d_k=%d, n=%d)",
                 feat_dim(c->d_k, c->n_terms), c->d_k, c->n_terms);
+  if (wide_built && c->d_v != 32 && c->d_v != 64)
+    return fail(TSA_ERR_UNSUPPORTED, "n_terms=5 is built for d_v = 32 or 64 (one value slice), not %d", c->d_v);
   return TSA_OK;
 }
 
@@ -196,12 +201,19 @@ static size_t simt_smem_bytes(int dk, int nt, int W) {
   if (dk == DK && nt == NT)                                                \
     return W == 64 ? SimtLayout<DK, NT, 64>::bytes : SimtLayout<DK, NT, 32>::bytes;
   TSA_SMEM_CASE(16, 1) TSA_SMEM_CASE(16, 2) TSA_SMEM_CASE(16, 3) TSA_SMEM_CASE(16, 4)
-  TSA_SMEM_CASE(32, 1) TSA_SMEM_CASE(32, 2) TSA_SMEM_CASE(32, 3)
+  TSA_SMEM_CASE(16, 5) TSA_SMEM_CASE(32, 1) TSA_SMEM_CASE(32, 2) TSA_SMEM_CASE(32, 3)
 #undef TSA_SMEM_CASE
   return 0;
 }
 
 static constexpr size_t kSmemLimit = 227 * 1024;
+
+// The CUDA-core slice width: 64 where d_v allows and the layout fits, else
+// 32; the global-state layout (order 4 at d_k = 16) takes one slice, W = d_v.
+static int simt_width(const tsa_config* c) {
+  if (c->n_terms >= 5) return c->d_v;
+  return (c->d_v % 64 == 0 && simt_smem_bytes(c->d_k, c->n_terms, 64) <= kSmemLimit) ? 64 : 32;
+}
 static constexpr size_t kSmemPerSm = 228 * 1024;
 
 // Tensor-core plan (bf16 inputs): chunks of 128 tokens, d_v sliced under the
@@ -324,7 +336,7 @@ tsa_status make_plan(const tsa_config* c, long long N, int num_sms, tsa_plan* pl
   const int chunk = 64;
   if (c->chunk != 0 && c->chunk != chunk)
     return fail(TSA_ERR_UNSUPPORTED, "chunk=%d not built (0 or 64)", c->chunk);
-  int W = (c->d_v % 64 == 0 && simt_smem_bytes(c->d_k, c->n_terms, 64) <= kSmemLimit) ? 64 : 32;
+  const int W = simt_width(c);
   const size_t smem = simt_smem_bytes(c->d_k, c->n_terms, W);
   if (smem == 0 || smem > kSmemLimit) return fail(TSA_ERR_UNSUPPORTED, "no kernel fits shared memory");
   const int occ = std::max(1, std::min(2, (int)(kSmemPerSm / (smem + 1024))));
@@ -398,7 +410,7 @@ static tsa_status dispatch_prefill(const tsa_config* c, const tsa_plan& pl, Pref
                                    cudaStream_t s) {
 #define TSA_PF_CASE(DK, NT) \
   if (c->d_k == DK && c->n_terms == NT) return dispatch_prefill_w<T, DK, NT>(pl, p, s);
-  TSA_PF_CASE(16, 1) TSA_PF_CASE(16, 2) TSA_PF_CASE(16, 3) TSA_PF_CASE(16, 4)
+  TSA_PF_CASE(16, 1) TSA_PF_CASE(16, 2) TSA_PF_CASE(16, 3) TSA_PF_CASE(16, 4) TSA_PF_CASE(16, 5)
   TSA_PF_CASE(32, 1) TSA_PF_CASE(32, 2) TSA_PF_CASE(32, 3)
 #undef TSA_PF_CASE
   return fail(TSA_ERR_UNSUPPORTED, "no prefill kernel for d_k=%d n=%d", c->d_k, c->n_terms);
@@ -429,7 +441,7 @@ static tsa_status dispatch_states_simt(const tsa_config* c, const tsa_plan& pl, 
   if (c->d_k == DK && c->n_terms == NT)                                      \
     return pl.slice_width == 64 ? launch_states_simt<T, DK, NT, 64>(pl, p, s) \
                                 : launch_states_simt<T, DK, NT, 32>(pl, p, s);
-  TSA_ST_CASE(16, 1) TSA_ST_CASE(16, 2) TSA_ST_CASE(16, 3) TSA_ST_CASE(16, 4)
+  TSA_ST_CASE(16, 1) TSA_ST_CASE(16, 2) TSA_ST_CASE(16, 3) TSA_ST_CASE(16, 4) TSA_ST_CASE(16, 5)
   TSA_ST_CASE(32, 1) TSA_ST_CASE(32, 2) TSA_ST_CASE(32, 3)
 #undef TSA_ST_CASE
   return fail(TSA_ERR_UNSUPPORTED, "no span pass for d_k=%d n=%d", c->d_k, c->n_terms);
@@ -451,7 +463,7 @@ tsa_status make_states_plan(const tsa_config* c, long long N, int num_sms, tsa_p
   } else if (c->dtype == TSA_F32 && tc32_fits(c->d_k, c->n_terms, c->d_v)) {
     chunk = 128; path = TSA_PATH_TC_F32; smem = tc32_smem(c->d_k, c->n_terms, c->d_v);
   } else {
-    const int W = (c->d_v % 64 == 0 && simt_smem_bytes(c->d_k, c->n_terms, 64) <= kSmemLimit) ? 64 : 32;
+    const int W = simt_width(c);
     smem = simt_smem_bytes(c->d_k, c->n_terms, W);
     if (smem == 0 || smem > kSmemLimit) return fail(TSA_ERR_UNSUPPORTED, "no kernel fits shared memory");
     slice_w = W;
@@ -514,7 +526,7 @@ template <typename T>
 static tsa_status dispatch_decode(const tsa_config* c, DecodeParams p, cudaStream_t s) {
 #define TSA_DC_CASE(DK, NT) \
   if (c->d_k == DK && c->n_terms == NT) return dispatch_decode_dv<T, DK, NT>(c->d_v, p, s);
-  TSA_DC_CASE(16, 1) TSA_DC_CASE(16, 2) TSA_DC_CASE(16, 3) TSA_DC_CASE(16, 4)
+  TSA_DC_CASE(16, 1) TSA_DC_CASE(16, 2) TSA_DC_CASE(16, 3) TSA_DC_CASE(16, 4) TSA_DC_CASE(16, 5)
   TSA_DC_CASE(32, 1) TSA_DC_CASE(32, 2) TSA_DC_CASE(32, 3)
 #undef TSA_DC_CASE
   return fail(TSA_ERR_UNSUPPORTED, "no decode kernel for d_k=%d n=%d", c->d_k, c->n_terms);
@@ -533,7 +545,7 @@ __global__ void feature_map_kernel(const float* __restrict__ x, float* __restric
     const uint32_t code = g_feat<DK, NT>.code[a];
     float v = g_feat<DK, NT>.w[a];
 #pragma unroll
-    for (int f = 0; f < 3; ++f) {
+    for (int f = 0; f < (NT > 4 ? 4 : 3); ++f) {
       const int i = (int)((code >> (8 * f)) & 255u);
       if (i != DK) v *= x[r * DK + i];
     }
@@ -578,16 +590,17 @@ tsa_status tsa_feature_index(int d_k, int n_terms, int* idx, float* weight) {
 #define TSA_FI_CASE(DK, NT)                                                  \
   if (d_k == DK && n_terms == NT) {                                          \
     constexpr FeatTab<DK, NT> t = make_feat_tab<DK, NT>();                   \
+    constexpr int F = NT > 4 ? NT - 1 : 3;                                   \
     for (int a = 0; a < FeatTab<DK, NT>::D; ++a) {                           \
-      for (int f = 0; f < 3; ++f) {                                          \
+      for (int f = 0; f < F; ++f) {                                          \
         const int i = (int)((t.code[a] >> (8 * f)) & 255u);                  \
-        idx[3 * a + f] = (i == DK) ? -1 : i;                                 \
+        idx[F * a + f] = (i == DK) ? -1 : i;                                 \
       }                                                                      \
       weight[a] = t.w[a];                                                    \
     }                                                                        \
     return TSA_OK;                                                           \
   }
-  TSA_FI_CASE(16, 1) TSA_FI_CASE(16, 2) TSA_FI_CASE(16, 3) TSA_FI_CASE(16, 4)
+  TSA_FI_CASE(16, 1) TSA_FI_CASE(16, 2) TSA_FI_CASE(16, 3) TSA_FI_CASE(16, 4) TSA_FI_CASE(16, 5)
   TSA_FI_CASE(32, 1) TSA_FI_CASE(32, 2) TSA_FI_CASE(32, 3)
 #undef TSA_FI_CASE
   return fail(TSA_ERR_UNSUPPORTED, "no feature table for d_k=%d n=%d", d_k, n_terms);
@@ -607,7 +620,7 @@ tsa_status tsa_feature_map(int d_k, int n_terms, int64_t rows, const float* x, f
     cudaError_t e = cudaGetLastError();                                                        \
     return e == cudaSuccess ? TSA_OK : cuda_fail(e, "launch feature_map");                     \
   }
-  TSA_FM_CASE(16, 1) TSA_FM_CASE(16, 2) TSA_FM_CASE(16, 3) TSA_FM_CASE(16, 4)
+  TSA_FM_CASE(16, 1) TSA_FM_CASE(16, 2) TSA_FM_CASE(16, 3) TSA_FM_CASE(16, 4) TSA_FM_CASE(16, 5)
   TSA_FM_CASE(32, 1) TSA_FM_CASE(32, 2) TSA_FM_CASE(32, 3)
 #undef TSA_FM_CASE
   return fail(TSA_ERR_UNSUPPORTED, "no feature table for d_k=%d n=%d", d_k, n_terms);

@@ -160,11 +160,13 @@ def state_bytes(cfg) -> int:
 
 
 def feature_index(d_k: int, n_terms: int):
+    """(idx [D, F], weight [D]) of the state rows, F = max(3, n_terms - 1)."""
     D = feature_dim(d_k, n_terms)
-    idx = (ctypes.c_int * (3 * max(D, 1)))()
+    F = max(3, n_terms - 1)
+    idx = (ctypes.c_int * (F * max(D, 1)))()
     w = (ctypes.c_float * max(D, 1))()
     _check("tsa_feature_index", _lib.tsa_feature_index(d_k, n_terms, idx, w))
-    return np.array(idx[:3 * D], dtype=np.int32).reshape(D, 3), np.array(w[:D], dtype=np.float32)
+    return np.array(idx[:F * D], dtype=np.int32).reshape(D, F), np.array(w[:D], dtype=np.float32)
 
 
 def feature_map(d_k: int, n_terms: int, x, out, stream=None):

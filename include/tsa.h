@@ -60,7 +60,9 @@ typedef struct {
   int H;            /* heads; B*H independent (b,h) heads                     */
   int d_k;          /* query/key width d: 16 or 32                            */
   int d_v;          /* value width: 32, 64 or 128                             */
-  int n_terms;      /* n Taylor terms, orders 0..n-1: 1..4 (feature dim <= 1024) */
+  int n_terms;      /* n Taylor terms, orders 0..n-1: 1..4 (feature dim <= 1024);
+                       5 at d_k = 16 (4,845 features) with d_v 32 or 64, on the
+                       CUDA-core path with each head's state in global memory */
   tsa_dtype dtype;  /* element type of q, k, v and out (states are always fp32) */
   int chunk;        /* prefill chunk length; 0 = library's choice (see tsa_plan) */
 } tsa_config;
@@ -89,10 +91,10 @@ size_t tsa_state_elems(const tsa_config* cfg);
  * Rows a >= D are padding and stay exactly 0. */
 size_t tsa_state_bytes(const tsa_config* cfg);
 
-/* Feature ordering: for row a < D of the state, idx[3a..3a+2] are the input
- * indices whose product forms the monomial (-1 = no factor; an order-m row has
- * m indices >= 0, non-decreasing) and weight[a] = 1/sqrt(a!). Host only; idx
- * holds 3*D ints, weight D floats. */
+/* Feature ordering: for row a < D of the state, idx[F*a .. F*a+F-1] are the
+ * input indices whose product forms the monomial, F = max(3, n_terms - 1)
+ * (-1 = no factor; an order-m row has m indices >= 0, non-decreasing) and
+ * weight[a] = 1/sqrt(a!). Host only; idx holds F*D ints, weight D floats. */
 tsa_status tsa_feature_index(int d_k, int n_terms, int* idx, float* weight);
 
 /* The feature map phi(x) = [phi_0(x) | ... | phi_{n-1}(x)] of `rows` inputs, in

@@ -51,7 +51,7 @@ def test_sizes(T):
     assert T.feature_dim(16, 4) == 969 and T.feature_dim(32, 3) == 561
 
 
-@pytest.mark.parametrize("d,n", [(16, 1), (16, 2), (16, 3), (16, 4), (32, 3)])
+@pytest.mark.parametrize("d,n", [(16, 1), (16, 2), (16, 3), (16, 4), (16, 5), (32, 3)])
 def test_feature_order_matches_oracle(T, d, n):
     """The CUDA feature table (rows of the state) enumerates the same monomials
     in the same order with the same 1/sqrt(a!) weights as the oracle."""
@@ -62,6 +62,19 @@ def test_feature_order_matches_oracle(T, d, n):
     assert got == want
     ww = np.array([1.0 / math.sqrt(O._alpha_factorial(t)) for t in want], dtype=np.float32)
     assert np.array_equal(w, ww)
+
+
+def test_order_five_plans(T):
+    """n = 5 at d_k = 16 (4,845 features): the CUDA-core path, one value slice
+    of d_v columns, both dtypes, from one span to many."""
+    assert T.feature_dim(16, 5) == 4845 == 1 + 16 + 136 + 816 + 3876
+    for dt in ("f32", "bf16"):
+        for dv in (32, 64):
+            for N in (1, 64, 300, 8192):
+                p = T.prefill_plan(T.Config(1, 8, 16, dv, 5, dt), N, num_sms=148)
+                assert p["path"] == T.TSA_PATH_SIMT and p["n_slices"] == 1 and p["slice_width"] == dv
+                assert p["n_spans"] * p["chunks_per_span"] >= -(-N // 64)
+    assert T.prefill_plan(T.Config(1, 8, 16, 64, 5), 8192, num_sms=148)["n_spans"] > 1
 
 
 def test_plan_covers_all_chunks(T):
@@ -133,7 +146,8 @@ def test_validation_codes(T):
     cases = [
         (T.Config(1, 1, 8, 64, 3), T.TSA_ERR_UNSUPPORTED),
         (T.Config(1, 1, 16, 48, 3), T.TSA_ERR_UNSUPPORTED),
-        (T.Config(1, 1, 16, 64, 5), T.TSA_ERR_UNSUPPORTED),
+        (T.Config(1, 1, 16, 64, 6), T.TSA_ERR_UNSUPPORTED),
+        (T.Config(1, 1, 16, 128, 5), T.TSA_ERR_UNSUPPORTED),  # order 4: one value slice only
         (T.Config(1, 1, 32, 64, 4), T.TSA_ERR_UNSUPPORTED),   # D = 6545 > 1024
         (T.Config(0, 1, 16, 64, 3), T.TSA_ERR_INVALID),
         (T.Config(1, 1, 16, 64, 0), T.TSA_ERR_INVALID),

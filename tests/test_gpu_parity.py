@@ -206,7 +206,7 @@ def test_order_sweep_against_softmax(G, d, dtype):
     truncation error to within the parity tolerance, and it falls strictly
     from one order to the next."""
     T, O = G.T, G.O
-    orders = [1, 2, 3, 4] if d == 16 else [1, 2, 3]
+    orders = [1, 2, 3, 4, 5] if d == 16 else [1, 2, 3]
     B, H, N, dv = 1, 4, 512, 64
     errs = []
     for n in orders:
@@ -221,9 +221,15 @@ def test_order_sweep_against_softmax(G, d, dtype):
             e_gpu = max(e_gpu, G.rel_err(og[0, h], sm))
             e_ref = max(e_ref, G.rel_err(ref, sm))
         assert abs(e_gpu - e_ref) <= G.TOL[dtype], (n, e_gpu, e_ref)
-        errs.append((T.state_elems(cfg), e_gpu))
-    for (s0, e0), (s1, e1) in zip(errs, errs[1:]):
-        assert s1 > s0 and e1 < e0, errs
+        errs.append((T.state_elems(cfg), e_gpu, e_ref))
+    # the truncation error falls with every order; the GPU's error with it
+    # wherever the drop exceeds twice the rounding of the output dtype (bf16:
+    # 2^-8; from n = 4 to 5 the drop, ~2e-3, is below that in bf16)
+    noise = 2.0 ** -8 if dtype == "bf16" else 0.0
+    for (s0, e0, r0), (s1, e1, r1) in zip(errs, errs[1:]):
+        assert s1 > s0 and r1 < r0, errs
+        if r0 - r1 > 2 * noise:
+            assert e1 < e0, errs
 
 
 def test_merge_of_segments_equals_whole(G):
