@@ -36,7 +36,7 @@ def _unit_rows(K, d, seed):
     return x / torch.linalg.vector_norm(x, dim=1, keepdim=True)
 
 
-@pytest.mark.parametrize("d,n", [(16, 4), (32, 3)])
+@pytest.mark.parametrize("d,n", [(16, 4), (16, 5), (32, 3)])
 def test_width_by_rank_of_stacked_features(G, d, n):
     T, O = G.T, G.O
     K = 2000
@@ -52,16 +52,18 @@ def test_width_by_rank_of_stacked_features(G, d, n):
     off = 0
     for m in range(n):
         w = math.comb(d + m - 1, m)
-        full = torch.ones((K, 1), device="cuda", dtype=torch.float64)
-        for _ in range(m):   # the full tensor power, d^m columns
-            full = torch.einsum("ka,kb->kab", full, x64).reshape(K, -1)
         block = phi[:, off:off + w].double()
-        r_full = int(torch.linalg.matrix_rank(full, rtol=1e-8).item())
-        r_block = int(torch.linalg.matrix_rank(block, rtol=1e-5).item())
-        r_both = int(torch.linalg.matrix_rank(torch.cat([full, block], dim=1), rtol=1e-5).item())
-        assert r_full == w, (m, r_full, w)
-        assert r_block == w, (m, r_block, w)
-        assert r_both == w, (m, r_both, w)
+        if m <= 3:   # the order-4 block (3,876 columns, 65,536 for the full power) is
+            # checked through its exact enumeration (host test) and the closed form
+            full = torch.ones((K, 1), device="cuda", dtype=torch.float64)
+            for _ in range(m):   # the full tensor power, d^m columns
+                full = torch.einsum("ka,kb->kab", full, x64).reshape(K, -1)
+            r_full = int(torch.linalg.matrix_rank(full, rtol=1e-8).item())
+            r_block = int(torch.linalg.matrix_rank(block, rtol=1e-5).item())
+            r_both = int(torch.linalg.matrix_rank(torch.cat([full, block], dim=1), rtol=1e-5).item())
+            assert r_full == w, (m, r_full, w)
+            assert r_block == w, (m, r_block, w)
+            assert r_both == w, (m, r_both, w)
         # <phi_m(q), phi_m(k)> = (q.k)^m / m! for pairs of the rows
         q_, k_ = block[: K // 2], block[K // 2:]
         dots = (x64[: K // 2] * x64[K // 2:]).sum(1)
