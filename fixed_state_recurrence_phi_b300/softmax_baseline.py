@@ -20,12 +20,13 @@ backend runs instead; that is only for checking the conventions without a GPU.
 The library's fast kernels do not all take d_k != d_v. Zero-padding q and k
 to d_v columns leaves every q.k unchanged, so the padded call computes the
 same attention; `select` times the backends in both forms on
-a sample and keeps the fastest, so the comparator is never handicapped by a
-form the library runs slowly.
+the inputs at hand and keeps the fastest, so the comparator is never
+handicapped by a form the library runs slowly at that size.
 """
 from __future__ import annotations
 
-import time
+import statistics
+import warnings
 
 import torch
 import torch.nn.functional as F
@@ -100,31 +101,40 @@ def candidates(device) -> list:
     return [SoftmaxAttention(b, p) for b in FAST_BACKENDS for p in (False, True)]
 
 
-def select(q, k, v, causal: bool = True, reps: int = 3):
+def select(q, k, v, causal: bool = True, reps: int = 5):
     """The fastest comparator for these inputs ([B, H, L, *] queries against
     [B, H, S, *] keys and values on CUDA; causal for a prefill, not causal for
     the single query of a decode step) among the library's fast backends,
-    unpadded and padded. Returns (comparator, {name: ms or the refusal}).
-    Backends that refuse the shapes or dtype are skipped; ValueError if none
-    takes them."""
+    unpadded and padded, each timed with CUDA events on the current stream
+    (median of `reps` calls after one untimed call). Returns (comparator,
+    {name: ms or the refusal}). Backends that refuse the shapes or dtype are
+    skipped; ValueError if none takes them."""
     d_v = v.shape[-1]
+    stream = torch.cuda.current_stream(q.device)
     tried, best, best_ms = {}, None, float("inf")
     for c in candidates(q.device):
         qq, kk = c.keys(q, d_v), c.keys(k, d_v)
         try:
-            c.attend(qq, kk, v, causal)
+            with warnings.catch_warnings():   # a refusal is expected here, not news
+                warnings.simplefilter("ignore", UserWarning)
+                c.attend(qq, kk, v, causal)
             torch.cuda.synchronize(q.device)
         except RuntimeError as e:
             tried[c.name] = f"refused: {str(e).splitlines()[0][:80]}"
             continue
-        t0 = time.perf_counter()
+        evs = []
         for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
             c.attend(qq, kk, v, causal)
+            b.record(stream)
+            evs.append((a, b))
         torch.cuda.synchronize(q.device)
-        ms = (time.perf_counter() - t0) * 1e3 / reps
+        ms = statistics.median(a.elapsed_time(b) for a, b in evs)
         tried[c.name] = round(ms, 4)
         if ms < best_ms:
             best, best_ms = c, ms
+        del qq, kk
     if best is None:
         raise ValueError(f"no softmax attention backend takes these inputs: {tried}")
     return best, tried
