@@ -48,8 +48,11 @@ struct SimtLayoutDT {
   // Order 4 (NT = 5): the state slice (4,845 rows at d_k = 16) does not fit
   // shared memory; each CTA works on its own slice in global memory instead
   // (in place in the caller's state or in its span's scratch slot, one value
-  // slice of W = d_v columns), read and written through L1/L2.
-  static constexpr bool SG = NT >= 5;
+  // slice of W = d_v columns), read and written through L1/L2. Order 3 with
+  // 64 columns (969 x 64 floats, 248 KB) takes the same layout: one slice
+  // instead of two 32-column ones in shared memory builds every feature tile
+  // once and gives each thread 4 x 4 outputs per pair of operand loads.
+  static constexpr bool SG = NT >= 5 || (NT == 4 && W == 64);
   static constexpr int oS = 0;
   static constexpr int oZ = oS + (SG ? 0 : DROWS * W);
   static constexpr int oCode = oZ + (SG ? 0 : DROWS);

@@ -209,9 +209,11 @@ static size_t simt_smem_bytes(int dk, int nt, int W) {
 static constexpr size_t kSmemLimit = 227 * 1024;
 
 // The CUDA-core slice width: 64 where d_v allows and the layout fits, else
-// 32; the global-state layout (order 4 at d_k = 16) takes one slice, W = d_v.
+// 32. The layouts that keep the state slice in global memory (n = 5; n = 4
+// with W = 64) take one slice, W = d_v.
 static int simt_width(const tsa_config* c) {
-  if (c->n_terms >= 5) return c->d_v;
+  if (c->n_terms >= 5 || (c->n_terms == 4 && c->d_v == 64)) return c->d_v;
+  if (c->n_terms == 4) return 32;
   return (c->d_v % 64 == 0 && simt_smem_bytes(c->d_k, c->n_terms, 64) <= kSmemLimit) ? 64 : 32;
 }
 static constexpr size_t kSmemPerSm = 228 * 1024;

@@ -62,7 +62,8 @@ typedef struct {
   int d_v;          /* value width: 32, 64 or 128                             */
   int n_terms;      /* n Taylor terms, orders 0..n-1: 1..4 (feature dim <= 1024);
                        5 at d_k = 16 (4,845 features) with d_v 32 or 64, on the
-                       CUDA-core path with each head's state in global memory */
+                       CUDA-core path with each CTA's state slice in global
+                       memory */
   tsa_dtype dtype;  /* element type of q, k, v and out (states are always fp32) */
   int chunk;        /* prefill chunk length; 0 = library's choice (see tsa_plan) */
 } tsa_config;
