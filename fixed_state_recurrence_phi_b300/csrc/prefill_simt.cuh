@@ -514,9 +514,7 @@ span_output_kernel(PrefillParams p) {
       const int a0 = tile * L::DT;
       build_phi_tile<DK, NT, W, true>(sm, a0, valid, tid);
       __syncthreads();
-      const int amax = L::SG ? min(L::DT, L::D - a0) : L::DT;   // rows past D: global state ends
-#pragma unroll 8
-      for (int a = 0; a < amax; ++a) {
+      auto readout_row = [&](int a) {
         const float4 qq = *reinterpret_cast<const float4*>(phq + a * C + 4 * tr);
         float ss[TN];
         if constexpr (TN == 4) {
@@ -531,6 +529,35 @@ span_output_kernel(PrefillParams p) {
         for (int r = 0; r < 4; ++r)
 #pragma unroll
           for (int c = 0; c < TN; ++c) acc[r][c] = fmaf(qr[r], ss[c], acc[r][c]);
+      };
+      if constexpr (L::SG) {
+        // rows from global memory: 16 loads in flight per thread on full
+        // tiles; the last tile stops at D, where the global state ends
+        const int amax = min(L::DT, L::D - a0);
+        if (amax == L::DT && TN == 4) {
+          // 16 rows' loads issued before their FMAs
+          for (int b = 0; b < L::DT; b += 16) {
+            float4 sv[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+              sv[u] = *reinterpret_cast<const float4*>(S + (a0 + b + u) * W + tc * 4);
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const float4 qq = *reinterpret_cast<const float4*>(phq + (b + u) * C + 4 * tr);
+              const float qr[4] = {qq.x, qq.y, qq.z, qq.w};
+              const float ss[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
+#pragma unroll
+              for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(qr[r], ss[c], acc[r][c]);
+            }
+          }
+        } else {
+          for (int a = 0; a < amax; ++a) readout_row(a);
+        }
+      } else {
+#pragma unroll 8
+        for (int a = 0; a < L::DT; ++a) readout_row(a);
       }
 #pragma unroll
       for (int h = 0; h < L::DT / 16; ++h) {
