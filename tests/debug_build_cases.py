@@ -120,6 +120,8 @@ def main():
     prefill_case(32, 64, 2, "bf16", 40, H=4, accumulate_pre=100)   # append form, d_k 32
     prefill_case(16, 64, 3, "bf16", 24, H=4)                       # append form from a zero state
     prefill_case(16, 64, 3, "bf16", 1, H=4, chunk=128, accumulate_pre=129)   # append form, one token
+    prefill_case(16, 64, 4, "f32", 300, expect_path=T.TSA_PATH_SIMT)          # one 64-column slice, global state
+    prefill_case(16, 64, 5, "f32", 200, expect_path=T.TSA_PATH_SIMT, accumulate_pre=70)   # n = 5, several spans
     decode_merge_states_case()
     feature_map_case()
     print("debug build ok")
