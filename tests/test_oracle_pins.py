@@ -53,6 +53,7 @@ def pin_widths():
     assert O.feature_dim(16, 3) == 153
     assert O.feature_dim(16, 4) == 969
     assert O.feature_dim(32, 3) == 561
+    assert O.feature_dim(16, 5) == 4845 == 969 + math.comb(19, 4)
     x = np.random.default_rng(1).standard_normal((3, 7))
     assert O.phi(x, 4).shape == (3, O.feature_dim(7, 4))
 
