@@ -60,7 +60,7 @@ typedef struct {
   int H;            /* heads; B*H independent (b,h) heads                     */
   int d_k;          /* query/key width d: 16 or 32                            */
   int d_v;          /* value width: 32, 64 or 128                             */
-  int n_terms;      /* n Taylor terms, orders 0..n-1: 1..4 (feature dim <= 1024);
+  int n_terms;      /* n Taylor terms, orders 0..n-1: 1..4 (feature dim <= 1024), or
                        5 at d_k = 16 (4,845 features) with d_v 32 or 64, on the
                        CUDA-core path with each CTA's state slice in global
                        memory */
