@@ -240,6 +240,77 @@ __device__ __forceinline__ void update_tile(float* sm, float* S, float* z, int a
   }
 }
 
+// The span pass in the global-state layout: the same update, with this
+// thread's state rows of the tile in registers (s) on entry and the rows of
+// the tile at pf_a0 (this thread's again: a thread owns the same rows in
+// every tile pass) loaded into s before it returns, their loads issued before
+// this tile's token loop so that their latency overlaps it; pf_a0 < 0: none.
+template <int DK, int NT, int W>
+__device__ __forceinline__ void update_tile_sg(float* sm, float* S, float* z, int a0, int pf_a0,
+                                               float (&s)[SimtLayout<DK, NT, W>::RPT][SimtLayout<DK, NT, W>::TN],
+                                               int tid) {
+  using L = SimtLayout<DK, NT, W>;
+  constexpr int TN = L::TN, RPT = L::RPT;
+  static_assert(L::SG, "global-state layout only");
+  const float* phk = sm + L::oPhK;
+  const float* vs = sm + L::oV;
+  const int ta = tid >> 4, tc = tid & 15;
+  float nx[RPT][TN];
+#pragma unroll
+  for (int r = 0; r < RPT; ++r)
+#pragma unroll
+    for (int c = 0; c < TN; ++c)
+      nx[r][c] = (pf_a0 >= 0 && pf_a0 + RPT * ta + r < L::D) ? S[(pf_a0 + RPT * ta + r) * W + tc * TN + c] : 0.f;
+  float zp[RPT];
+#pragma unroll
+  for (int r = 0; r < RPT; ++r) zp[r] = 0.f;
+#pragma unroll 8
+  for (int t = 0; t < L::C; ++t) {
+    float kk[RPT];
+    if constexpr (RPT == 4) {
+      const float4 x = *reinterpret_cast<const float4*>(phk + t * L::PKS + 4 * ta);
+      kk[0] = x.x; kk[1] = x.y; kk[2] = x.z; kk[3] = x.w;
+    } else {
+      const float2 x = *reinterpret_cast<const float2*>(phk + t * L::PKS + 2 * ta);
+      kk[0] = x.x; kk[1] = x.y;
+    }
+    float vv[TN];
+    if constexpr (TN == 4) {
+      const float4 x = *reinterpret_cast<const float4*>(vs + t * W + tc * 4);
+      vv[0] = x.x; vv[1] = x.y; vv[2] = x.z; vv[3] = x.w;
+    } else {
+      const float2 x = *reinterpret_cast<const float2*>(vs + t * W + tc * 2);
+      vv[0] = x.x; vv[1] = x.y;
+    }
+#pragma unroll
+    for (int r = 0; r < RPT; ++r)
+#pragma unroll
+      for (int c = 0; c < TN; ++c) s[r][c] = fmaf(kk[r], vv[c], s[r][c]);
+    if ((t & 15) == tc) {
+#pragma unroll
+      for (int r = 0; r < RPT; ++r) zp[r] += kk[r];
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < RPT; ++r)
+#pragma unroll
+    for (int c = 0; c < TN; ++c)
+      if (a0 + RPT * ta + r < L::D) S[(a0 + RPT * ta + r) * W + tc * TN + c] = s[r][c];
+#pragma unroll
+  for (int r = 0; r < RPT; ++r)
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) zp[r] += __shfl_xor_sync(0xffffffffu, zp[r], off);
+  if (tc == 0) {
+#pragma unroll
+    for (int r = 0; r < RPT; ++r)
+      if (a0 + RPT * ta + r < L::D) z[a0 + RPT * ta + r] += zp[r];
+  }
+#pragma unroll
+  for (int r = 0; r < RPT; ++r)
+#pragma unroll
+    for (int c = 0; c < TN; ++c) s[r][c] = nx[r][c];
+}
+
 template <int DK, int NT>
 __device__ __forceinline__ void load_feat_table(uint32_t* code, float* w, int tid) {
   constexpr int D = feat_dim(DK, NT);
@@ -294,6 +365,12 @@ span_state_kernel(PrefillParams p) {
 
   const T* kg = static_cast<const T*>(p.k) + (size_t)head * p.N * DK;
   const T* vg = static_cast<const T*>(p.v) + (size_t)head * p.N * p.dv + c0;
+  // global-state layout: this thread's rows of the next tile, prefetched
+  float srow[L::RPT][L::TN];
+#pragma unroll
+  for (int r = 0; r < L::RPT; ++r)
+#pragma unroll
+    for (int c = 0; c < L::TN; ++c) srow[r][c] = 0.f;   // the slot starts at zero
   for (long long t0 = t_begin; t0 < t_end; t0 += L::C) {
     const int valid = (int)min((long long)L::C, t_end - t0);
     __syncthreads();
@@ -303,8 +380,14 @@ span_state_kernel(PrefillParams p) {
     for (int tile = 0; tile < L::NTILE; ++tile) {
       build_phi_tile<DK, NT, W, false>(sm, tile * L::DT, valid, tid);
       __syncthreads();
-      if constexpr (L::SG) update_tile<DK, NT, W>(sm, S, z, tile * L::DT, tid);
-      else update_tile<DK, NT, W>(sm, sm + L::oS, sm + L::oZ, tile * L::DT, tid);
+      if constexpr (L::SG) {
+        // the next tile's rows: this chunk's next tile, else the first tile
+        // of the next chunk (this thread wrote them itself)
+        const int pf = tile + 1 < L::NTILE ? (tile + 1) * L::DT : (t0 + L::C < t_end ? 0 : -1);
+        update_tile_sg<DK, NT, W>(sm, S, z, tile * L::DT, pf, srow, tid);
+      } else {
+        update_tile<DK, NT, W>(sm, sm + L::oS, sm + L::oZ, tile * L::DT, tid);
+      }
       __syncthreads();
     }
   }
