@@ -82,3 +82,31 @@ def test_noalloc_caps_its_plan_at_the_static_scratch(T):
     T.sync_status()
     assert _rel(out_b, out_a) <= 2e-2
     assert _rel(st_b, st_a) <= 1e-4
+
+
+def test_noalloc_order5_in_place(T):
+    """n = 5 (4,845 features, 1.26 MB of state per head): tsa_prefill's plan
+    takes several spans whose slots need far more than the 16 MiB array, so
+    the no-alloc call plans fewer (down to one span, whose CTA updates the
+    caller's state in place) and must give the same results, from zero and
+    continuing a prefix."""
+    from fixed_state_recurrence_phi_b300.inputs import torch_qkv
+    cfg = T.Config(1, 8, 16, 64, 5, "f32")
+    N = 640
+    assert T.prefill_plan(cfg, N)["scratch_bytes"] > 16 << 20
+    q, k, v = torch_qkv(1, 8, N, 16, 64, "f32", 31, device="cuda")
+    for acc in (False, True):
+        st0 = T.new_states(cfg)
+        if acc:
+            q0, k0, v0 = torch_qkv(1, 8, 100, 16, 64, "f32", 32, device="cuda")
+            T.prefill(cfg, 100, q0, k0, v0, torch.empty_like(v0), st0)
+        ref_out = torch.empty((1, 8, N, 64), device="cuda")
+        ref_st = st0.clone()
+        T.prefill(cfg, N, q, k, v, ref_out, ref_st, accumulate=acc)
+        out = torch.full_like(ref_out, float("nan"))
+        st = st0.clone()
+        T.prefill_noalloc(cfg, N, q, k, v, out, st, accumulate=acc)
+        T.sync_status()
+        for h in range(8):
+            assert _rel(out[0, h], ref_out[0, h]) <= 1e-4, (acc, h)
+        assert _rel(st, ref_st) <= 1e-4, acc
